@@ -1,0 +1,234 @@
+"""Float64 CPU oracle for the Siddon projector pair -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+legs of ``bench.py`` may import this package.  The product library never loads
+it, and it never loads the product library: the two share no code; both are
+fed from :mod:`ctp_inputs`.
+
+The arithmetic lives in ``siddon_oracle.c`` (plain C, float64, OpenMP over rays
+or over owned bands of cells).  This module compiles it with gcc on first use
+(or via :func:`build`) and wraps it with ctypes.
+
+Functions and what pins them (the tests under ``tests/test_oracle_*.py``):
+
+* :func:`forward` / :func:`backward` -- textbook parametric Siddon path sum and
+  its transpose.  Pinned by chord-length closed forms (uniform boxes, balls),
+  the brute-force clip-every-cell path, the supersampled line integral, the
+  textbook axis-aligned and diagonal cases, and the float64 adjoint identity.
+* :func:`brute_forward`, :func:`brute_count` -- O(cells) per ray; pinned by the
+  same closed forms.
+* :func:`backward_voxels` -- voxel-driven transpose at chosen voxels; pinned by
+  equality with :func:`backward` on small cases.
+* :func:`segment_count` -- positive-length pieces; pinned by :func:`brute_count`.
+* :func:`ambiguous` -- rays lying on a cell-face plane; pinned on hand-built rays.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "siddon_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "libctp_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (float64, no fast-math, no FP contraction)."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
+           "-shared", "-fPIC", "-Wall", "-Wextra", "-Wno-unused-parameter",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Ctx(ctypes.Structure):
+    _fields_ = [
+        ("beam", ctypes.c_int), ("n_views", ctypes.c_int), ("n_u", ctypes.c_int),
+        ("n_v", ctypes.c_int),
+        ("src", ctypes.c_void_p), ("det_centre", ctypes.c_void_p),
+        ("det_u", ctypes.c_void_p), ("det_v", ctypes.c_void_p),
+        ("pitch_u", ctypes.c_double), ("pitch_v", ctypes.c_double),
+        ("offset_u", ctypes.c_double), ("offset_v", ctypes.c_double),
+        ("n", ctypes.c_int * 3), ("pad_", ctypes.c_int),
+        ("d", ctypes.c_double * 3), ("o", ctypes.c_double * 3),
+    ]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P, L, I, D = ctypes.c_void_p, ctypes.c_long, ctypes.c_int, ctypes.c_double
+            C = ctypes.POINTER(_Ctx)
+            sigs = {
+                "ora_forward": [C, P, P, L, L, I],
+                "ora_forward_rays": [C, P, P, L, P, I],
+                "ora_backward": [C, P, P, L, L, I],
+                "ora_segment_count": [C, L, L, I, P],
+                "ora_brute_forward": [C, P, P, I],
+                "ora_brute_count": [C, P, I],
+                "ora_backward_voxels": [C, P, P, L, P, I],
+                "ora_ambiguous": [C, D, P, I],
+                "ora_supersampled": [C, P, P, L, L, P, I],
+            }
+            for name, args in sigs.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+class Scan:
+    """A scan in the oracle's terms: geometry arrays (float32, (n_views, 3)) and
+    the volume grid.  ``shape`` is (D, H, W), ``spacing`` (dz, dy, dx), ``origin``
+    the world (x, y, z) of the min corner of voxel (0, 0, 0)."""
+
+    def __init__(self, beam, src, det_centre, det_u, det_v, n_u, n_v, pitch_u, pitch_v,
+                 shape, spacing, origin, offset_u=0.0, offset_v=0.0):
+        self.beam = beam
+        self.arrays = [np.ascontiguousarray(a, dtype=np.float32).reshape(-1, 3)
+                       for a in (src, det_centre, det_u, det_v)]
+        self.n_views = self.arrays[0].shape[0]
+        self.n_u, self.n_v = int(n_u), int(n_v)
+        self.shape = tuple(int(s) for s in shape)
+        self.spacing = tuple(float(s) for s in spacing)
+        self.origin = tuple(float(s) for s in origin)
+        c = _Ctx()
+        c.beam = 1 if beam == "divergent" else 0
+        c.n_views, c.n_u, c.n_v = self.n_views, self.n_u, self.n_v
+        c.src, c.det_centre, c.det_u, c.det_v = (a.ctypes.data for a in self.arrays)
+        c.pitch_u, c.pitch_v = float(pitch_u), float(pitch_v)
+        c.offset_u, c.offset_v = float(offset_u), float(offset_v)
+        D, H, W = self.shape
+        dz, dy, dx = self.spacing
+        c.n[0], c.n[1], c.n[2] = W, H, D
+        c.d[0], c.d[1], c.d[2] = dx, dy, dz
+        c.o[0], c.o[1], c.o[2] = self.origin
+        self._ctx = c
+
+    @classmethod
+    def from_workload(cls, w, frames):
+        return cls(w.beam, frames["src"], frames["det_centre"], frames["det_u"],
+                   frames["det_v"], w.n_u, w.n_v, w.pitch_u, w.pitch_v, w.shape,
+                   w.spacing, w.origin, w.offset_u, w.offset_v)
+
+    @property
+    def n_rays(self):
+        return self.n_views * self.n_u * self.n_v
+
+    @property
+    def sino_shape(self):
+        return (self.n_views, self.n_v, self.n_u)
+
+    def ref(self):
+        return ctypes.byref(self._ctx)
+
+
+def _f32(a, shape=None):
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    if shape is not None and a.size != int(np.prod(shape)):
+        raise ValueError(f"expected {shape}, got {a.shape}")
+    return a
+
+
+def _check(code, name):
+    if code != 0:
+        raise MemoryError(f"{name} failed ({code})")
+
+
+def forward(scan: Scan, vol, ray0=0, ray1=None, threads=0):
+    """Float64 forward projection of rays [ray0, ray1) (default: all), as (n_rays,)."""
+    vol = _f32(vol, scan.shape)
+    ray1 = scan.n_rays if ray1 is None else ray1
+    out = np.zeros(ray1 - ray0, dtype=np.float64)
+    _check(_load().ora_forward(scan.ref(), vol.ctypes.data, out.ctypes.data, ray0, ray1,
+                               threads), "ora_forward")
+    if ray0 == 0 and ray1 == scan.n_rays:
+        return out.reshape(scan.sino_shape)
+    return out
+
+
+def forward_rays(scan: Scan, vol, rays, threads=0):
+    vol = _f32(vol, scan.shape)
+    rays = np.ascontiguousarray(rays, dtype=np.int64)
+    out = np.zeros(rays.size, dtype=np.float64)
+    _check(_load().ora_forward_rays(scan.ref(), vol.ctypes.data, rays.ctypes.data, rays.size,
+                                    out.ctypes.data, threads), "ora_forward_rays")
+    return out
+
+
+def backward(scan: Scan, sino, ray0=0, ray1=None, threads=0):
+    """Float64 backprojection of the rays [ray0, ray1) with values ``sino``
+    (length ray1 - ray0), as a (D, H, W) float64 volume."""
+    ray1 = scan.n_rays if ray1 is None else ray1
+    sino = _f32(sino, (ray1 - ray0,))
+    out = np.zeros(scan.shape, dtype=np.float64)
+    _check(_load().ora_backward(scan.ref(), sino.ctypes.data, out.ctypes.data, ray0, ray1,
+                                threads), "ora_backward")
+    return out
+
+
+def backward_voxels(scan: Scan, sino, voxels, threads=0):
+    sino = _f32(sino, scan.sino_shape)
+    voxels = np.ascontiguousarray(voxels, dtype=np.int64)
+    out = np.zeros(voxels.size, dtype=np.float64)
+    _check(_load().ora_backward_voxels(scan.ref(), sino.ctypes.data, voxels.ctypes.data,
+                                       voxels.size, out.ctypes.data, threads),
+           "ora_backward_voxels")
+    return out
+
+
+def segment_count(scan: Scan, ray0=0, ray1=None, threads=0) -> int:
+    ray1 = scan.n_rays if ray1 is None else ray1
+    out = ctypes.c_ulonglong(0)
+    _check(_load().ora_segment_count(scan.ref(), ray0, ray1, threads, ctypes.byref(out)),
+           "ora_segment_count")
+    return int(out.value)
+
+
+def brute_forward(scan: Scan, vol, threads=0):
+    vol = _f32(vol, scan.shape)
+    out = np.zeros(scan.n_rays, dtype=np.float64)
+    _check(_load().ora_brute_forward(scan.ref(), vol.ctypes.data, out.ctypes.data, threads),
+           "ora_brute_forward")
+    return out.reshape(scan.sino_shape)
+
+
+def brute_count(scan: Scan, threads=0) -> int:
+    out = ctypes.c_ulonglong(0)
+    _check(_load().ora_brute_count(scan.ref(), ctypes.byref(out), threads), "ora_brute_count")
+    return int(out.value)
+
+
+def ambiguous(scan: Scan, tol=1e-6, threads=0):
+    """Boolean (n_views, n_v, n_u): rays lying (numerically) in a cell-face plane."""
+    out = np.zeros(scan.n_rays, dtype=np.uint8)
+    _check(_load().ora_ambiguous(scan.ref(), float(tol), out.ctypes.data, threads),
+           "ora_ambiguous")
+    return out.reshape(scan.sino_shape).astype(bool)
+
+
+def supersampled(scan: Scan, vol, rays, samples, threads=0):
+    vol = _f32(vol, scan.shape)
+    rays = np.ascontiguousarray(rays, dtype=np.int64)
+    out = np.zeros(rays.size, dtype=np.float64)
+    _check(_load().ora_supersampled(scan.ref(), vol.ctypes.data, rays.ctypes.data, rays.size,
+                                    int(samples), out.ctypes.data, threads),
+           "ora_supersampled")
+    return out

@@ -1,0 +1,600 @@
+/*
+ * Float64 CPU oracle for the ray-driven Siddon projector pair.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code, header
+ * or constant with the CUDA library; both are fed from the seeded input
+ * generators only.
+ *
+ * What it computes (diffct release pages, my.diffend.io):
+ *   - forward: p(R) = sum over cells of |R n cell| * f(cell), the exact line
+ *     integral of the cell-constant image ("exact adjoint pair for the
+ *     cell-constant Siddon model", diffct 2.1.0 -> 2.2.1, README "Matched
+ *     operators"; "Siddon path sum; matched adjoint", diffct 2.4.1 -> 2.4.2,
+ *     docs/video/README.md, shot "Autograd");
+ *   - backward: g(cell) = sum over rays of |R n cell| * y(R), the transpose;
+ *   - lengths in physical units with per-axis spacing (diffct 2.4.3 -> 2.4.4,
+ *     CHANGELOG 2.4.4 "Added": per-axis voxel spacing, physical length units).
+ *
+ * Method: the textbook parametric Siddon traversal in float64 -- clip the ray to
+ * the box, merge the plane-crossing parameters of the three axes, and give each
+ * positive-length piece to the cell that contains its midpoint.  A second,
+ * independent brute-force path clips the ray against every cell's box.  A third
+ * path (voxel-driven) evaluates the transpose at chosen voxels by clipping every
+ * candidate ray of every view against that voxel's box.
+ *
+ * Readings where the pages are silent:
+ *   - pixel centre: det_centre + (iu - (n_u-1)/2 + offset_u) * pitch_u * u
+ *                              + (iv - (n_v-1)/2 + offset_v) * pitch_v * v;
+ *   - divergent ray: the segment source -> pixel centre (t in [0, 1]);
+ *     parallel ray: the full line through the pixel centre along src (t free);
+ *   - cell (i, j, k) is [o + i d, o + (i+1) d) per axis; a ray lying exactly in a
+ *     face plane belongs to the cell on the + side of that plane.
+ * Every floating-point value is a double; inputs are float32 promoted exactly.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+    int beam;            /* 0 = parallel, 1 = divergent (fan / cone) */
+    int n_views, n_u, n_v;
+    const float *src;    /* (n_views, 3): source, or unit ray direction (parallel) */
+    const float *det_centre;
+    const float *det_u;
+    const float *det_v;
+    double pitch_u, pitch_v, offset_u, offset_v;
+    int n[3];            /* cells along x, y, z */
+    int pad_;
+    double d[3];         /* spacing along x, y, z */
+    double o[3];         /* world position of the min corner of cell (0, 0, 0) */
+} ora_ctx;
+
+static int ora_threads(int requested)
+{
+#ifdef _OPENMP
+    if (requested > 0) return requested;
+    return omp_get_max_threads();
+#else
+    (void)requested;
+    return 1;
+#endif
+}
+
+/* The ray of detector sample `ray` (view-major, then v, then u). */
+static void ora_ray(const ora_ctx *c, long ray, double X0[3], double r[3],
+                    double *tlo, double *thi)
+{
+    long per_view = (long)c->n_u * c->n_v;
+    long view = ray / per_view;
+    long pix = ray % per_view;
+    long iv = pix / c->n_u, iu = pix % c->n_u;
+    double a = ((double)iu - 0.5 * (double)(c->n_u - 1) + c->offset_u) * c->pitch_u;
+    double b = ((double)iv - 0.5 * (double)(c->n_v - 1) + c->offset_v) * c->pitch_v;
+    const float *S = c->src + 3 * view, *C = c->det_centre + 3 * view;
+    const float *U = c->det_u + 3 * view, *V = c->det_v + 3 * view;
+    double P[3];
+    for (int ax = 0; ax < 3; ++ax)
+        P[ax] = (double)C[ax] + a * (double)U[ax] + b * (double)V[ax];
+    if (c->beam == 1) {
+        for (int ax = 0; ax < 3; ++ax) {
+            X0[ax] = (double)S[ax];
+            r[ax] = P[ax] - (double)S[ax];
+        }
+        *tlo = 0.0;
+        *thi = 1.0;
+    } else {
+        for (int ax = 0; ax < 3; ++ax) {
+            X0[ax] = P[ax];
+            r[ax] = (double)S[ax];
+        }
+        *tlo = -INFINITY;
+        *thi = INFINITY;
+    }
+}
+
+static double ora_norm(const double r[3])
+{
+    return sqrt(r[0] * r[0] + r[1] * r[1] + r[2] * r[2]);
+}
+
+/* Parameter interval of the line X0 + t r inside the cell box [lo, hi) (in cell
+ * indices), intersected with [tlo, thi].  Returns 0 when empty. */
+static int ora_clip_cells(const ora_ctx *c, const double X0[3], const double r[3],
+                          double tlo, double thi, const int lo[3], const int hi[3],
+                          double *amin, double *amax)
+{
+    double a0 = tlo, a1 = thi;
+    for (int ax = 0; ax < 3; ++ax) {
+        double p0 = c->o[ax] + (double)lo[ax] * c->d[ax];
+        double p1 = c->o[ax] + (double)hi[ax] * c->d[ax];
+        if (r[ax] == 0.0) {
+            if (!(X0[ax] >= p0 && X0[ax] < p1)) return 0;
+        } else {
+            double t0 = (p0 - X0[ax]) / r[ax], t1 = (p1 - X0[ax]) / r[ax];
+            a0 = fmax(a0, fmin(t0, t1));
+            a1 = fmin(a1, fmax(t0, t1));
+        }
+    }
+    *amin = a0;
+    *amax = a1;
+    return a0 < a1;
+}
+
+/*
+ * Siddon traversal of one ray inside the cell box [lo, hi).  Writes the linear
+ * cell index ((k * ny + j) * nx + i) and the physical length of every
+ * positive-length piece; returns the number of pieces.  `buf` must hold
+ * (hi-lo summed over axes) + 6 doubles; cells/lens the same count.
+ */
+static int ora_trace(const ora_ctx *c, const double X0[3], const double r[3],
+                     double tlo, double thi, const int lo[3], const int hi[3],
+                     double *buf, long *cells, double *lens)
+{
+    double amin, amax;
+    if (!ora_clip_cells(c, X0, r, tlo, thi, lo, hi, &amin, &amax)) return 0;
+
+    /* Per-axis crossing parameters strictly inside (amin, amax), each in
+     * increasing order, then a three-way merge. */
+    double *seq[3];
+    int len[3], pos[3];
+    double *next = buf;
+    for (int ax = 0; ax < 3; ++ax) {
+        seq[ax] = next;
+        len[ax] = 0;
+        pos[ax] = 0;
+        if (r[ax] == 0.0) continue;
+        int count = hi[ax] - lo[ax] + 1;
+        for (int m = 0; m < count; ++m) {
+            int k = r[ax] > 0.0 ? lo[ax] + m : hi[ax] - m;
+            double t = (c->o[ax] + (double)k * c->d[ax] - X0[ax]) / r[ax];
+            if (t > amin && t < amax) seq[ax][len[ax]++] = t;
+        }
+        next += len[ax];
+    }
+    double norm = ora_norm(r);
+    double prev = amin;
+    int out = 0;
+    for (;;) {
+        double t = amax;
+        int which = -1;
+        for (int ax = 0; ax < 3; ++ax)
+            if (pos[ax] < len[ax] && seq[ax][pos[ax]] < t) {
+                t = seq[ax][pos[ax]];
+                which = ax;
+            }
+        if (t > prev) {
+            double mid = 0.5 * (prev + t);
+            long idx[3];
+            for (int ax = 0; ax < 3; ++ax) {
+                long q = (long)floor((X0[ax] + mid * r[ax] - c->o[ax]) / c->d[ax]);
+                if (q < lo[ax]) q = lo[ax];
+                if (q > hi[ax] - 1) q = hi[ax] - 1;
+                idx[ax] = q;
+            }
+            cells[out] = (idx[2] * c->n[1] + idx[1]) * c->n[0] + idx[0];
+            lens[out] = (t - prev) * norm;
+            ++out;
+            prev = t;
+        }
+        if (which < 0) break;
+        pos[which]++;
+    }
+    return out;
+}
+
+static long ora_n_rays(const ora_ctx *c)
+{
+    return (long)c->n_views * c->n_u * c->n_v;
+}
+
+static int ora_buf_len(const ora_ctx *c)
+{
+    return c->n[0] + c->n[1] + c->n[2] + 8;
+}
+
+/* Forward projection of rays [ray0, ray1): sino[ray - ray0] = sum len * vol. */
+int ora_forward(const ora_ctx *c, const float *vol, double *sino, long ray0, long ray1,
+                int nthreads)
+{
+    int T = ora_threads(nthreads);
+    int B = ora_buf_len(c);
+    int err = 0;
+#pragma omp parallel num_threads(T)
+    {
+        double *buf = (double *)malloc(sizeof(double) * B);
+        long *cells = (long *)malloc(sizeof(long) * B);
+        double *lens = (double *)malloc(sizeof(double) * B);
+        if (!buf || !cells || !lens) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+            int lo[3] = {0, 0, 0};
+#pragma omp for schedule(dynamic, 64)
+            for (long ray = ray0; ray < ray1; ++ray) {
+                double X0[3], r[3], tlo, thi;
+                ora_ray(c, ray, X0, r, &tlo, &thi);
+                int n = ora_trace(c, X0, r, tlo, thi, lo, c->n, buf, cells, lens);
+                double acc = 0.0;
+                for (int s = 0; s < n; ++s) acc += lens[s] * (double)vol[cells[s]];
+                sino[ray - ray0] = acc;
+            }
+        }
+        free(buf);
+        free(cells);
+        free(lens);
+    }
+    return err;
+}
+
+/* Forward projection of an explicit list of rays. */
+int ora_forward_rays(const ora_ctx *c, const float *vol, const long *rays, long count,
+                     double *out, int nthreads)
+{
+    int T = ora_threads(nthreads);
+    int B = ora_buf_len(c);
+    int err = 0;
+#pragma omp parallel num_threads(T)
+    {
+        double *buf = (double *)malloc(sizeof(double) * B);
+        long *cells = (long *)malloc(sizeof(long) * B);
+        double *lens = (double *)malloc(sizeof(double) * B);
+        if (!buf || !cells || !lens) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+            int lo[3] = {0, 0, 0};
+#pragma omp for schedule(dynamic, 16)
+            for (long q = 0; q < count; ++q) {
+                double X0[3], r[3], tlo, thi;
+                ora_ray(c, rays[q], X0, r, &tlo, &thi);
+                int n = ora_trace(c, X0, r, tlo, thi, lo, c->n, buf, cells, lens);
+                double acc = 0.0;
+                for (int s = 0; s < n; ++s) acc += lens[s] * (double)vol[cells[s]];
+                out[q] = acc;
+            }
+        }
+        free(buf);
+        free(cells);
+        free(lens);
+    }
+    return err;
+}
+
+/*
+ * Backprojection (transpose) of rays [ray0, ray1) into vol (zeroed first).
+ * Deterministic without atomics: each thread owns a band of cells along one
+ * axis (z when there are enough z cells, else y) and walks every ray clipped
+ * to its band.  sino is indexed by ray - ray0.
+ */
+int ora_backward(const ora_ctx *c, const float *sino, double *vol, long ray0, long ray1,
+                 int nthreads)
+{
+    int T = ora_threads(nthreads);
+    int B = ora_buf_len(c);
+    long nvox = (long)c->n[0] * c->n[1] * c->n[2];
+    memset(vol, 0, sizeof(double) * nvox);
+    int own = c->n[2] >= T ? 2 : (c->n[1] >= T ? 1 : 0);
+    int bands = c->n[own] < T ? c->n[own] : T;
+    int err = 0;
+#pragma omp parallel num_threads(bands)
+    {
+        int t = 0;
+#ifdef _OPENMP
+        t = omp_get_thread_num();
+#endif
+        double *buf = (double *)malloc(sizeof(double) * B);
+        long *cells = (long *)malloc(sizeof(long) * B);
+        double *lens = (double *)malloc(sizeof(double) * B);
+        if (!buf || !cells || !lens) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+            int lo[3] = {0, 0, 0}, hi[3] = {c->n[0], c->n[1], c->n[2]};
+            lo[own] = (int)((long)c->n[own] * t / bands);
+            hi[own] = (int)((long)c->n[own] * (t + 1) / bands);
+            for (long ray = ray0; ray < ray1 && hi[own] > lo[own]; ++ray) {
+                double y = (double)sino[ray - ray0];
+                double X0[3], r[3], tlo, thi;
+                ora_ray(c, ray, X0, r, &tlo, &thi);
+                int n = ora_trace(c, X0, r, tlo, thi, lo, hi, buf, cells, lens);
+                for (int s = 0; s < n; ++s) vol[cells[s]] += lens[s] * y;
+            }
+        }
+        free(buf);
+        free(cells);
+        free(lens);
+    }
+    return err;
+}
+
+/* Number of positive-length (ray, cell) pieces over rays [ray0, ray1). */
+int ora_segment_count(const ora_ctx *c, long ray0, long ray1, int nthreads,
+                      unsigned long long *out)
+{
+    int T = ora_threads(nthreads);
+    int B = ora_buf_len(c);
+    unsigned long long total = 0;
+    int err = 0;
+#pragma omp parallel num_threads(T) reduction(+ : total)
+    {
+        double *buf = (double *)malloc(sizeof(double) * B);
+        long *cells = (long *)malloc(sizeof(long) * B);
+        double *lens = (double *)malloc(sizeof(double) * B);
+        if (!buf || !cells || !lens) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+            int lo[3] = {0, 0, 0};
+#pragma omp for schedule(dynamic, 256)
+            for (long ray = ray0; ray < ray1; ++ray) {
+                double X0[3], r[3], tlo, thi;
+                ora_ray(c, ray, X0, r, &tlo, &thi);
+                total += (unsigned long long)ora_trace(c, X0, r, tlo, thi, lo, c->n, buf,
+                                                       cells, lens);
+            }
+        }
+        free(buf);
+        free(cells);
+        free(lens);
+    }
+    *out = total;
+    return err;
+}
+
+/* Length of the line X0 + t r, t in [tlo, thi], inside the box [blo, bhi)
+ * (half-open in the sense of the face-plane rule above). */
+static double ora_clip_box(const double X0[3], const double r[3], double tlo, double thi,
+                           const double blo[3], const double bhi[3])
+{
+    double a0 = tlo, a1 = thi;
+    for (int ax = 0; ax < 3; ++ax) {
+        if (r[ax] == 0.0) {
+            if (!(X0[ax] >= blo[ax] && X0[ax] < bhi[ax])) return 0.0;
+        } else {
+            double t0 = (blo[ax] - X0[ax]) / r[ax], t1 = (bhi[ax] - X0[ax]) / r[ax];
+            a0 = fmax(a0, fmin(t0, t1));
+            a1 = fmin(a1, fmax(t0, t1));
+        }
+    }
+    return a1 > a0 ? (a1 - a0) * ora_norm(r) : 0.0;
+}
+
+static void ora_cell_box(const ora_ctx *c, long i, long j, long k, double blo[3], double bhi[3])
+{
+    long idx[3] = {i, j, k};
+    for (int ax = 0; ax < 3; ++ax) {
+        blo[ax] = c->o[ax] + (double)idx[ax] * c->d[ax];
+        bhi[ax] = c->o[ax] + (double)(idx[ax] + 1) * c->d[ax];
+    }
+}
+
+/* Brute force forward: every ray clipped against every cell box.  O(cells) per
+ * ray; tiny volumes only.  Shares no traversal logic with ora_trace. */
+int ora_brute_forward(const ora_ctx *c, const float *vol, double *sino, int nthreads)
+{
+    int T = ora_threads(nthreads);
+    long nr = ora_n_rays(c);
+#pragma omp parallel for num_threads(T) schedule(dynamic, 16)
+    for (long ray = 0; ray < nr; ++ray) {
+        double X0[3], r[3], tlo, thi;
+        ora_ray(c, ray, X0, r, &tlo, &thi);
+        double acc = 0.0;
+        for (long k = 0; k < c->n[2]; ++k)
+            for (long j = 0; j < c->n[1]; ++j)
+                for (long i = 0; i < c->n[0]; ++i) {
+                    double blo[3], bhi[3];
+                    ora_cell_box(c, i, j, k, blo, bhi);
+                    double L = ora_clip_box(X0, r, tlo, thi, blo, bhi);
+                    if (L > 0.0) acc += L * (double)vol[(k * c->n[1] + j) * c->n[0] + i];
+                }
+        sino[ray] = acc;
+    }
+    return 0;
+}
+
+/* Brute-force segment count: cells with positive clipped length, per ray. */
+int ora_brute_count(const ora_ctx *c, unsigned long long *out, int nthreads)
+{
+    int T = ora_threads(nthreads);
+    long nr = ora_n_rays(c);
+    unsigned long long total = 0;
+#pragma omp parallel for num_threads(T) schedule(dynamic, 16) reduction(+ : total)
+    for (long ray = 0; ray < nr; ++ray) {
+        double X0[3], r[3], tlo, thi;
+        ora_ray(c, ray, X0, r, &tlo, &thi);
+        for (long k = 0; k < c->n[2]; ++k)
+            for (long j = 0; j < c->n[1]; ++j)
+                for (long i = 0; i < c->n[0]; ++i) {
+                    double blo[3], bhi[3];
+                    ora_cell_box(c, i, j, k, blo, bhi);
+                    if (ora_clip_box(X0, r, tlo, thi, blo, bhi) > 0.0) total++;
+                }
+    }
+    *out = total;
+    return 0;
+}
+
+/* Solve the 3x3 system M x = rhs (columns m0, m1, m2) by Cramer's rule. */
+static int ora_solve3(const double m0[3], const double m1[3], const double m2[3],
+                      const double rhs[3], double x[3])
+{
+    double det = m0[0] * (m1[1] * m2[2] - m1[2] * m2[1])
+               - m1[0] * (m0[1] * m2[2] - m0[2] * m2[1])
+               + m2[0] * (m0[1] * m1[2] - m0[2] * m1[1]);
+    if (!(fabs(det) > 0.0)) return 0;
+    double d0 = rhs[0] * (m1[1] * m2[2] - m1[2] * m2[1])
+              - m1[0] * (rhs[1] * m2[2] - rhs[2] * m2[1])
+              + m2[0] * (rhs[1] * m1[2] - rhs[2] * m1[1]);
+    double d1 = m0[0] * (rhs[1] * m2[2] - rhs[2] * m2[1])
+              - rhs[0] * (m0[1] * m2[2] - m0[2] * m2[1])
+              + m2[0] * (m0[1] * rhs[2] - m0[2] * rhs[1]);
+    double d2 = m0[0] * (m1[1] * rhs[2] - m1[2] * rhs[1])
+              - m1[0] * (m0[1] * rhs[2] - m0[2] * rhs[1])
+              + rhs[0] * (m0[1] * m1[2] - m0[2] * m1[1]);
+    x[0] = d0 / det;
+    x[1] = d1 / det;
+    x[2] = d2 / det;
+    return 1;
+}
+
+/*
+ * Voxel-driven transpose at chosen voxels: out[q] = sum over every ray of
+ * |ray n box(voxel q)| * sino(ray).  For each view the voxel's 8 corners are
+ * projected onto the detector plane to bound the candidate pixels (with one
+ * pixel of margin); every candidate ray is clipped against the voxel box.
+ * voxels[q] is the linear index (k * ny + j) * nx + i.
+ */
+int ora_backward_voxels(const ora_ctx *c, const float *sino, const long *voxels, long count,
+                        double *out, int nthreads)
+{
+    int T = ora_threads(nthreads);
+#pragma omp parallel for num_threads(T) schedule(dynamic, 1)
+    for (long q = 0; q < count; ++q) {
+        long v = voxels[q];
+        long i = v % c->n[0], j = (v / c->n[0]) % c->n[1], k = v / ((long)c->n[0] * c->n[1]);
+        double blo[3], bhi[3];
+        ora_cell_box(c, i, j, k, blo, bhi);
+        double acc = 0.0;
+        for (long view = 0; view < c->n_views; ++view) {
+            const float *S = c->src + 3 * view, *C = c->det_centre + 3 * view;
+            const float *U = c->det_u + 3 * view, *V = c->det_v + 3 * view;
+            double Ud[3], Vd[3], Sd[3], Cd[3];
+            for (int ax = 0; ax < 3; ++ax) {
+                Ud[ax] = U[ax];
+                Vd[ax] = V[ax];
+                Sd[ax] = S[ax];
+                Cd[ax] = C[ax];
+            }
+            double umin = INFINITY, umax = -INFINITY, vmin = INFINITY, vmax = -INFINITY;
+            int full = 0;
+            for (int corner = 0; corner < 8 && !full; ++corner) {
+                double X[3] = {(corner & 1) ? bhi[0] : blo[0], (corner & 2) ? bhi[1] : blo[1],
+                               (corner & 4) ? bhi[2] : blo[2]};
+                double m2[3], rhs[3], sol[3];
+                for (int ax = 0; ax < 3; ++ax) {
+                    if (c->beam == 1) {
+                        m2[ax] = -(X[ax] - Sd[ax]);
+                        rhs[ax] = Sd[ax] - Cd[ax];
+                    } else {
+                        m2[ax] = -Sd[ax];
+                        rhs[ax] = X[ax] - Cd[ax];
+                    }
+                }
+                if (!ora_solve3(Ud, Vd, m2, rhs, sol) || (c->beam == 1 && !(sol[2] > 0.0))) {
+                    full = 1;
+                    break;
+                }
+                double iu = sol[0] / c->pitch_u + 0.5 * (c->n_u - 1) - c->offset_u;
+                double iv = sol[1] / c->pitch_v + 0.5 * (c->n_v - 1) - c->offset_v;
+                umin = fmin(umin, iu);
+                umax = fmax(umax, iu);
+                vmin = fmin(vmin, iv);
+                vmax = fmax(vmax, iv);
+            }
+            long u0 = 0, u1 = c->n_u - 1, v0 = 0, v1 = c->n_v - 1;
+            if (!full) {
+                u0 = (long)floor(umin) - 1;
+                u1 = (long)ceil(umax) + 1;
+                v0 = (long)floor(vmin) - 1;
+                v1 = (long)ceil(vmax) + 1;
+                if (u0 < 0) u0 = 0;
+                if (v0 < 0) v0 = 0;
+                if (u1 > c->n_u - 1) u1 = c->n_u - 1;
+                if (v1 > c->n_v - 1) v1 = c->n_v - 1;
+            }
+            for (long iv = v0; iv <= v1; ++iv)
+                for (long iu = u0; iu <= u1; ++iu) {
+                    long ray = (view * c->n_v + iv) * c->n_u + iu;
+                    double X0[3], r[3], tlo, thi;
+                    ora_ray(c, ray, X0, r, &tlo, &thi);
+                    double L = ora_clip_box(X0, r, tlo, thi, blo, bhi);
+                    if (L > 0.0) acc += L * (double)sino[ray];
+                }
+        }
+        out[q] = acc;
+    }
+    return 0;
+}
+
+/*
+ * Face-plane ambiguity flag per ray: 1 when, over its chord through the closed
+ * volume box, the ray stays within tol * d of one cell-face plane of some axis
+ * (it lies in, or numerically on, a face, where the two neighbouring cells
+ * both contain it).  Such rays are assigned by the + side rule above, which any
+ * other finite-precision traversal can only reproduce up to rounding.
+ */
+int ora_ambiguous(const ora_ctx *c, double tol, unsigned char *flags, int nthreads)
+{
+    int T = ora_threads(nthreads);
+    long nr = ora_n_rays(c);
+#pragma omp parallel for num_threads(T) schedule(dynamic, 256)
+    for (long ray = 0; ray < nr; ++ray) {
+        double X0[3], r[3], tlo, thi;
+        ora_ray(c, ray, X0, r, &tlo, &thi);
+        double a0 = tlo, a1 = thi;
+        int miss = 0;
+        for (int ax = 0; ax < 3; ++ax) {
+            double p0 = c->o[ax], p1 = c->o[ax] + (double)c->n[ax] * c->d[ax];
+            double slack = tol * c->d[ax];
+            if (r[ax] == 0.0) {
+                if (X0[ax] < p0 - slack || X0[ax] > p1 + slack) miss = 1;
+            } else {
+                double t0 = (p0 - slack - X0[ax]) / r[ax], t1 = (p1 + slack - X0[ax]) / r[ax];
+                a0 = fmax(a0, fmin(t0, t1));
+                a1 = fmin(a1, fmax(t0, t1));
+            }
+        }
+        unsigned char flag = 0;
+        if (!miss && a0 <= a1) {
+            for (int ax = 0; ax < 3 && !flag; ++ax) {
+                double e0 = X0[ax] + (r[ax] == 0.0 ? 0.0 : a0 * r[ax]);
+                double e1 = X0[ax] + (r[ax] == 0.0 ? 0.0 : a1 * r[ax]);
+                double slack = tol * c->d[ax];
+                if (fabs(e1 - e0) > slack) continue;
+                double q = (0.5 * (e0 + e1) - c->o[ax]) / c->d[ax];
+                double nearest = floor(q + 0.5);
+                if (nearest >= 0.0 && nearest <= (double)c->n[ax] &&
+                    fabs(q - nearest) * c->d[ax] <= slack)
+                    flag = 1;
+            }
+        }
+        flags[ray] = flag;
+    }
+    return 0;
+}
+
+/* Midpoint-rule line integral with M samples along the chord through the
+ * volume (nearest-cell lookup), for convergence checks of ora_forward. */
+int ora_supersampled(const ora_ctx *c, const float *vol, const long *rays, long count,
+                     long M, double *out, int nthreads)
+{
+    int T = ora_threads(nthreads);
+#pragma omp parallel for num_threads(T) schedule(dynamic, 1)
+    for (long q = 0; q < count; ++q) {
+        double X0[3], r[3], tlo, thi, amin, amax;
+        int lo[3] = {0, 0, 0};
+        ora_ray(c, rays[q], X0, r, &tlo, &thi);
+        double acc = 0.0;
+        if (ora_clip_cells(c, X0, r, tlo, thi, lo, c->n, &amin, &amax)) {
+            double h = (amax - amin) / (double)M;
+            for (long m = 0; m < M; ++m) {
+                double t = amin + ((double)m + 0.5) * h;
+                long idx[3];
+                int inside = 1;
+                for (int ax = 0; ax < 3; ++ax) {
+                    idx[ax] = (long)floor((X0[ax] + t * r[ax] - c->o[ax]) / c->d[ax]);
+                    if (idx[ax] < 0 || idx[ax] >= c->n[ax]) inside = 0;
+                }
+                if (inside) acc += (double)vol[(idx[2] * c->n[1] + idx[1]) * c->n[0] + idx[0]];
+            }
+            acc *= h * ora_norm(r);
+        }
+        out[q] = acc;
+    }
+    return 0;
+}
