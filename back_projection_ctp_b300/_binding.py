@@ -1,0 +1,261 @@
+"""Thin ctypes binding of the C ABI in ``include/ctp.h`` -- argument marshalling only.
+
+Every step of the projector runs in ``libctp.so`` (CUDA, sm_103a).  There is no
+CPU or PyTorch fallback: if the library cannot be loaded, importing the entry
+points raises.  PyTorch is used for device memory and streams only.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libctp.so")
+_lib = None
+_lock = threading.Lock()
+
+PATHS = {"auto": 0, "ray": 1, "column": 2}
+PATH_NAMES = {v: k for k, v in PATHS.items()}
+BEAMS = {"parallel": 0, "divergent": 1}
+
+
+class CtpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {ctp_status_string(status)} (status {status})")
+
+
+class _Geometry(ctypes.Structure):
+    _fields_ = [("ndim", ctypes.c_int), ("beam", ctypes.c_int), ("n_views", ctypes.c_int),
+                ("n_u", ctypes.c_int), ("n_v", ctypes.c_int),
+                ("src", ctypes.c_void_p), ("det_centre", ctypes.c_void_p),
+                ("det_u", ctypes.c_void_p), ("det_v", ctypes.c_void_p),
+                ("pitch_u", ctypes.c_float), ("pitch_v", ctypes.c_float),
+                ("offset_u", ctypes.c_float), ("offset_v", ctypes.c_float)]
+
+
+class _Volume(ctypes.Structure):
+    _fields_ = [("nx", ctypes.c_int), ("ny", ctypes.c_int), ("nz", ctypes.c_int),
+                ("dx", ctypes.c_double), ("dy", ctypes.c_double), ("dz", ctypes.c_double),
+                ("ox", ctypes.c_double), ("oy", ctypes.c_double), ("oz", ctypes.c_double)]
+
+
+class _PlanInfo(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("device", ctypes.c_int), ("n_rays", ctypes.c_longlong),
+                ("n_cells", ctypes.c_longlong), ("device_bytes", ctypes.c_ulonglong)]
+
+
+EXPORTS = ("ctp_plan", "ctp_destroy", "ctp_plan_info_get", "ctp_forward", "ctp_backward",
+           "ctp_segment_count", "ctp_forward_host", "ctp_backward_host", "ctp_status_string")
+
+
+def load_library(path: str | None = None):
+    """Load ``libctp.so`` (building it first when it is absent and nvcc exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib_path = path or _LIB_PATH
+        if not os.path.exists(lib_path):
+            from . import build as _build
+            _build.build()
+        lib = ctypes.CDLL(lib_path)
+        P, I = ctypes.c_void_p, ctypes.c_int
+        lib.ctp_plan.argtypes = [ctypes.POINTER(_Geometry), ctypes.POINTER(_Volume), I,
+                                 ctypes.POINTER(ctypes.c_void_p)]
+        lib.ctp_destroy.argtypes = [P]
+        lib.ctp_destroy.restype = None
+        lib.ctp_plan_info_get.argtypes = [P, ctypes.POINTER(_PlanInfo)]
+        for name in ("ctp_forward", "ctp_backward", "ctp_forward_host", "ctp_backward_host"):
+            getattr(lib, name).argtypes = [P, P, P, P]
+        lib.ctp_segment_count.argtypes = [P, ctypes.POINTER(ctypes.c_ulonglong), P]
+        lib.ctp_status_string.argtypes = [I]
+        lib.ctp_status_string.restype = ctypes.c_char_p
+        for name in EXPORTS:
+            if name not in ("ctp_destroy", "ctp_status_string"):
+                getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def ctp_status_string(status: int) -> str:
+    return load_library().ctp_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise CtpError(status, where)
+
+
+@dataclasses.dataclass
+class Geometry:
+    """Per-view frames (float32, (n_views, 3)) and detector description."""
+    ndim: int
+    beam: str
+    src: np.ndarray
+    det_centre: np.ndarray
+    det_u: np.ndarray
+    det_v: np.ndarray
+    n_u: int
+    n_v: int
+    pitch_u: float
+    pitch_v: float
+    offset_u: float = 0.0
+    offset_v: float = 0.0
+
+
+@dataclasses.dataclass
+class Volume:
+    """Grid in tensor order: shape (D, H, W), spacing (dz, dy, dx); origin is the
+    world (x, y, z) of the min corner of cell (0, 0, 0)."""
+    shape: tuple
+    spacing: tuple
+    origin: tuple
+
+
+class Plan:
+    """Owner of a ``ctp_plan_t``; destroyed with the object."""
+
+    def __init__(self, handle, geometry: Geometry, volume: Volume):
+        self._h = handle
+        self.geometry = geometry
+        self.volume = volume
+        info = _PlanInfo()
+        _check(load_library().ctp_plan_info_get(handle, ctypes.byref(info)), "ctp_plan_info_get")
+        self.path = PATH_NAMES[info.path]
+        self.device = info.device
+        self.n_rays = int(info.n_rays)
+        self.n_cells = int(info.n_cells)
+        self.device_bytes = int(info.device_bytes)
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("plan was destroyed")
+        return self._h
+
+    @property
+    def sino_shape(self):
+        g = self.geometry
+        return (g.src.shape[0], g.n_v, g.n_u)
+
+    @property
+    def vol_shape(self):
+        return tuple(self.volume.shape)
+
+    def destroy(self):
+        if self._h is not None and _lib is not None:
+            _lib.ctp_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def ctp_plan(geometry: Geometry, volume: Volume, path: str = "auto") -> Plan:
+    lib = load_library()
+    arrays = [np.ascontiguousarray(a, dtype=np.float32).reshape(-1, 3)
+              for a in (geometry.src, geometry.det_centre, geometry.det_u, geometry.det_v)]
+    n_views = arrays[0].shape[0]
+    if any(a.shape[0] != n_views for a in arrays):
+        raise ValueError("frame arrays must all have shape (n_views, 3)")
+    g = _Geometry()
+    g.ndim, g.beam, g.n_views = int(geometry.ndim), BEAMS[geometry.beam], n_views
+    g.n_u, g.n_v = int(geometry.n_u), int(geometry.n_v)
+    g.src, g.det_centre, g.det_u, g.det_v = (a.ctypes.data for a in arrays)
+    g.pitch_u, g.pitch_v = float(geometry.pitch_u), float(geometry.pitch_v)
+    g.offset_u, g.offset_v = float(geometry.offset_u), float(geometry.offset_v)
+    D, H, W = (int(s) for s in volume.shape)
+    dz, dy, dx = (float(s) for s in volume.spacing)
+    v = _Volume()
+    v.nx, v.ny, v.nz = W, H, D
+    v.dx, v.dy, v.dz = dx, dy, dz
+    v.ox, v.oy, v.oz = (float(s) for s in volume.origin)
+    h = ctypes.c_void_p()
+    _check(lib.ctp_plan(ctypes.byref(g), ctypes.byref(v), PATHS[path], ctypes.byref(h)),
+           "ctp_plan")
+    geometry = dataclasses.replace(geometry, src=arrays[0], det_centre=arrays[1],
+                                   det_u=arrays[2], det_v=arrays[3])
+    return Plan(h.value, geometry, volume)
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _device_f32(t, shape, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32:
+        raise TypeError(f"{name} must be a float32 CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() != int(np.prod(shape)):
+        raise ValueError(f"{name} must hold {shape} elements, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def ctp_forward(plan: Plan, vol, sino, stream=None):
+    """sino <- A vol (both float32 CUDA tensors; sino fully overwritten)."""
+    _check(load_library().ctp_forward(plan.handle, _device_f32(vol, plan.vol_shape, "vol"),
+                                      _device_f32(sino, plan.sino_shape, "sino"),
+                                      _stream_ptr(stream)), "ctp_forward")
+    return sino
+
+
+def ctp_backward(plan: Plan, sino, vol, stream=None):
+    """vol <- A^T sino (vol fully overwritten)."""
+    _check(load_library().ctp_backward(plan.handle, _device_f32(sino, plan.sino_shape, "sino"),
+                                       _device_f32(vol, plan.vol_shape, "vol"),
+                                       _stream_ptr(stream)), "ctp_backward")
+    return vol
+
+
+def ctp_segment_count(plan: Plan, stream=None) -> int:
+    out = ctypes.c_ulonglong(0)
+    _check(load_library().ctp_segment_count(plan.handle, ctypes.byref(out), _stream_ptr(stream)),
+           "ctp_segment_count")
+    return int(out.value)
+
+
+def _host_f32(a, shape, name, writable=False):
+    if not isinstance(a, np.ndarray) or a.dtype != np.float32 or not a.flags.c_contiguous:
+        raise TypeError(f"{name} must be a C-contiguous float32 numpy array")
+    if a.size != int(np.prod(shape)):
+        raise ValueError(f"{name} must hold {shape} elements")
+    if writable and not a.flags.writeable:
+        raise ValueError(f"{name} must be writable")
+    return a.ctypes.data
+
+
+def ctp_forward_host(plan: Plan, vol_host, sino_host, stream=None):
+    """End to end: host vol -> device -> A -> host sino (waits for the stream)."""
+    _check(load_library().ctp_forward_host(
+        plan.handle, _host_f32(vol_host, plan.vol_shape, "vol_host"),
+        _host_f32(sino_host, plan.sino_shape, "sino_host", True), _stream_ptr(stream)),
+        "ctp_forward_host")
+    return sino_host
+
+
+def ctp_backward_host(plan: Plan, sino_host, vol_host, stream=None):
+    _check(load_library().ctp_backward_host(
+        plan.handle, _host_f32(sino_host, plan.sino_shape, "sino_host"),
+        _host_f32(vol_host, plan.vol_shape, "vol_host", True), _stream_ptr(stream)),
+        "ctp_backward_host")
+    return vol_host
+
+
+def ctp_destroy(plan: Plan):
+    plan.destroy()

@@ -1,0 +1,418 @@
+// C ABI of the Siddon projector pair: validation, plans, launches.
+//
+// Host side of the boundary declared in include/ctp.h.  Validation follows the
+// pages' error set for frame vectors (non-finite, coincident source/detector,
+// the 1e6 and 1e15 magnitude limits; diffct tests/test_surface_geometry_cudasim.py,
+// release diff 2.4.1 -> 2.4.2, the failure/message parametrisation) and the native
+// spacing bounds ([1e-6, 1e6], max/min ratio <= 1e4; diffct CHANGELOG 2.4.4).
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/ctp.h"
+#include "ctp_column.cuh"
+#include "ctp_internal.h"
+#include "ctp_ray.cuh"
+
+struct ctp_plan {
+    int device = 0;
+    int path = CTP_PATH_RAY;
+    int ndim = 3, beam = 1;
+    int n_views = 0, n_u = 0, n_v = 0;
+    int n[3] = {0, 0, 0};
+    double spacing[3] = {0, 0, 0};
+    double origin[3] = {0, 0, 0};
+    long long n_rays = 0, n_cells = 0;
+    std::vector<ctp::ViewFrame> frames;     // host copy
+    ctp::ViewFrame *d_frames = nullptr;     // device copy
+    unsigned long long *d_counter = nullptr;
+    // column path
+    ctp::ColumnPlan col{};
+    void *d_columns = nullptr;              // ColumnTrace table
+    float *d_zvol = nullptr;                // z-fastest working volume
+    // host-buffer entry points
+    float *d_stage_vol = nullptr, *d_stage_sino = nullptr;
+    unsigned long long device_bytes = 0;
+};
+
+namespace {
+
+bool finite3(const float *v) { return std::isfinite(v[0]) && std::isfinite(v[1]) && std::isfinite(v[2]); }
+
+double norm3(const double *v) { return std::sqrt(v[0] * v[0] + v[1] * v[1] + v[2] * v[2]); }
+
+void cross3(const double *a, const double *b, double *out)
+{
+    out[0] = a[1] * b[2] - a[2] * b[1];
+    out[1] = a[2] * b[0] - a[0] * b[2];
+    out[2] = a[0] * b[1] - a[1] * b[0];
+}
+
+int check_device(const ctp_plan_t *plan)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CTP_E_CUDA;
+    return dev == plan->device ? CTP_OK : CTP_E_DEVICE;
+}
+
+ctp::RayParams ray_params(const ctp_plan_t *plan)
+{
+    ctp::RayParams P{};
+    P.views = plan->d_frames;
+    P.beam = plan->beam;
+    P.n_u = plan->n_u;
+    P.n_v = plan->n_v;
+    P.n_views = plan->n_views;
+    for (int a = 0; a < 3; ++a) {
+        P.n[a] = plan->n[a];
+        P.spacing[a] = plan->spacing[a];
+    }
+    P.stride[0] = 1;
+    P.stride[1] = plan->n[0];
+    P.stride[2] = plan->n[0] * plan->n[1];
+    return P;
+}
+
+// Threads of one ray block: 32 (u) x 4 (v) for 3-D scans, 128 (u) for single-row detectors.
+int launch_ray(const ctp_plan_t *plan, int which, const float *in, float *out, cudaStream_t s)
+{
+    const ctp::RayParams P = ray_params(plan);
+    if (plan->n_v == 1) {
+        dim3 grid((plan->n_u + 127) / 128, plan->n_views, 1), block(128);
+        if (which == 0) ctp::ray_forward_kernel<128, 1><<<grid, block, 0, s>>>(P, in, out);
+        else if (which == 1) ctp::ray_backward_kernel<128, 1><<<grid, block, 0, s>>>(P, in, out);
+        else ctp::ray_count_kernel<128, 1><<<grid, block, 0, s>>>(P, plan->d_counter);
+    } else {
+        dim3 grid((plan->n_u + 31) / 32, plan->n_views, (plan->n_v + 3) / 4), block(128);
+        if (which == 0) ctp::ray_forward_kernel<32, 4><<<grid, block, 0, s>>>(P, in, out);
+        else if (which == 1) ctp::ray_backward_kernel<32, 4><<<grid, block, 0, s>>>(P, in, out);
+        else ctp::ray_count_kernel<32, 4><<<grid, block, 0, s>>>(P, plan->d_counter);
+    }
+    return cudaGetLastError() == cudaSuccess ? CTP_OK : CTP_E_CUDA;
+}
+
+void free_plan(ctp_plan_t *p)
+{
+    if (!p) return;
+    cudaDeviceSynchronize();
+    cudaFree(p->d_frames);
+    cudaFree(p->d_counter);
+    cudaFree(p->d_columns);
+    cudaFree(p->d_zvol);
+    cudaFree(p->d_stage_vol);
+    cudaFree(p->d_stage_sino);
+    delete p;
+}
+
+int validate(const ctp_geometry *g, const ctp_volume *v)
+{
+    if (g->ndim != 2 && g->ndim != 3) return CTP_E_OPTION;
+    if (g->beam != CTP_PARALLEL && g->beam != CTP_DIVERGENT) return CTP_E_OPTION;
+    if (v->nx < 1 || v->ny < 1 || v->nz < 1 || v->nx > 32768 || v->ny > 32768 || v->nz > 32768)
+        return CTP_E_SHAPE;
+    if ((long long)v->nx * v->ny * v->nz >= (1LL << 31)) return CTP_E_SHAPE;
+    if (g->n_views < 0 || g->n_u < 1 || g->n_v < 1 || g->n_views > 65535) return CTP_E_SHAPE;
+    if ((g->n_v + 3) / 4 > 65535) return CTP_E_SHAPE;
+    if ((long long)g->n_views * g->n_u * g->n_v >= (1LL << 40)) return CTP_E_SHAPE;
+    if (g->ndim == 2 && (v->nz != 1 || g->n_v != 1)) return CTP_E_SHAPE;
+    const double sp[3] = {v->dx, v->dy, v->dz};
+    const double org[3] = {v->ox, v->oy, v->oz};
+    for (int a = 0; a < 3; ++a)
+        if (!std::isfinite(sp[a]) || !std::isfinite(org[a])) return CTP_E_NONFINITE;
+    if (!std::isfinite(g->pitch_u) || !std::isfinite(g->pitch_v) || !std::isfinite(g->offset_u) ||
+        !std::isfinite(g->offset_v))
+        return CTP_E_NONFINITE;
+    // 2-D scans ignore dz (one cell along z); only the in-plane pitches are bound.
+    const int naxes = g->ndim == 2 ? 2 : 3;
+    double smin = 1e300, smax = 0;
+    for (int a = 0; a < naxes; ++a) {
+        if (!(sp[a] >= 1e-6 && sp[a] <= 1e6)) return CTP_E_SPACING;
+        smin = std::fmin(smin, sp[a]);
+        smax = std::fmax(smax, sp[a]);
+    }
+    if (g->ndim == 2 && !(sp[2] > 0.0)) return CTP_E_SPACING;
+    if (smax / smin > 1e4) return CTP_E_SPACING;
+    if (!(g->pitch_u > 0.0f) || !(g->pitch_v > 0.0f)) return CTP_E_SHAPE;
+    if (g->n_views == 0) return CTP_OK;
+    if (!g->src || !g->det_centre || !g->det_u || !g->det_v) return CTP_E_NULL;
+
+    const double centre[3] = {v->ox + 0.5 * v->nx * v->dx, v->oy + 0.5 * v->ny * v->dy,
+                              v->oz + 0.5 * v->nz * v->dz};
+    for (int s = 0; s < g->n_views; ++s) {
+        const float *S = g->src + 3 * s, *C = g->det_centre + 3 * s;
+        const float *U = g->det_u + 3 * s, *V = g->det_v + 3 * s;
+        if (!finite3(S) || !finite3(C) || !finite3(U) || !finite3(V)) return CTP_E_NONFINITE;
+        double Sd[3], Cd[3], Ud[3], Vd[3], nrm[3];
+        for (int a = 0; a < 3; ++a) {
+            Sd[a] = S[a];
+            Cd[a] = C[a];
+            Ud[a] = U[a];
+            Vd[a] = V[a];
+        }
+        cross3(Ud, Vd, nrm);
+        if (!(norm3(Ud) > 0) || !(norm3(Vd) > 0) || !(norm3(nrm) > 1e-6 * norm3(Ud) * norm3(Vd)))
+            return CTP_E_AXES;
+        // magnitude limits on positions relative to the volume centre
+        const double *pts[2] = {Sd, Cd};
+        for (int q = 0; q < 2; ++q) {
+            if (q == 0 && g->beam == CTP_PARALLEL) continue;
+            for (int a = 0; a < 3; ++a)
+                if (std::fabs(pts[q][a] - centre[a]) > 1e15) return CTP_E_FAR;
+            for (int a = 0; a < 3; ++a)
+                if (std::fabs(pts[q][a] - centre[a]) > 1e6 * smax) return CTP_E_NEAR;
+        }
+        if (g->beam == CTP_PARALLEL) {
+            if (!(norm3(Sd) > 0)) return CTP_E_AXES;
+            const double dn = std::fabs(Sd[0] * nrm[0] + Sd[1] * nrm[1] + Sd[2] * nrm[2]);
+            if (!(dn > 1e-9 * norm3(Sd) * norm3(nrm))) return CTP_E_COINCIDENT;
+        } else {
+            // the source must not lie in the detector plane (some pixel would coincide)
+            double SC[3] = {Sd[0] - Cd[0], Sd[1] - Cd[1], Sd[2] - Cd[2]};
+            const double dn = std::fabs(SC[0] * nrm[0] + SC[1] * nrm[1] + SC[2] * nrm[2]);
+            if (!(dn > 1e-9 * norm3(nrm) * (norm3(SC) + 1e-300))) return CTP_E_COINCIDENT;
+        }
+    }
+    return CTP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ctp_status_string(int status)
+{
+    switch (status) {
+    case CTP_OK: return "ok";
+    case CTP_E_NULL: return "a required pointer is NULL";
+    case CTP_E_SHAPE: return "sizes out of range";
+    case CTP_E_NONFINITE: return "geometry and grid values must be finite";
+    case CTP_E_COINCIDENT: return "source and detector must differ";
+    case CTP_E_NEAR: return "frame coordinates must lie within 1e6 voxel widths of the volume";
+    case CTP_E_FAR: return "frame coordinates must be below 1e15 in magnitude";
+    case CTP_E_SPACING: return "spacing must be in [1e-6, 1e6] with max/min <= 1e4";
+    case CTP_E_AXES: return "detector axes must be non-zero and not parallel";
+    case CTP_E_CUDA: return "CUDA runtime error";
+    case CTP_E_DEVICE: return "current CUDA device differs from the plan's";
+    case CTP_E_OPTION: return "unknown ndim, beam or path";
+    case CTP_E_LIMIT: return "request exceeds a fixed limit of this entry point";
+    default: return "unknown status";
+    }
+}
+
+int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan_t **out)
+{
+    if (!out) return CTP_E_NULL;
+    *out = nullptr;
+    if (!geom || !vol) return CTP_E_NULL;
+    if (path != CTP_PATH_AUTO && path != CTP_PATH_RAY && path != CTP_PATH_COLUMN)
+        return CTP_E_OPTION;
+    int st = validate(geom, vol);
+    if (st != CTP_OK) return st;
+
+    ctp_plan_t *p = new (std::nothrow) ctp_plan_t();
+    if (!p) return CTP_E_CUDA;
+    if (cudaGetDevice(&p->device) != cudaSuccess) {
+        delete p;
+        return CTP_E_CUDA;
+    }
+    p->ndim = geom->ndim;
+    p->beam = geom->beam;
+    p->n_views = geom->n_views;
+    p->n_u = geom->n_u;
+    p->n_v = geom->n_v;
+    p->n[0] = vol->nx;
+    p->n[1] = vol->ny;
+    p->n[2] = vol->nz;
+    p->spacing[0] = vol->dx;
+    p->spacing[1] = vol->dy;
+    p->spacing[2] = vol->dz;
+    p->origin[0] = vol->ox;
+    p->origin[1] = vol->oy;
+    p->origin[2] = vol->oz;
+    p->n_rays = (long long)geom->n_views * geom->n_u * geom->n_v;
+    p->n_cells = (long long)vol->nx * vol->ny * vol->nz;
+
+    // Per-view frames in cell coordinates, float64.
+    p->frames.resize(geom->n_views > 0 ? geom->n_views : 1);
+    bool v_is_z = geom->ndim == 3;
+    const double cu = 0.5 * (geom->n_u - 1) - geom->offset_u;
+    const double cv = 0.5 * (geom->n_v - 1) - geom->offset_v;
+    for (int s = 0; s < geom->n_views; ++s) {
+        const float *S = geom->src + 3 * s, *C = geom->det_centre + 3 * s;
+        const float *U = geom->det_u + 3 * s, *V = geom->det_v + 3 * s;
+        ctp::ViewFrame &F = p->frames[s];
+        for (int a = 0; a < 3; ++a) {
+            const double d = p->spacing[a], o = p->origin[a];
+            const double pu = (double)geom->pitch_u * (double)U[a];
+            const double pv = (double)geom->pitch_v * (double)V[a];
+            // pixel (0, 0) = centre - cu * pitch_u * u - cv * pitch_v * v
+            const double p00 = (double)C[a] - cu * pu - cv * pv;
+            F.p00[a] = (p00 - o) / d;
+            F.du[a] = pu / d;
+            F.dv[a] = pv / d;
+            F.a[a] = geom->beam == CTP_DIVERGENT ? ((double)S[a] - o) / d : (double)S[a] / d;
+        }
+        if (!(V[0] == 0.0f && V[1] == 0.0f && V[2] != 0.0f)) v_is_z = false;
+    }
+
+    int chosen = path;
+    if (chosen == CTP_PATH_AUTO) chosen = v_is_z ? CTP_PATH_COLUMN : CTP_PATH_RAY;
+    if (chosen == CTP_PATH_COLUMN && !v_is_z) {
+        free_plan(p);
+        return CTP_E_OPTION;
+    }
+    p->path = chosen;
+
+    size_t fbytes = sizeof(ctp::ViewFrame) * p->frames.size();
+    if (cudaMalloc(&p->d_frames, fbytes) != cudaSuccess ||
+        cudaMemcpy(p->d_frames, p->frames.data(), fbytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMalloc(&p->d_counter, sizeof(unsigned long long)) != cudaSuccess) {
+        free_plan(p);
+        return CTP_E_CUDA;
+    }
+    p->device_bytes = fbytes + sizeof(unsigned long long);
+    if (chosen == CTP_PATH_COLUMN) {
+        st = ctp::column_plan_build(ray_params(p), &p->col, &p->d_columns, &p->d_zvol,
+                                    &p->device_bytes);
+        if (st == CTP_E_OPTION && path == CTP_PATH_AUTO) {
+            // some rows cross more than one z plane per slab: use the ray path
+            cudaFree(p->d_columns);
+            cudaFree(p->d_zvol);
+            p->d_columns = nullptr;
+            p->d_zvol = nullptr;
+            p->device_bytes = fbytes + sizeof(unsigned long long);
+            p->path = CTP_PATH_RAY;
+            st = CTP_OK;
+        }
+        if (st != CTP_OK) {
+            free_plan(p);
+            return st;
+        }
+    }
+    *out = p;
+    return CTP_OK;
+}
+
+void ctp_destroy(ctp_plan_t *plan) { free_plan(plan); }
+
+int ctp_plan_info_get(const ctp_plan_t *plan, ctp_plan_info *info)
+{
+    if (!plan || !info) return CTP_E_NULL;
+    info->path = plan->path;
+    info->device = plan->device;
+    info->n_rays = plan->n_rays;
+    info->n_cells = plan->n_cells;
+    info->device_bytes = plan->device_bytes;
+    return CTP_OK;
+}
+
+int ctp_forward(const ctp_plan_t *plan, const float *vol_dev, float *sino_dev, void *stream)
+{
+    if (!plan || !vol_dev || !sino_dev) return CTP_E_NULL;
+    int st = check_device(plan);
+    if (st != CTP_OK) return st;
+    if (plan->n_rays == 0) return CTP_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (plan->path == CTP_PATH_COLUMN)
+        return ctp::column_forward(ray_params(plan), plan->col, plan->d_columns, plan->d_zvol,
+                                   vol_dev, sino_dev, s);
+    return launch_ray(plan, 0, vol_dev, sino_dev, s);
+}
+
+int ctp_backward(const ctp_plan_t *plan, const float *sino_dev, float *vol_dev, void *stream)
+{
+    if (!plan || !vol_dev || !sino_dev) return CTP_E_NULL;
+    int st = check_device(plan);
+    if (st != CTP_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (plan->path == CTP_PATH_COLUMN)
+        return ctp::column_backward(ray_params(plan), plan->col, plan->d_columns, plan->d_zvol,
+                                    sino_dev, vol_dev, s);
+    if (cudaMemsetAsync(vol_dev, 0, sizeof(float) * plan->n_cells, s) != cudaSuccess)
+        return CTP_E_CUDA;
+    if (plan->n_rays == 0) return CTP_OK;
+    return launch_ray(plan, 1, sino_dev, vol_dev, s);
+}
+
+int ctp_segment_count(const ctp_plan_t *plan, unsigned long long *out, void *stream)
+{
+    if (!plan || !out) return CTP_E_NULL;
+    int st = check_device(plan);
+    if (st != CTP_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    *out = 0;
+    if (plan->n_rays == 0) return CTP_OK;
+    if (cudaMemsetAsync(plan->d_counter, 0, sizeof(unsigned long long), s) != cudaSuccess)
+        return CTP_E_CUDA;
+    if (plan->path == CTP_PATH_COLUMN)
+        st = ctp::column_count(ray_params(plan), plan->col, plan->d_columns, plan->d_counter, s);
+    else
+        st = launch_ray(plan, 2, nullptr, nullptr, s);
+    if (st != CTP_OK) return st;
+    if (cudaMemcpyAsync(out, plan->d_counter, sizeof(unsigned long long), cudaMemcpyDeviceToHost,
+                        s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return CTP_E_CUDA;
+    return CTP_OK;
+}
+
+static int ensure_stage(ctp_plan_t *plan)
+{
+    if (!plan->d_stage_vol) {
+        if (cudaMalloc(&plan->d_stage_vol, sizeof(float) * plan->n_cells) != cudaSuccess)
+            return CTP_E_CUDA;
+        plan->device_bytes += sizeof(float) * plan->n_cells;
+    }
+    if (!plan->d_stage_sino && plan->n_rays > 0) {
+        if (cudaMalloc(&plan->d_stage_sino, sizeof(float) * plan->n_rays) != cudaSuccess)
+            return CTP_E_CUDA;
+        plan->device_bytes += sizeof(float) * plan->n_rays;
+    }
+    return CTP_OK;
+}
+
+int ctp_forward_host(ctp_plan_t *plan, const float *vol_host, float *sino_host, void *stream)
+{
+    if (!plan || !vol_host || !sino_host) return CTP_E_NULL;
+    int st = check_device(plan);
+    if (st != CTP_OK) return st;
+    if (plan->n_rays == 0) return CTP_OK;
+    if ((st = ensure_stage(plan)) != CTP_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(plan->d_stage_vol, vol_host, sizeof(float) * plan->n_cells,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return CTP_E_CUDA;
+    if ((st = ctp_forward(plan, plan->d_stage_vol, plan->d_stage_sino, stream)) != CTP_OK) return st;
+    if (cudaMemcpyAsync(sino_host, plan->d_stage_sino, sizeof(float) * plan->n_rays,
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return CTP_E_CUDA;
+    return CTP_OK;
+}
+
+int ctp_backward_host(ctp_plan_t *plan, const float *sino_host, float *vol_host, void *stream)
+{
+    if (!plan || !vol_host || (!sino_host && plan->n_rays > 0)) return CTP_E_NULL;
+    int st = check_device(plan);
+    if (st != CTP_OK) return st;
+    if ((st = ensure_stage(plan)) != CTP_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (plan->n_rays > 0 &&
+        cudaMemcpyAsync(plan->d_stage_sino, sino_host, sizeof(float) * plan->n_rays,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return CTP_E_CUDA;
+    const float *sino = plan->n_rays > 0 ? plan->d_stage_sino : plan->d_stage_vol;
+    if ((st = ctp_backward(plan, sino, plan->d_stage_vol, stream)) != CTP_OK) return st;
+    if (cudaMemcpyAsync(vol_host, plan->d_stage_vol, sizeof(float) * plan->n_cells,
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return CTP_E_CUDA;
+    return CTP_OK;
+}
+
+}  // extern "C"

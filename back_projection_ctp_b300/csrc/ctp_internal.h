@@ -1,0 +1,28 @@
+// Internal types shared by the host plan code and the device kernels.
+#pragma once
+
+#include <cstdint>
+
+namespace ctp {
+
+// Per-view frame in CELL coordinates (x, y, z): world X maps to (X - o) / d.
+// Divergent: a = source.  Parallel: a = ray direction (cell units).
+// Pixel (iu, iv) = p00 + iu * du + iv * dv.  Built on the host in float64.
+struct ViewFrame {
+    double a[3];
+    double p00[3];
+    double du[3];
+    double dv[3];
+};
+
+// Launch-time constants of the ray path.
+struct RayParams {
+    const ViewFrame *views;
+    int beam;             // 0 parallel, 1 divergent
+    int n_u, n_v, n_views;
+    int n[3];             // cells along x, y, z
+    int stride[3];        // element stride of x, y, z in the (nz, ny, nx) buffer
+    double spacing[3];    // dx, dy, dz
+};
+
+}  // namespace ctp

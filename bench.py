@@ -1,0 +1,372 @@
+#!/usr/bin/env python
+"""Benchmark of the Siddon projector pair: forward + matched backprojection.
+
+One step = ctp_forward of the workload's phantom followed by ctp_backward of its
+N(0,1) sinogram (the whole hot path: ray set-up, traversal-gather, zero-fill,
+traversal-scatter).  Metric: giga ray-voxel segments per second, forward plus
+backward, where one pass holds the float64 oracle's count of positive-length
+(ray, cell) pieces (tests/golden/segment_counts.json; the plan's own counter
+agrees to 1e-6, tested).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl reference]
+
+With --gpus N > 1 (under torchrun) every rank runs an independent replica of the
+workload; the line reports the units of all ranks over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import ctp_inputs as ci  # noqa: E402
+
+METRIC = "Gray-segments/s (voxel-ray updates) fwd+bwd on 1 B300; % of BW roofline"
+UNIT = "Gseg/s"
+DEFAULT_CONFIG = 4
+FALLBACK_HBM_GBS = 6400.0
+CSRC = os.path.join(ROOT, "back_projection_ctp_b300", "csrc")
+
+
+# ----------------------------------------------------------------- helpers
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def golden_segments(idx: int) -> int:
+    with open(os.path.join(ROOT, "tests", "golden", "segment_counts.json")) as fh:
+        return int(json.load(fh)["full"][str(idx)]["segments"])
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            peaks = json.load(fh)
+        return float(peaks["hbm_gbs"]), "of measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "of fallback"
+
+
+def stored_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(kernel, {}).get(workload)
+    if not entry or entry.get("source_hash") != source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def geometry_of(w, frames):
+    from back_projection_ctp_b300 import Geometry
+    return Geometry(ndim=w.ndim, beam=w.beam, src=frames["src"], det_centre=frames["det_centre"],
+                    det_u=frames["det_u"], det_v=frames["det_v"], n_u=w.n_u, n_v=w.n_v,
+                    pitch_u=w.pitch_u, pitch_v=w.pitch_v, offset_u=w.offset_u,
+                    offset_v=w.offset_v)
+
+
+def volume_of(w):
+    from back_projection_ctp_b300 import Volume
+    return Volume(shape=w.shape, spacing=w.spacing, origin=w.origin)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ distributed
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- oracle arm
+def oracle_sample_rate(w, vol, y, budget_s: float = 15.0):
+    """The float64 oracle, as it stands, on a bounded sample of the workload:
+    forward and backward over the rays of the first m views, m sized so the
+    timed work is about budget_s seconds.  Returns (Gseg/s, sample text, cores)."""
+    import oracle
+    scan = oracle.Scan.from_workload(w, ci.frames(w))
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    per_view = w.n_u * w.n_v
+    # probe one view (untimed for the result) to size the sample
+    t = time.perf_counter()
+    oracle.forward(scan, vol, 0, per_view, threads=cores)
+    oracle.backward(scan, y[:per_view], 0, per_view, threads=cores)
+    probe = time.perf_counter() - t
+    m = int(max(1, min(w.n_views, budget_s // max(probe, 1e-3))))
+    ray1 = m * per_view
+    segs = oracle.segment_count(scan, 0, ray1, threads=cores)
+    t = time.perf_counter()
+    oracle.forward(scan, vol, 0, ray1, threads=cores)
+    oracle.backward(scan, y[:ray1], 0, ray1, threads=cores)
+    dt = time.perf_counter() - t
+    sample = (f"views 0..{m - 1} of {w.n_views} ({ray1} rays, {segs} segments), forward + "
+              f"backward, float64 C oracle, {cores} threads, {dt:.1f} s")
+    return 2.0 * segs / dt / 1e9, sample, cores, dt
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return 0
+    vol = ci.phantom(w)
+    y = ci.sinogram_noise(w).ravel()
+    rates, samples = [], []
+    for step in range(args.warmup + args.steps):
+        rate, sample, cores, dt = oracle_sample_rate(w, vol, y, budget_s=args.ref_budget)
+        if step >= args.warmup:
+            rates.append(rate)
+            samples.append(dt)
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * statistics.median(samples), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "note": "each step is a bounded sample of the workload"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, w, world, rank, local):
+    import torch
+    import back_projection_ctp_b300 as ctp
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    frames = ci.frames(w)
+    vol_h = ci.phantom(w)
+    y_h = ci.sinogram_noise(w)
+    plan = ctp.ctp_plan(geometry_of(w, frames), volume_of(w), args.path)
+    segments = golden_segments(args.config)
+
+    stream = torch.cuda.current_stream(dev)
+    d_vol = torch.from_numpy(vol_h).to(dev)
+    d_y = torch.from_numpy(y_h).to(dev)
+    d_sino = torch.empty(plan.sino_shape, dtype=torch.float32, device=dev)
+    d_g = torch.empty(plan.vol_shape, dtype=torch.float32, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ctp.ctp_forward(plan, d_vol, d_sino, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ctp.ctp_backward(plan, d_y, d_g, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(args.steps):
+        step(events[k])
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(start.elapsed_time(stop), world)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+    ms_per_step = total_ms / args.steps
+    value = world * 2.0 * segments / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the host-buffer C-ABI calls (pinned host memory)
+    vol_pin = torch.from_numpy(vol_h).pin_memory().numpy()
+    y_pin = torch.from_numpy(y_h).pin_memory().numpy()
+    sino_pin = torch.empty(plan.sino_shape, dtype=torch.float32).pin_memory().numpy()
+    g_pin = torch.empty(plan.vol_shape, dtype=torch.float32).pin_memory().numpy()
+    ctp.ctp_forward_host(plan, vol_pin, sino_pin, stream)
+    ctp.ctp_backward_host(plan, y_pin, g_pin, stream)
+    e2e_steps = max(1, min(args.steps, 3))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        ctp.ctp_forward_host(plan, vol_pin, sino_pin, stream)
+        ctp.ctp_backward_host(plan, y_pin, g_pin, stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+    barrier(world)
+    e2e_value = world * 2.0 * segments / e2e_s / 1e9
+    bytes_io = 4 * (w.n_voxels + w.n_rays)
+
+    # roofline of the dominant call (4 algorithmic bytes per segment: one voxel
+    # read per forward segment, one float atomic per backward segment)
+    dominant = "backward" if bwd_ms >= fwd_ms else "forward"
+    dom_ms = max(bwd_ms, fwd_ms)
+    achieved = 4.0 * segments / (dom_ms * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+    kernel_name = {"column": {"forward": "column_forward_kernel", "backward": "column_backward_kernel"},
+                   "ray": {"forward": "ray_forward_kernel", "backward": "ray_backward_kernel"}}[plan.path][dominant]
+    launches_per_step = 4 if plan.path == "column" else 2
+
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            rate, sample, cores, _ = oracle_sample_rate(w, vol_h, y_h.ravel(), args.ref_budget)
+            cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "shape_DHW": list(w.shape),
+                       "spacing_DHW": list(w.spacing), "views": w.n_views,
+                       "detector_vu": [w.n_v, w.n_u], "segments_per_pass": segments,
+                       "path": plan.path, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (no flush)" if 4 * w.n_voxels > 126e6
+                       else "inputs smaller than L2 (no flush)",
+                       "fwd_ms": fwd_ms, "bwd_ms": bwd_ms},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": stored_traffic(kernel_name, w.name),
+                         "kernel": kernel_name, "call": dominant,
+                         "note": f"4 B per segment over the {dominant} call's event time; peak {peak_src}"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bytes_io,
+                    "d2h_bytes_per_step": bytes_io, "ms_per_step": e2e_s * 1e3},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    plan.destroy()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ctp", choices=["ctp", "reference"])
+    ap.add_argument("--path", default="auto", choices=["auto", "ray", "column"])
+    ap.add_argument("--ref-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = ci.get(args.config)
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, w, world, rank)
+        return run_gpu(args, w, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

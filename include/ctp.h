@@ -1,0 +1,160 @@
+/*
+ * ctp.h -- C ABI of the B300 (sm_103a) ray-driven Siddon projector pair.
+ *
+ * The library computes, for every detector ray R of a scan and a volume f of
+ * axis-aligned constant cells,
+ *
+ *     forward    p(R)    = sum over cells c of |R n c| * f(c)
+ *     backward   g(c)    = sum over rays  R of |R n c| * y(R)
+ *
+ * where |R n c| is the physical length of the ray inside the cell.  The two
+ * are an exact adjoint pair of the cell-constant Siddon model ("Matched
+ * operators", diffct README, release diff 2.1.0 -> 2.2.1; "Siddon path sum;
+ * matched adjoint", docs/video/README.md, release diff 2.4.1 -> 2.4.2), with
+ * per-axis voxel spacing in physical length units (diffct CHANGELOG 2.4.4,
+ * "Added": native per-axis voxel spacing).
+ *
+ * Conventions (all calls):
+ *   - World axes x, y, z.  Volume buffers are float32, C-contiguous with shape
+ *     (nz, ny, nx): x fastest ("(D, H, W)" tensor order).  Cell (i, j, k)
+ *     covers [o + i d, o + (i+1) d) per axis, o = (ox, oy, oz).
+ *   - Sinogram buffers are float32, C-contiguous (n_views, n_v, n_u): u fastest.
+ *   - Detector pixel (iu, iv) of view s sits at
+ *         det_centre[s] + (iu - (n_u-1)/2 + offset_u) * pitch_u * det_u[s]
+ *                       + (iv - (n_v-1)/2 + offset_v) * pitch_v * det_v[s].
+ *     Divergent beams (fan in 2-D, cone in 3-D): the ray is the segment from
+ *     src[s] to the pixel.  Parallel beams: src[s] is the ray direction and the
+ *     ray is the whole line through the pixel.  Each view has its own frame
+ *     (per-view trajectory tuple, diffct README "Arbitrary trajectories").
+ *   - A ray lying exactly in a cell-face plane counts in the cell on the + side.
+ *   - 2-D scans are 3-D scans with nz = 1 and n_v = 1.
+ *
+ * Ownership: the caller owns every volume / sinogram buffer (device pointers
+ * unless a name says _host); the library never frees or keeps them ("caller-owned
+ * float32 buffers", diffct release diff 2.4.1 -> 2.4.2, kernels/surface_geometry.py
+ * docstring; project_into / backproject_into, CHANGELOG 2.2.0).  A plan owns its
+ * copy of the geometry and its device tables and scratch.  Calls are asynchronous
+ * on the given stream unless stated; a NULL stream is the legacy default stream.
+ *
+ * Errors: every entry point returns a ctp_status; no C++ exception crosses the
+ * ABI.  Validation happens on the host in ctp_plan before any device work
+ * (validation errors surface before numerical work, CHANGELOG 2.4.0 "Fixed").
+ */
+#ifndef CTP_H
+#define CTP_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ctp_status {
+    CTP_OK = 0,
+    CTP_E_NULL = 1,        /* a required pointer is NULL */
+    CTP_E_SHAPE = 2,       /* sizes out of range (see ctp_plan) */
+    CTP_E_NONFINITE = 3,   /* a frame vector, pitch, offset, spacing or origin is not finite */
+    CTP_E_COINCIDENT = 4,  /* source and detector must differ (or parallel ray along the detector) */
+    CTP_E_NEAR = 5,        /* frame coordinates beyond 1e6 voxel widths of the volume */
+    CTP_E_FAR = 6,         /* frame coordinates beyond 1e15 in magnitude */
+    CTP_E_SPACING = 7,     /* spacing outside [1e-6, 1e6] or max/min ratio above 1e4 */
+    CTP_E_AXES = 8,        /* detector axes zero or parallel; parallel ray direction zero */
+    CTP_E_CUDA = 9,        /* a CUDA runtime call failed */
+    CTP_E_DEVICE = 10,     /* called with a different current device than the plan's */
+    CTP_E_OPTION = 11,     /* unknown beam / ndim / path value */
+    CTP_E_LIMIT = 12       /* request beyond a fixed size limit of this entry point */
+} ctp_status;
+
+typedef enum ctp_beam { CTP_PARALLEL = 0, CTP_DIVERGENT = 1 } ctp_beam;
+
+/* Traversal path.  AUTO picks COLUMN when every view's detector v axis is
+ * exactly +-z (then all rays of a detector column share one xy trace), else RAY. */
+typedef enum ctp_path { CTP_PATH_AUTO = 0, CTP_PATH_RAY = 1, CTP_PATH_COLUMN = 2 } ctp_path;
+
+typedef struct ctp_geometry {
+    int ndim;                 /* 2 or 3 */
+    int beam;                 /* ctp_beam */
+    int n_views, n_u, n_v;    /* n_v = 1 for 2-D; n_views may be 0 (empty scan) */
+    const float *src;         /* HOST (n_views, 3): source, or unit ray direction (PARALLEL) */
+    const float *det_centre;  /* HOST (n_views, 3) */
+    const float *det_u;       /* HOST (n_views, 3) unit u axis */
+    const float *det_v;       /* HOST (n_views, 3) unit v axis (2-D: any vector not along u) */
+    float pitch_u, pitch_v;   /* detector pitch (physical units) */
+    float offset_u, offset_v; /* detector-centre offset in pixels */
+} ctp_geometry;
+
+typedef struct ctp_volume {
+    int nx, ny, nz;           /* cells; nz = 1 for 2-D */
+    double dx, dy, dz;        /* spacing; each in [1e-6, 1e6], max/min <= 1e4 */
+    double ox, oy, oz;        /* world position of the min corner of cell (0, 0, 0);
+                                 a centred volume has o = -n * d / 2 */
+} ctp_volume;
+
+typedef struct ctp_plan ctp_plan_t;
+
+typedef struct ctp_plan_info {
+    int path;                         /* ctp_path actually used */
+    int device;                       /* CUDA device the plan lives on */
+    long long n_rays;                 /* n_views * n_v * n_u */
+    long long n_cells;                /* nx * ny * nz */
+    unsigned long long device_bytes;  /* device memory owned by the plan */
+} ctp_plan_info;
+
+/*
+ * ctp_plan -- validate a scan and build a plan on the current CUDA device.
+ * geom, vol: host structs, read only during the call (all frame arrays are
+ * copied).  path: a ctp_path.  *out receives the plan (NULL on error).
+ * Limits: 1 <= nx, ny, nz <= 32768 with nx*ny*nz < 2^31; n_u, n_v >= 1,
+ * n_views >= 0, n_views*n_v*n_u < 2^40, n_views <= 65535, ceil(n_v/4) <= 65535.
+ * Errors: CTP_E_NULL, CTP_E_OPTION, CTP_E_SHAPE, CTP_E_NONFINITE, CTP_E_SPACING,
+ * CTP_E_AXES, CTP_E_COINCIDENT, CTP_E_NEAR, CTP_E_FAR (the validation set of the
+ * pages' tests: "finite", "must differ", "1e6", "1e15"), CTP_E_CUDA.
+ * Synchronous: allocates and fills the plan's device tables.
+ */
+int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan_t **out);
+
+/* Release a plan (NULL is ignored).  Synchronises the device before freeing. */
+void ctp_destroy(ctp_plan_t *plan);
+
+/* Plan facts; info is a host struct. */
+int ctp_plan_info_get(const ctp_plan_t *plan, ctp_plan_info *info);
+
+/*
+ * ctp_forward -- p = A f.  vol_dev: device float32 (nz, ny, nx), read only.
+ * sino_dev: device float32 (n_views, n_v, n_u), fully overwritten (rays that
+ * miss the volume get 0).  stream: a cudaStream_t (NULL = default stream).
+ * The two buffers must not overlap.  Errors: CTP_E_NULL, CTP_E_DEVICE, CTP_E_CUDA.
+ */
+int ctp_forward(const ctp_plan_t *plan, const float *vol_dev, float *sino_dev, void *stream);
+
+/*
+ * ctp_backward -- g = A^T y.  sino_dev: device float32 (n_views, n_v, n_u), read
+ * only.  vol_dev: device float32 (nz, ny, nx), fully overwritten (zeroed, then
+ * accumulated with float32 atomics, so the summation order -- not the set of
+ * terms -- varies between calls).  Errors as ctp_forward.
+ */
+int ctp_backward(const ctp_plan_t *plan, const float *sino_dev, float *vol_dev, void *stream);
+
+/*
+ * ctp_segment_count -- number of positive-length (ray, cell) pieces the plan's
+ * traversal visits in one pass (identical for forward and backward).  *out is a
+ * host value; the call waits for the stream.  Diagnostics and throughput units.
+ */
+int ctp_segment_count(const ctp_plan_t *plan, unsigned long long *out, void *stream);
+
+/*
+ * Host-buffer variants (end-to-end): copy the input from host memory, run the
+ * operator, copy the result back, and wait for the stream.  Host buffers may be
+ * pageable or pinned (pinned copies overlap better).  The plan allocates one
+ * device volume and one device sinogram on the first host-buffer call (do that
+ * first call before any stream capture) and reuses them.
+ */
+int ctp_forward_host(ctp_plan_t *plan, const float *vol_host, float *sino_host, void *stream);
+int ctp_backward_host(ctp_plan_t *plan, const float *sino_host, float *vol_host, void *stream);
+
+/* Static English text of a status code. */
+const char *ctp_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CTP_H */

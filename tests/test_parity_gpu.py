@@ -1,0 +1,257 @@
+"""GPU parity: the CUDA pair (through the C ABI) against the float64 oracle.
+
+Bars: forward relative L2 <= 1e-5, backward relative L2 <= 1e-4 (float32
+atomics, order-dependent), the GPU pair's own adjoint identity <= 1e-5
+(Cauchy-Schwarz normalised).  Rays that lie in a cell-face plane (where the
++ side rule decides and any finite-precision traversal may legitimately pick
+the other side) are excluded: their pixels from the forward comparison, their
+values from the backward input.
+"""
+
+import dataclasses
+import json
+import os
+
+import numpy as np
+import pytest
+
+from cases import (TOL_ADJOINT, TOL_BACKWARD, TOL_FORWARD, adjoint_mismatch, ci, geometry_of,
+                   rel_l2, volume_of)
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as _torch
+    assert _torch.cuda.is_available(), "CUDA device required"
+    return _torch
+
+
+@pytest.fixture(scope="module")
+def ctp():
+    import back_projection_ctp_b300 as _ctp
+    _ctp.load_library()
+    return _ctp
+
+
+def _run_pair(torch, ctp, plan, vol, y):
+    d_vol = torch.from_numpy(np.ascontiguousarray(vol)).cuda()
+    d_sino = torch.empty(plan.sino_shape, dtype=torch.float32, device="cuda")
+    ctp.ctp_forward(plan, d_vol, d_sino)
+    d_y = torch.from_numpy(np.ascontiguousarray(y)).cuda()
+    d_g = torch.full(plan.vol_shape, float("nan"), dtype=torch.float32, device="cuda")
+    ctp.ctp_backward(plan, d_y, d_g)
+    torch.cuda.synchronize()
+    return d_sino.cpu().numpy(), d_g.cpu().numpy()
+
+
+SMALL = ci.small_cases()
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("path", ["auto", "ray"])
+def test_small_cases_match_oracle(torch, ctp, oracle_mod, idx, path):
+    w = SMALL[idx]
+    f = ci.frames(w)
+    scan = oracle_mod.Scan.from_workload(w, f)
+    vol = ci.phantom(w)
+    y = ci.sinogram_noise(w)
+    amb = oracle_mod.ambiguous(scan)
+    y_clean = np.where(amb, np.float32(0), y)
+    p_ref = oracle_mod.forward(scan, vol)
+    g_ref = oracle_mod.backward(scan, y_clean.ravel())
+
+    plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w), path)
+    assert plan.path == ("column" if (path == "auto" and w.ndim == 3) else "ray")
+    p, g = _run_pair(torch, ctp, plan, vol, y_clean)
+    assert rel_l2(p[~amb], p_ref[~amb]) <= TOL_FORWARD
+    assert rel_l2(g, g_ref) <= TOL_BACKWARD
+
+    # the GPU pair's own adjoint identity, random x and y, every ray included
+    rng = np.random.default_rng(idx)
+    x = rng.standard_normal(w.shape).astype(np.float32)
+    Ax, Aty = _run_pair(torch, ctp, plan, x, y)
+    cs, raw = adjoint_mismatch(Ax, y, x, Aty)
+    assert cs <= TOL_ADJOINT, (cs, raw)
+
+    n_ref = oracle_mod.segment_count(scan)
+    n_gpu = ctp.ctp_segment_count(plan)
+    assert abs(n_gpu - n_ref) <= max(1e-6 * n_ref, 4), (n_gpu, n_ref)
+
+
+@pytest.mark.parametrize("idx", [3, 4, 5])
+def test_ray_and_column_paths_agree(torch, ctp, idx):
+    w = SMALL[idx]
+    f = ci.frames(w)
+    vol = ci.phantom(w)
+    y = ci.sinogram_noise(w)
+    out = {}
+    for path in ("ray", "column"):
+        plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w), path)
+        out[path] = _run_pair(torch, ctp, plan, vol, y)
+    assert rel_l2(out["column"][0], out["ray"][0]) <= TOL_FORWARD
+    assert rel_l2(out["column"][1], out["ray"][1]) <= TOL_BACKWARD
+
+
+def test_host_entry_points_match_device(torch, ctp):
+    w = SMALL[3]
+    f = ci.frames(w)
+    plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w))
+    vol = ci.phantom(w)
+    y = ci.sinogram_noise(w)
+    p_dev, g_dev = _run_pair(torch, ctp, plan, vol, y)
+    p_host = np.empty(plan.sino_shape, np.float32)
+    ctp.ctp_forward_host(plan, vol, p_host)
+    g_host = np.empty(plan.vol_shape, np.float32)
+    ctp.ctp_backward_host(plan, y, g_host)
+    assert np.array_equal(p_host, p_dev)
+    assert rel_l2(g_host, g_dev) <= 1e-6
+
+
+# ------------------------------------------------------------------ edge cases
+def _custom(oracle_mod, beam, frames, shape, spacing, n_u, n_v, pu, pv, ou=0.0, ov=0.0):
+    D, H, W = shape
+    origin = (-0.5 * W * spacing[2], -0.5 * H * spacing[1], -0.5 * D * spacing[0])
+    frames = {k: np.ascontiguousarray(v, np.float32) for k, v in frames.items()}
+    scan = oracle_mod.Scan(beam, frames["src"], frames["det_centre"], frames["det_u"],
+                           frames["det_v"], n_u, n_v, pu, pv, shape, spacing, origin, ou, ov)
+    import back_projection_ctp_b300 as ctp
+    g = ctp.Geometry(ndim=3, beam=beam, n_u=n_u, n_v=n_v, pitch_u=pu, pitch_v=pv, offset_u=ou,
+                     offset_v=ov, **frames)
+    return scan, g, ctp.Volume(shape, spacing, origin)
+
+
+def _check_case(torch, ctp, oracle_mod, scan, g, v, paths=("ray",), seed=0):
+    rng = np.random.default_rng(seed)
+    vol = rng.uniform(0, 1, v.shape).astype(np.float32)
+    y = rng.standard_normal(scan.sino_shape).astype(np.float32)
+    amb = oracle_mod.ambiguous(scan)
+    y = np.where(amb, np.float32(0), y)
+    p_ref = oracle_mod.forward(scan, vol)
+    g_ref = oracle_mod.backward(scan, y.ravel())
+    for path in paths:
+        plan = ctp.ctp_plan(g, v, path)
+        p, gg = _run_pair(torch, ctp, plan, vol, y)
+        assert rel_l2(p[~amb], p_ref[~amb]) <= TOL_FORWARD, path
+        assert rel_l2(gg, g_ref) <= TOL_BACKWARD, path
+
+
+def test_empty_scan_zeroes_backprojection(torch, ctp):
+    z = np.zeros((0, 3), np.float32)
+    g = ctp.Geometry(ndim=3, beam="divergent", src=z, det_centre=z, det_u=z, det_v=z, n_u=4,
+                     n_v=4, pitch_u=1.0, pitch_v=1.0)
+    plan = ctp.ctp_plan(g, ctp.Volume((3, 4, 5), (1.0, 1.0, 1.0), (-2.5, -2.0, -1.5)))
+    assert plan.n_rays == 0
+    sino = torch.empty((0, 4, 4), dtype=torch.float32, device="cuda")
+    vol = torch.full((3, 4, 5), 7.0, dtype=torch.float32, device="cuda")
+    ctp.ctp_forward(plan, vol, sino)
+    ctp.ctp_backward(plan, sino, vol)
+    assert float(vol.abs().max()) == 0.0
+    assert ctp.ctp_segment_count(plan) == 0
+
+
+def test_single_cell_and_single_pixel(torch, ctp, oracle_mod):
+    frames = dict(src=[[5.0, 0.3, 0.2]], det_centre=[[-5.0, -0.1, 0.05]], det_u=[[0, 1, 0]],
+                  det_v=[[0, 0, 1]])
+    scan, g, v = _custom(oracle_mod, "divergent", frames, (1, 1, 1), (0.7, 1.3, 0.9), 1, 1, 1.0, 1.0)
+    _check_case(torch, ctp, oracle_mod, scan, g, v, paths=("ray", "column"))
+
+
+def test_source_and_detector_inside_volume(torch, ctp, oracle_mod):
+    # rays start and end inside the grid: partial first / last slabs
+    rng = np.random.default_rng(3)
+    n = 6
+    src = rng.uniform(-3, 3, (n, 3))
+    cen = rng.uniform(-3, 3, (n, 3))
+    u = np.tile([0.0, 1.0, 0.0], (n, 1))
+    vv = np.tile([0.0, 0.0, 1.0], (n, 1))
+    cen[:, 0] = src[:, 0] - rng.uniform(2, 5, n)
+    frames = dict(src=src, det_centre=cen, det_u=u, det_v=vv)
+    scan, g, v = _custom(oracle_mod, "divergent", frames, (9, 10, 11), (1.0, 0.9, 0.8), 7, 5, 0.4, 0.5)
+    _check_case(torch, ctp, oracle_mod, scan, g, v, paths=("ray", "column"))
+
+
+def test_tilted_detectors_and_parallel_3d(torch, ctp, oracle_mod):
+    from geom_helpers import random_frames
+    rng = np.random.default_rng(4)
+    for beam in ("divergent", "parallel"):
+        fr = random_frames(rng, 7, beam, radius=50.0, det_dist=30.0)
+        frames = dict(src=fr[0], det_centre=fr[1], det_u=fr[2], det_v=fr[3])
+        scan, g, v = _custom(oracle_mod, beam, frames, (13, 17, 15), (1.1, 0.9, 1.0), 19, 23, 1.3, 1.1,
+                             0.25, -0.5)
+        _check_case(torch, ctp, oracle_mod, scan, g, v, paths=("ray",), seed=5)
+
+
+def test_parallel_3d_vertical_detector_uses_column_path(torch, ctp, oracle_mod):
+    b = np.linspace(0, np.pi, 10, endpoint=False)
+    c, s, z = np.cos(b), np.sin(b), np.zeros_like(b)
+    frames = dict(src=np.stack([c, s, 0.1 + z], 1) / np.sqrt(1.01), det_centre=np.stack([z, z, z], 1),
+                  det_u=np.stack([-s, c, z], 1), det_v=np.stack([z, z, 1 + z], 1))
+    scan, g, v = _custom(oracle_mod, "parallel", frames, (12, 14, 16), (1.0, 1.0, 1.0), 25, 40, 0.8, 0.45)
+    assert ctp.ctp_plan(g, v).path == "column"
+    _check_case(torch, ctp, oracle_mod, scan, g, v, paths=("column", "ray"), seed=6)
+
+
+def test_axis_aligned_rays(torch, ctp, oracle_mod):
+    frames = dict(src=[[1, 0, 0], [0, 1, 0], [0, 0, 1], [0, -1, 0]],
+                  det_centre=[[0, 0.31, 0.17], [0.23, 0, 0.41], [0.13, 0.29, 0], [0.37, 0, 0.11]],
+                  det_u=[[0, 1, 0], [0, 0, 1], [1, 0, 0], [1, 0, 0]],
+                  det_v=[[0, 0, 1], [1, 0, 0], [0, 1, 0], [0, 0, 1]])
+    scan, g, v = _custom(oracle_mod, "parallel", frames, (6, 7, 8), (1.0, 0.8, 1.2), 9, 8, 0.77, 0.61)
+    _check_case(torch, ctp, oracle_mod, scan, g, v, paths=("ray",), seed=7)
+
+
+def test_steep_cone_falls_back_to_ray_path(torch, ctp, oracle_mod):
+    # cone half-angle above 45 degrees in cell units: some rows cross several
+    # z planes per slab, which the column walk does not cover
+    frames = dict(src=[[30, 0, 0], [0, 30, 0]], det_centre=[[-10, 0, 0], [0, -10, 0]],
+                  det_u=[[0, 1, 0], [-1, 0, 0]], det_v=[[0, 0, 1], [0, 0, 1]])
+    scan, g, v = _custom(oracle_mod, "divergent", frames, (20, 8, 8), (1.0, 1.0, 1.0), 12, 101, 1.0, 1.0)
+    assert ctp.ctp_plan(g, v).path == "ray"
+    with pytest.raises(ctp.CtpError):
+        ctp.ctp_plan(g, v, "column")
+    _check_case(torch, ctp, oracle_mod, scan, g, v, paths=("auto",), seed=8)
+
+
+# ------------------------------------------------------------- full-size runs
+def _full_counts():
+    with open(os.path.join(HERE, "golden", "segment_counts.json")) as fh:
+        return json.load(fh)["full"]
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
+def test_full_size_sampled_parity(torch, ctp, oracle_mod, idx):
+    """The workloads at full size in the benchmark's launch configuration
+    (AUTO path, default stream): sampled rays and voxels against the oracle,
+    the adjoint identity and the segment count over the whole scan."""
+    w = ci.get(idx)
+    f = ci.frames(w)
+    scan = oracle_mod.Scan.from_workload(w, f)
+    vol = ci.phantom(w)
+    y = ci.sinogram_noise(w)
+    amb = oracle_mod.ambiguous(scan)
+    y_clean = np.where(amb, np.float32(0), y)
+    plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w))
+    p, g = _run_pair(torch, ctp, plan, vol, y_clean)
+
+    rng = np.random.default_rng(100 + idx)
+    flat_ok = np.flatnonzero(~amb.ravel())
+    rays = rng.choice(flat_ok, min(4000, flat_ok.size), replace=False)
+    p_ref = oracle_mod.forward_rays(scan, vol, rays)
+    assert rel_l2(p.ravel()[rays], p_ref) <= TOL_FORWARD
+
+    # voxels inside the reconstruction region (where many rays pass)
+    vox = rng.choice(w.n_voxels, 300 if w.ndim == 3 else 2000, replace=False)
+    g_ref = oracle_mod.backward_voxels(scan, y_clean, vox)
+    assert rel_l2(g.ravel()[vox], g_ref) <= TOL_BACKWARD
+
+    Aty = g
+    cs, raw = adjoint_mismatch(p, y_clean, vol, Aty)
+    assert cs <= TOL_ADJOINT, (cs, raw)
+
+    n_gpu = ctp.ctp_segment_count(plan)
+    n_ref = _full_counts()[str(idx)]["segments"]
+    assert abs(n_gpu - n_ref) <= 1e-6 * n_ref, (n_gpu, n_ref)
