@@ -34,7 +34,8 @@ struct ctp_plan {
     // column path
     ctp::ColumnPlan col{};
     void *d_columns = nullptr;              // ColumnTrace table
-    float *d_zvol = nullptr;                // z-fastest working volume
+    float *d_zfwd = nullptr;                // padded z-fastest copy read by the forward
+    float *d_zbwd = nullptr;                // padded z-fastest accumulator of the backward
     // host-buffer entry points
     float *d_stage_vol = nullptr, *d_stage_sino = nullptr;
     unsigned long long device_bytes = 0;
@@ -75,6 +76,8 @@ ctp::RayParams ray_params(const ctp_plan_t *plan)
     P.stride[0] = 1;
     P.stride[1] = plan->n[0];
     P.stride[2] = plan->n[0] * plan->n[1];
+    P.min_len = (float)(1e-5 * std::fmin(plan->spacing[0],
+                                         std::fmin(plan->spacing[1], plan->spacing[2])));
     return P;
 }
 
@@ -103,7 +106,8 @@ void free_plan(ctp_plan_t *p)
     cudaFree(p->d_frames);
     cudaFree(p->d_counter);
     cudaFree(p->d_columns);
-    cudaFree(p->d_zvol);
+    cudaFree(p->d_zfwd);
+    cudaFree(p->d_zbwd);
     cudaFree(p->d_stage_vol);
     cudaFree(p->d_stage_sino);
     delete p;
@@ -277,14 +281,16 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
     }
     p->device_bytes = fbytes + sizeof(unsigned long long);
     if (chosen == CTP_PATH_COLUMN) {
-        st = ctp::column_plan_build(ray_params(p), &p->col, &p->d_columns, &p->d_zvol,
-                                    &p->device_bytes);
+        st = ctp::column_plan_build(ray_params(p), &p->col, &p->d_columns, &p->d_zfwd,
+                                    &p->d_zbwd, &p->device_bytes);
         if (st == CTP_E_OPTION && path == CTP_PATH_AUTO) {
             // some rows cross more than one z plane per slab: use the ray path
             cudaFree(p->d_columns);
-            cudaFree(p->d_zvol);
+            cudaFree(p->d_zfwd);
+            cudaFree(p->d_zbwd);
             p->d_columns = nullptr;
-            p->d_zvol = nullptr;
+            p->d_zfwd = nullptr;
+            p->d_zbwd = nullptr;
             p->device_bytes = fbytes + sizeof(unsigned long long);
             p->path = CTP_PATH_RAY;
             st = CTP_OK;
@@ -313,25 +319,26 @@ int ctp_plan_info_get(const ctp_plan_t *plan, ctp_plan_info *info)
 
 int ctp_forward(const ctp_plan_t *plan, const float *vol_dev, float *sino_dev, void *stream)
 {
-    if (!plan || !vol_dev || !sino_dev) return CTP_E_NULL;
+    if (!plan) return CTP_E_NULL;
+    if (plan->n_rays > 0 && (!vol_dev || !sino_dev)) return CTP_E_NULL;
     int st = check_device(plan);
     if (st != CTP_OK) return st;
     if (plan->n_rays == 0) return CTP_OK;
     cudaStream_t s = (cudaStream_t)stream;
     if (plan->path == CTP_PATH_COLUMN)
-        return ctp::column_forward(ray_params(plan), plan->col, plan->d_columns, plan->d_zvol,
+        return ctp::column_forward(ray_params(plan), plan->col, plan->d_columns, plan->d_zfwd,
                                    vol_dev, sino_dev, s);
     return launch_ray(plan, 0, vol_dev, sino_dev, s);
 }
 
 int ctp_backward(const ctp_plan_t *plan, const float *sino_dev, float *vol_dev, void *stream)
 {
-    if (!plan || !vol_dev || !sino_dev) return CTP_E_NULL;
+    if (!plan || !vol_dev || (plan->n_rays > 0 && !sino_dev)) return CTP_E_NULL;
     int st = check_device(plan);
     if (st != CTP_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     if (plan->path == CTP_PATH_COLUMN)
-        return ctp::column_backward(ray_params(plan), plan->col, plan->d_columns, plan->d_zvol,
+        return ctp::column_backward(ray_params(plan), plan->col, plan->d_columns, plan->d_zbwd,
                                     sino_dev, vol_dev, s);
     if (cudaMemsetAsync(vol_dev, 0, sizeof(float) * plan->n_cells, s) != cudaSuccess)
         return CTP_E_CUDA;

@@ -23,6 +23,7 @@ struct RayParams {
     int n[3];             // cells along x, y, z
     int stride[3];        // element stride of x, y, z in the (nz, ny, nx) buffer
     double spacing[3];    // dx, dy, dz
+    float min_len;        // segment counter: pieces longer than this (physical units)
 };
 
 }  // namespace ctp

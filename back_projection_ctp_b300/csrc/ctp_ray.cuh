@@ -111,13 +111,11 @@ __device__ __forceinline__ bool slab_setup(const RayParams &P, int view, int iu,
     }
     if (!(lo < hi)) return false;
 
-    // Slab range, one slab wider than the transverse clip (cells outside the
-    // volume are skipped by the walk's bounds test), never past the ray's ends.
-    double k0 = floor(lo) - 1.0, k1 = ceil(hi);
-    k0 = fmax(k0, floor(lo_t));
-    k1 = fmin(k1, ceil(hi_t) - 1.0);
-    k0 = fmax(k0, 0.0);
-    k1 = fmin(k1, (double)(P.n[p] - 1));
+    // Slabs that hold part of [lo, hi).  Where the fixed-point walk and this
+    // float64 clip disagree by rounding (~1e-9 slab), the walk's bounds test
+    // drops the sliver outside the grid.
+    double k0 = fmax(floor(lo), 0.0);
+    double k1 = fmin(ceil(hi) - 1.0, (double)(P.n[p] - 1));
     if (k0 > k1) return false;
     R.k0 = (int)k0;
     R.k1 = (int)k1;
@@ -211,9 +209,15 @@ struct ScatterOp {
     }
 };
 
+// Counts the pieces longer than thr slab units (the counting threshold over
+// the ray's length per slab).
 struct CountOp {
     unsigned n;
-    __device__ __forceinline__ void operator()(int, float, bool on) { n += on ? 1u : 0u; }
+    float thr;
+    __device__ __forceinline__ void operator()(int, float d, bool on)
+    {
+        n += (on && d > thr) ? 1u : 0u;
+    }
 };
 
 template <int TU, int TV>
@@ -264,7 +268,7 @@ __global__ void __launch_bounds__(TU *TV) ray_count_kernel(RayParams P,
     if (iu < P.n_u && iv < P.n_v) {
         SlabRay R;
         if (slab_setup(P, view, iu, iv, R)) {
-            CountOp op{0u};
+            CountOp op{0u, __fdiv_rn(P.min_len, R.ell)};
             slab_walk(R, op);
             n = op.n;
         }

@@ -232,6 +232,7 @@ def run_reference(args, w, world, rank):
 
 # ------------------------------------------------------------------ GPU arm
 def run_gpu(args, w, world, rank, local):
+    """Time K steps of forward + backward on this rank's GPU."""
     import torch
     import back_projection_ctp_b300 as ctp
 
@@ -241,7 +242,12 @@ def run_gpu(args, w, world, rank, local):
     vol_h = ci.phantom(w)
     y_h = ci.sinogram_noise(w)
     plan = ctp.ctp_plan(geometry_of(w, frames), volume_of(w), args.path)
-    segments = golden_segments(args.config)
+    if args.views is None:
+        segments = golden_segments(args.config)
+        seg_source = "float64 oracle (tests/golden/segment_counts.json)"
+    else:
+        segments = ctp.ctp_segment_count(plan)
+        seg_source = "plan counter (reduced-view scan)"
 
     stream = torch.cuda.current_stream(dev)
     d_vol = torch.from_numpy(vol_h).to(dev)
@@ -324,6 +330,7 @@ def run_gpu(args, w, world, rank, local):
             "config": {"workload": w.name, "shape_DHW": list(w.shape),
                        "spacing_DHW": list(w.spacing), "views": w.n_views,
                        "detector_vu": [w.n_v, w.n_u], "segments_per_pass": segments,
+                       "segments_from": seg_source,
                        "path": plan.path, "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (no flush)" if 4 * w.n_voxels > 126e6
                        else "inputs smaller than L2 (no flush)",
@@ -349,6 +356,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--views", type=int, default=None,
+                    help="replace the workload's number of views (same arc); for profiling "
+                         "captures of the same kernels on a shorter scan")
     ap.add_argument("--impl", default="ctp", choices=["ctp", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "ray", "column"])
     ap.add_argument("--ref-budget", type=float, default=15.0)
@@ -357,6 +367,9 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = ci.get(args.config)
+    if args.views is not None:
+        import dataclasses
+        w = dataclasses.replace(w, n_views=args.views, name=f"{w.name}_views{args.views}")
     world, rank, local = dist_setup(args.gpus)
     try:
         if args.impl == "reference":

@@ -121,7 +121,8 @@ int ctp_plan_info_get(const ctp_plan_t *plan, ctp_plan_info *info);
  * ctp_forward -- p = A f.  vol_dev: device float32 (nz, ny, nx), read only.
  * sino_dev: device float32 (n_views, n_v, n_u), fully overwritten (rays that
  * miss the volume get 0).  stream: a cudaStream_t (NULL = default stream).
- * The two buffers must not overlap.  Errors: CTP_E_NULL, CTP_E_DEVICE, CTP_E_CUDA.
+ * The two buffers must not overlap.  For a plan without rays both pointers may
+ * be NULL (nothing is done).  Errors: CTP_E_NULL, CTP_E_DEVICE, CTP_E_CUDA.
  */
 int ctp_forward(const ctp_plan_t *plan, const float *vol_dev, float *sino_dev, void *stream);
 
@@ -129,14 +130,17 @@ int ctp_forward(const ctp_plan_t *plan, const float *vol_dev, float *sino_dev, v
  * ctp_backward -- g = A^T y.  sino_dev: device float32 (n_views, n_v, n_u), read
  * only.  vol_dev: device float32 (nz, ny, nx), fully overwritten (zeroed, then
  * accumulated with float32 atomics, so the summation order -- not the set of
- * terms -- varies between calls).  Errors as ctp_forward.
+ * terms -- varies between calls).  sino_dev may be NULL for a plan without
+ * rays (vol_dev is then zeroed).  Errors as ctp_forward.
  */
 int ctp_backward(const ctp_plan_t *plan, const float *sino_dev, float *vol_dev, void *stream);
 
 /*
- * ctp_segment_count -- number of positive-length (ray, cell) pieces the plan's
- * traversal visits in one pass (identical for forward and backward).  *out is a
- * host value; the call waits for the stream.  Diagnostics and throughput units.
+ * ctp_segment_count -- number of (ray, cell) pieces longer than 1e-5 of the
+ * smallest cell width that the plan's traversal visits in one pass (the same for
+ * forward and backward).  The threshold drops only the rounding-sized pieces of
+ * rays that cross a cell edge or corner exactly.  *out is a host value; the call
+ * waits for the stream.  Diagnostics and throughput units.
  */
 int ctp_segment_count(const ctp_plan_t *plan, unsigned long long *out, void *stream);
 

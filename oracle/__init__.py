@@ -19,7 +19,8 @@ Functions and what pins them (the tests under ``tests/test_oracle_*.py``):
   same closed forms.
 * :func:`backward_voxels` -- voxel-driven transpose at chosen voxels; pinned by
   equality with :func:`backward` on small cases.
-* :func:`segment_count` -- positive-length pieces; pinned by :func:`brute_count`.
+* :func:`segment_count` -- pieces longer than 1e-5 of the smallest cell width
+  (the benchmark's unit); pinned by :func:`brute_count`.
 * :func:`ambiguous` -- rays lying on a cell-face plane; pinned on hand-built rays.
 """
 
@@ -79,9 +80,9 @@ def _load():
                 "ora_forward": [C, P, P, L, L, I],
                 "ora_forward_rays": [C, P, P, L, P, I],
                 "ora_backward": [C, P, P, L, L, I],
-                "ora_segment_count": [C, L, L, I, P],
+                "ora_segment_count": [C, L, L, I, D, P],
                 "ora_brute_forward": [C, P, P, I],
-                "ora_brute_count": [C, P, I],
+                "ora_brute_count": [C, D, P, I],
                 "ora_backward_voxels": [C, P, P, L, P, I],
                 "ora_ambiguous": [C, D, P, I],
                 "ora_supersampled": [C, P, P, L, L, P, I],
@@ -194,11 +195,23 @@ def backward_voxels(scan: Scan, sino, voxels, threads=0):
     return out
 
 
-def segment_count(scan: Scan, ray0=0, ray1=None, threads=0) -> int:
+SEGMENT_MIN_FRACTION = 1e-5
+
+
+def segment_min_len(scan: Scan) -> float:
+    """Counting threshold: 1e-5 of the smallest cell width.  Pieces shorter than
+    this are the degenerate ones of rays crossing a cell edge or corner exactly."""
+    return SEGMENT_MIN_FRACTION * min(scan.spacing)
+
+
+def segment_count(scan: Scan, ray0=0, ray1=None, threads=0, min_len=None) -> int:
+    """Pieces longer than ``min_len`` (default :func:`segment_min_len`; 0 counts
+    every positive-length piece) over rays [ray0, ray1)."""
     ray1 = scan.n_rays if ray1 is None else ray1
+    min_len = segment_min_len(scan) if min_len is None else float(min_len)
     out = ctypes.c_ulonglong(0)
-    _check(_load().ora_segment_count(scan.ref(), ray0, ray1, threads, ctypes.byref(out)),
-           "ora_segment_count")
+    _check(_load().ora_segment_count(scan.ref(), ray0, ray1, threads, min_len,
+                                     ctypes.byref(out)), "ora_segment_count")
     return int(out.value)
 
 
@@ -210,9 +223,11 @@ def brute_forward(scan: Scan, vol, threads=0):
     return out.reshape(scan.sino_shape)
 
 
-def brute_count(scan: Scan, threads=0) -> int:
+def brute_count(scan: Scan, threads=0, min_len=None) -> int:
+    min_len = segment_min_len(scan) if min_len is None else float(min_len)
     out = ctypes.c_ulonglong(0)
-    _check(_load().ora_brute_count(scan.ref(), ctypes.byref(out), threads), "ora_brute_count")
+    _check(_load().ora_brute_count(scan.ref(), min_len, ctypes.byref(out), threads),
+           "ora_brute_count")
     return int(out.value)
 
 

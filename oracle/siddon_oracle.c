@@ -312,8 +312,11 @@ int ora_backward(const ora_ctx *c, const float *sino, double *vol, long ray0, lo
     return err;
 }
 
-/* Number of positive-length (ray, cell) pieces over rays [ray0, ray1). */
-int ora_segment_count(const ora_ctx *c, long ray0, long ray1, int nthreads,
+/* Number of (ray, cell) pieces longer than min_len over rays [ray0, ray1).
+ * min_len = 0 counts every positive-length piece; a small positive min_len
+ * drops the numerically degenerate pieces of rays that cross a cell edge or
+ * corner exactly (length 0 in exact arithmetic, rounding-sized here). */
+int ora_segment_count(const ora_ctx *c, long ray0, long ray1, int nthreads, double min_len,
                       unsigned long long *out)
 {
     int T = ora_threads(nthreads);
@@ -334,8 +337,8 @@ int ora_segment_count(const ora_ctx *c, long ray0, long ray1, int nthreads,
             for (long ray = ray0; ray < ray1; ++ray) {
                 double X0[3], r[3], tlo, thi;
                 ora_ray(c, ray, X0, r, &tlo, &thi);
-                total += (unsigned long long)ora_trace(c, X0, r, tlo, thi, lo, c->n, buf,
-                                                       cells, lens);
+                int n = ora_trace(c, X0, r, tlo, thi, lo, c->n, buf, cells, lens);
+                for (int s = 0; s < n; ++s) total += lens[s] > min_len ? 1u : 0u;
             }
         }
         free(buf);
@@ -397,8 +400,8 @@ int ora_brute_forward(const ora_ctx *c, const float *vol, double *sino, int nthr
     return 0;
 }
 
-/* Brute-force segment count: cells with positive clipped length, per ray. */
-int ora_brute_count(const ora_ctx *c, unsigned long long *out, int nthreads)
+/* Brute-force segment count: cells whose clipped length exceeds min_len. */
+int ora_brute_count(const ora_ctx *c, double min_len, unsigned long long *out, int nthreads)
 {
     int T = ora_threads(nthreads);
     long nr = ora_n_rays(c);
@@ -412,7 +415,7 @@ int ora_brute_count(const ora_ctx *c, unsigned long long *out, int nthreads)
                 for (long i = 0; i < c->n[0]; ++i) {
                     double blo[3], bhi[3];
                     ora_cell_box(c, i, j, k, blo, bhi);
-                    if (ora_clip_box(X0, r, tlo, thi, blo, bhi) > 0.0) total++;
+                    if (ora_clip_box(X0, r, tlo, thi, blo, bhi) > min_len) total++;
                 }
     }
     *out = total;

@@ -169,6 +169,7 @@ def test_source_and_detector_inside_volume(torch, ctp, oracle_mod):
     u = np.tile([0.0, 1.0, 0.0], (n, 1))
     vv = np.tile([0.0, 0.0, 1.0], (n, 1))
     cen[:, 0] = src[:, 0] - rng.uniform(2, 5, n)
+    cen[:, 2] = src[:, 2]  # rows stay shallow (at most one z plane per slab)
     frames = dict(src=src, det_centre=cen, det_u=u, det_v=vv)
     scan, g, v = _custom(oracle_mod, "divergent", frames, (9, 10, 11), (1.0, 0.9, 0.8), 7, 5, 0.4, 0.5)
     _check_case(torch, ctp, oracle_mod, scan, g, v, paths=("ray", "column"))
