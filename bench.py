@@ -4,9 +4,9 @@
 One step = ctp_forward of the workload's phantom followed by ctp_backward of its
 N(0,1) sinogram (the whole hot path: ray set-up, traversal-gather, zero-fill,
 traversal-scatter).  Metric: giga ray-voxel segments per second, forward plus
-backward, where one pass holds the float64 oracle's count of positive-length
-(ray, cell) pieces (tests/golden/segment_counts.json; the plan's own counter
-agrees to 1e-6, tested).
+backward, where one pass holds the float64 oracle's count of (ray, cell) pieces
+longer than 1e-5 of the smallest cell width (tests/golden/segment_counts.json;
+the plan's own counter agrees to 1e-6, tested).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl reference]
 
