@@ -35,8 +35,8 @@ class _Geometry(ctypes.Structure):
                 ("n_u", ctypes.c_int), ("n_v", ctypes.c_int),
                 ("src", ctypes.c_void_p), ("det_centre", ctypes.c_void_p),
                 ("det_u", ctypes.c_void_p), ("det_v", ctypes.c_void_p),
-                ("pitch_u", ctypes.c_float), ("pitch_v", ctypes.c_float),
-                ("offset_u", ctypes.c_float), ("offset_v", ctypes.c_float)]
+                ("pitch_u", ctypes.c_double), ("pitch_v", ctypes.c_double),
+                ("offset_u", ctypes.c_double), ("offset_v", ctypes.c_double)]
 
 
 class _Volume(ctypes.Structure):

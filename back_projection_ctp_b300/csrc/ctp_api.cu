@@ -141,7 +141,7 @@ int validate(const ctp_geometry *g, const ctp_volume *v)
     }
     if (g->ndim == 2 && !(sp[2] > 0.0)) return CTP_E_SPACING;
     if (smax / smin > 1e4) return CTP_E_SPACING;
-    if (!(g->pitch_u > 0.0f) || !(g->pitch_v > 0.0f)) return CTP_E_SHAPE;
+    if (!(g->pitch_u > 0.0) || !(g->pitch_v > 0.0)) return CTP_E_SHAPE;
     if (g->n_views == 0) return CTP_OK;
     if (!g->src || !g->det_centre || !g->det_u || !g->det_v) return CTP_E_NULL;
 
@@ -252,8 +252,8 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
         ctp::ViewFrame &F = p->frames[s];
         for (int a = 0; a < 3; ++a) {
             const double d = p->spacing[a], o = p->origin[a];
-            const double pu = (double)geom->pitch_u * (double)U[a];
-            const double pv = (double)geom->pitch_v * (double)V[a];
+            const double pu = geom->pitch_u * (double)U[a];
+            const double pv = geom->pitch_v * (double)V[a];
             // pixel (0, 0) = centre - cu * pitch_u * u - cv * pitch_v * v
             const double p00 = (double)C[a] - cu * pu - cv * pv;
             F.p00[a] = (p00 - o) / d;

@@ -77,8 +77,8 @@ typedef struct ctp_geometry {
     const float *det_centre;  /* HOST (n_views, 3) */
     const float *det_u;       /* HOST (n_views, 3) unit u axis */
     const float *det_v;       /* HOST (n_views, 3) unit v axis (2-D: any vector not along u) */
-    float pitch_u, pitch_v;   /* detector pitch (physical units) */
-    float offset_u, offset_v; /* detector-centre offset in pixels */
+    double pitch_u, pitch_v;  /* detector pitch (physical units) */
+    double offset_u, offset_v;/* detector-centre offset in pixels */
 } ctp_geometry;
 
 typedef struct ctp_volume {

@@ -86,6 +86,7 @@ def _load():
                 "ora_backward_voxels": [C, P, P, L, P, I],
                 "ora_ambiguous": [C, D, P, I],
                 "ora_supersampled": [C, P, P, L, L, P, I],
+                "ora_trace_ray": [C, L, P, P],
             }
             for name, args in sigs.items():
                 fn = getattr(lib, name)
@@ -247,3 +248,15 @@ def supersampled(scan: Scan, vol, rays, samples, threads=0):
                                     int(samples), out.ctypes.data, threads),
            "ora_supersampled")
     return out
+
+
+def trace_ray(scan: Scan, ray: int):
+    """(cells, lengths) of one ray's positive-length pieces, in traversal order;
+    cells are linear indices (k * ny + j) * nx + i."""
+    n = sum(scan.shape) + 8
+    cells = np.zeros(n, dtype=np.int64)
+    lens = np.zeros(n, dtype=np.float64)
+    m = _load().ora_trace_ray(scan.ref(), int(ray), cells.ctypes.data, lens.ctypes.data)
+    if m < 0:
+        raise MemoryError("ora_trace_ray failed")
+    return cells[:m], lens[:m]

@@ -601,3 +601,19 @@ int ora_supersampled(const ora_ctx *c, const float *vol, const long *rays, long 
     }
     return 0;
 }
+
+/* The pieces of one ray: linear cell index and physical length of every
+ * positive-length piece, in traversal order.  cells / lens must hold
+ * nx + ny + nz + 8 entries.  Returns the number of pieces. */
+int ora_trace_ray(const ora_ctx *c, long ray, long *cells, double *lens)
+{
+    int B = ora_buf_len(c);
+    double *buf = (double *)malloc(sizeof(double) * B);
+    if (!buf) return -1;
+    double X0[3], r[3], tlo, thi;
+    int lo[3] = {0, 0, 0};
+    ora_ray(c, ray, X0, r, &tlo, &thi);
+    int n = ora_trace(c, X0, r, tlo, thi, lo, c->n, buf, cells, lens);
+    free(buf);
+    return n;
+}
