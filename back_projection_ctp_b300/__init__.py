@@ -3,13 +3,16 @@ matched backprojection) behind the C ABI of ``include/ctp.h``.
 
 The entry points carry the C names: :func:`ctp_plan`, :func:`ctp_forward`,
 :func:`ctp_backward`, :func:`ctp_segment_count`, :func:`ctp_forward_host`,
-:func:`ctp_backward_host`, :func:`ctp_destroy`, :func:`ctp_status_string`.
+:func:`ctp_backward_host`, :func:`ctp_destroy`, :func:`ctp_status_string`, and the
+allocation-free :func:`ctp_forward_static`.
 """
 
 from ._binding import (EXPORTS, CtpError, Geometry, Plan, Volume, ctp_backward,
-                       ctp_backward_host, ctp_destroy, ctp_forward, ctp_forward_host, ctp_plan,
-                       ctp_segment_count, ctp_status_string, load_library)
+                       ctp_backward_host, ctp_destroy, ctp_forward, ctp_forward_host,
+                       ctp_forward_static, ctp_plan, ctp_segment_count, ctp_status_string,
+                       load_library)
 
 __all__ = ["EXPORTS", "CtpError", "Geometry", "Plan", "Volume", "ctp_backward",
-           "ctp_backward_host", "ctp_destroy", "ctp_forward", "ctp_forward_host", "ctp_plan",
-           "ctp_segment_count", "ctp_status_string", "load_library"]
+           "ctp_backward_host", "ctp_destroy", "ctp_forward", "ctp_forward_host",
+           "ctp_forward_static", "ctp_plan", "ctp_segment_count", "ctp_status_string",
+           "load_library"]

@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <new>
 #include <vector>
 
@@ -423,3 +424,115 @@ int ctp_backward_host(ctp_plan_t *plan, const float *sino_host, float *vol_host,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free forward projection.
+//
+// For callers that may not allocate device memory once they run: an application
+// whose device memory belongs to its own pool allocator (a raw cudaMalloc there
+// would take memory behind the pool's back and can fail when the pool has
+// reserved the rest), or a loop that must not take cudaMalloc / cudaFree's
+// implicit device synchronisation.  ctp_plan allocates its tables; this entry
+// point keeps its only scratch -- the per-view frame table of the ray path --
+// in a fixed file-scope device array instead.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kStaticMaxViews = 4096;   // 4096 frames x 96 B = 384 KiB per device
+constexpr int kStaticMaxDevices = 64;
+constexpr int kStaticChunk = 32;        // frames staged per host-to-device copy
+
+// Shared by every call on a device and held by every device that loads the
+// library until the process exits; keeps the last call's frames.
+static __device__ __align__(256) ctp::ViewFrame g_static_frames[kStaticMaxViews];
+
+std::atomic<void *> g_static_frames_addr[kStaticMaxDevices];
+
+// Device address of g_static_frames on the current device (looked up once per
+// device; host code may not use the symbol itself as a device pointer).
+int static_frames_address(int device, ctp::ViewFrame **out)
+{
+    void *ptr = g_static_frames_addr[device].load(std::memory_order_acquire);
+    if (!ptr) {
+        if (cudaGetSymbolAddress(&ptr, g_static_frames) != cudaSuccess || !ptr)
+            return CTP_E_CUDA;
+        g_static_frames_addr[device].store(ptr, std::memory_order_release);
+    }
+    *out = static_cast<ctp::ViewFrame *>(ptr);
+    return CTP_OK;
+}
+
+// Per-view frame in cell coordinates, the same arithmetic as ctp_plan's.
+void static_frame(const ctp_geometry *g, const ctp_volume *v, int s, ctp::ViewFrame *F)
+{
+    const double spacing[3] = {v->dx, v->dy, v->dz};
+    const double origin[3] = {v->ox, v->oy, v->oz};
+    const double cu = 0.5 * (g->n_u - 1) - g->offset_u;
+    const double cv = 0.5 * (g->n_v - 1) - g->offset_v;
+    const float *S = g->src + 3 * s, *C = g->det_centre + 3 * s;
+    const float *U = g->det_u + 3 * s, *V = g->det_v + 3 * s;
+    for (int a = 0; a < 3; ++a) {
+        const double d = spacing[a], o = origin[a];
+        const double pu = g->pitch_u * (double)U[a];
+        const double pv = g->pitch_v * (double)V[a];
+        const double p00 = (double)C[a] - cu * pu - cv * pv;
+        F->p00[a] = (p00 - o) / d;
+        F->du[a] = pu / d;
+        F->dv[a] = pv / d;
+        F->a[a] = g->beam == CTP_DIVERGENT ? ((double)S[a] - o) / d : (double)S[a] / d;
+    }
+}
+
+}  // namespace
+
+extern "C" int ctp_forward_static(const ctp_geometry *geom, const ctp_volume *vol,
+                                  const float *vol_dev, float *sino_dev, void *stream)
+{
+    if (!geom || !vol) return CTP_E_NULL;
+    int st = validate(geom, vol);
+    if (st != CTP_OK) return st;
+    if (geom->n_views > kStaticMaxViews) return CTP_E_LIMIT;
+    if (geom->n_views == 0) return CTP_OK;
+    if (!vol_dev || !sino_dev) return CTP_E_NULL;
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return CTP_E_CUDA;
+    if (device < 0 || device >= kStaticMaxDevices) return CTP_E_LIMIT;
+    ctp::ViewFrame *frames = nullptr;
+    if ((st = static_frames_address(device, &frames)) != CTP_OK) return st;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    ctp::ViewFrame chunk[kStaticChunk];
+    for (int s0 = 0; s0 < geom->n_views; s0 += kStaticChunk) {
+        const int n = geom->n_views - s0 < kStaticChunk ? geom->n_views - s0 : kStaticChunk;
+        for (int q = 0; q < n; ++q) static_frame(geom, vol, s0 + q, &chunk[q]);
+        // pageable source: the call returns once `chunk` has been staged
+        if (cudaMemcpyAsync(frames + s0, chunk, sizeof(ctp::ViewFrame) * n,
+                            cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return CTP_E_CUDA;
+    }
+
+    ctp::RayParams P{};
+    P.views = frames;
+    P.beam = geom->beam;
+    P.n_u = geom->n_u;
+    P.n_v = geom->n_v;
+    P.n_views = geom->n_views;
+    P.n[0] = vol->nx;
+    P.n[1] = vol->ny;
+    P.n[2] = vol->nz;
+    P.spacing[0] = vol->dx;
+    P.spacing[1] = vol->dy;
+    P.spacing[2] = vol->dz;
+    P.stride[0] = 1;
+    P.stride[1] = vol->nx;
+    P.stride[2] = vol->nx * vol->ny;
+    P.min_len = (float)(1e-5 * std::fmin(vol->dx, std::fmin(vol->dy, vol->dz)));
+    if (geom->n_v == 1) {
+        dim3 grid((geom->n_u + 127) / 128, geom->n_views, 1);
+        ctp::ray_forward_kernel<128, 1><<<grid, 128, 0, s>>>(P, vol_dev, sino_dev);
+    } else {
+        dim3 grid((geom->n_u + 31) / 32, geom->n_views, (geom->n_v + 3) / 4);
+        ctp::ray_forward_kernel<32, 4><<<grid, 128, 0, s>>>(P, vol_dev, sino_dev);
+    }
+    return cudaGetLastError() == cudaSuccess ? CTP_OK : CTP_E_CUDA;
+}

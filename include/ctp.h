@@ -154,6 +154,29 @@ int ctp_segment_count(const ctp_plan_t *plan, unsigned long long *out, void *str
 int ctp_forward_host(ctp_plan_t *plan, const float *vol_host, float *sino_host, void *stream);
 int ctp_backward_host(ctp_plan_t *plan, const float *sino_host, float *vol_host, void *stream);
 
+/*
+ * ctp_forward_static -- p = A f without any allocation, for callers that may not
+ * allocate device memory while they run: applications whose device memory is
+ * owned by their own pool allocator (a raw cudaMalloc would bypass the pool's
+ * budget and can fail once the pool has reserved the rest), and loops that must
+ * not take the implicit device synchronisation of cudaMalloc / cudaFree.  The
+ * reference has no counterpart; the result equals ctp_forward of a RAY-path plan
+ * of the same scan.
+ * geom, vol: host structs as for ctp_plan (validated the same way, same error
+ * codes).  vol_dev / sino_dev: device float32 buffers as for ctp_forward (may be
+ * NULL when n_views is 0).  stream: a cudaStream_t (NULL = default stream).
+ * Scratch: the per-view frame table lives in a fixed device array of
+ * 4096 views (384 KiB) that every device loading the library holds until exit;
+ * n_views above 4096 returns CTP_E_LIMIT, and so does a current device ordinal
+ * of 64 or more.  The first call on a device looks the array up
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call rewrites the frames it uses from the host and reads nothing left
+ * by earlier calls; calls that overlap on the GPU (other streams, other host
+ * threads) share the array and race.  Calls no cudaMalloc / cudaFree.
+ */
+int ctp_forward_static(const ctp_geometry *geom, const ctp_volume *vol, const float *vol_dev,
+                       float *sino_dev, void *stream);
+
 /* Static English text of a status code. */
 const char *ctp_status_string(int status);
 
