@@ -15,7 +15,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/ctp.h"
+#include "ctp.h"
 #include "ctp_column.cuh"
 #include "ctp_internal.h"
 #include "ctp_ray.cuh"

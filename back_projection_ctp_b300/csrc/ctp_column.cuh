@@ -19,6 +19,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cstdlib>
 #include <cuda_runtime.h>
 
 #include "ctp_internal.h"
@@ -43,6 +44,8 @@ struct ColumnTrace {
 
 struct ColumnPlan {
     int n_columns;       // n_views * n_u
+    int rows_fwd;        // detector rows per thread of the forward (1, 2 or 4)
+    int rows_bwd;        // ... of the backward and the counter
 };
 
 // Zero halo (cells) around x and y of the padded working copies: the walk's
@@ -178,198 +181,292 @@ __global__ void column_setup_kernel(RayParams P, ColumnTrace *__restrict__ T,
     T[col] = C;
 }
 
-// Per-lane z state: the row's own transverse axis of the slab walk.
-struct LaneZ {
-    uint32_t fz, bz;     // z fraction at slab k0 and slope (2^-32 cell units), mirrored
-    float ibz;           // 1 / bz
-    int jz;              // mirrored z index at slab k0
-    int sz;              // +-1: z stride in the padded z-fastest copy
-    int addr;            // padded offset of cell (k0, jb, jz)
+// Per-row z state: each row's own transverse axis of the slab walk.
+struct RowZ {
+    uint32_t fz, bz;     // mirrored z fraction at slab k0 and slope (2^-32 cell units)
+    float ibz;           // 1 / bz (0 when the row never crosses a z plane)
+    int zoff;            // z index of the current cell (inside the grid iff 0 <= zoff < nz)
+    int sz;              // +-1: step of zoff at a z crossing
     float ell;           // physical length per slab
+    int kin, kout;       // slabs k in [kin, kout]: the row and its next z cell are inside
 };
 
-// Lane set-up: the column's xy state plus this row's z line (float64: about
-// ten operations per lane; the shared xy part was built at plan time).
-__device__ __forceinline__ LaneZ column_lane_setup(const RayParams &P, const ColumnTrace &C,
-                                                   int iv)
+// A row that contributes nothing (beyond the detector, or zero weight): it stays
+// in z cell 0 (a valid address) and its weight / result is zero or discarded.
+__device__ __forceinline__ RowZ column_row_idle()
 {
-    LaneZ L;
+    RowZ Z;
+    Z.fz = 0;
+    Z.bz = 0;
+    Z.ibz = 0.0f;
+    Z.zoff = 0;
+    Z.sz = 1;
+    Z.ell = 0.0f;
+    Z.kin = -(1 << 30);
+    Z.kout = 1 << 30;
+    return Z;
+}
+
+// Row set-up: this row's z line at the column's first slab (float64, about ten
+// operations; the shared xy part was built at plan time).
+__device__ __forceinline__ RowZ column_row_setup(const RayParams &P, const ColumnTrace &C, int iv)
+{
+    RowZ Z;
     const double z = __fma_rn((double)iv, C.zd, C.zc);
     const double bz = __fma_rn((double)iv, C.bd, C.bc);
     const bool m = bz < 0.0;
     const double zm = m ? __dsub_rn((double)P.n[2], z) : z;
     const double abz = fabs(bz);
     // rows far outside the grid in z touch no cell; bound their index so the
-    // walk's integer address arithmetic stays small
+    // walk's integer arithmetic stays small
     const double zcl = fmin(fmax(zm, -65536.0), (double)P.n[2] + 65536.0);
     const double fjz = floor(zcl);
-    L.jz = (int)fjz;
-    L.fz = (uint32_t)__dmul_rn(__dsub_rn(zcl, fjz), 4294967296.0);
-    L.bz = to_fixed_slope(abz);
-    L.ibz = L.bz ? __frcp_rn((float)L.bz) : 0.0f;
-    L.sz = m ? -1 : 1;
-    L.addr = C.addr_xy + (m ? (P.n[2] - 1) : 0) + L.sz * L.jz;
+    const int jz = (int)fjz;
+    Z.fz = (uint32_t)__dmul_rn(__dsub_rn(zcl, fjz), 4294967296.0);
+    Z.bz = to_fixed_slope(abz);
+    Z.ibz = Z.bz ? __frcp_rn((float)Z.bz) : 0.0f;
+    Z.sz = m ? -1 : 1;
+    Z.zoff = m ? P.n[2] - 1 - jz : jz;
     const float dz = (float)(abz * P.spacing[2]);
-    L.ell = __fsqrt_rn(__fadd_rn(C.lxy2, __fmul_rn(dz, dz)));
-    return L;
+    Z.ell = __fsqrt_rn(__fadd_rn(C.lxy2, __fmul_rn(dz, dz)));
+    // Slabs k where the walk's mirrored z index j(k) and j(k+1) are both in
+    // [0, nz).  The walk follows zm + (k - k0) |bz| to within 6e-8 cell (slope
+    // quantised to 2^-33 over at most 512 slabs, start to 2^-32), so the line
+    // itself is required to stay 1e-6 cell inside: j(k) >= 0 once
+    // zm + (k - k0) |bz| >= 1e-6, and j(k+1) < nz while
+    // zm + (k + 1 - k0) |bz| <= nz - 1e-6.  A row with slope 0 keeps
+    // j = floor(zm) exactly.
+    const double nz = (double)P.n[2];
+    const double margin = 1e-6;
+    double kin, kout;
+    if (abz > 0.0) {
+        const double inv = __drcp_rn(abz);
+        kin = zm >= margin ? (double)C.k0 : (double)C.k0 + ceil((margin - zm) * inv);
+        kout = (double)C.k0 - 1.0 + floor((nz - margin - zm) * inv);
+    } else {
+        const bool inside = zcl >= 0.0 && zcl < nz;
+        kin = inside ? -1e9 : 1e9;
+        kout = inside ? 1e9 : -1e9;
+    }
+    Z.kin = (int)fmin(fmax(kin, -1e9), 1e9);
+    Z.kout = (int)fmin(fmax(kout, -1e9), 1e9);
+    return Z;
 }
 
-// One slab of the column walk.  The b (xy) crossing is the same for every lane
-// of a warp (one column per warp), so the branch on it does not diverge; the
-// common slab without it holds one or two pieces, split only by the lane's own
-// z crossing.  A crossing's slab fraction comes from the wrapped sum g of the
-// fixed-point add: t = (beta - g) / beta = 1 - g / beta.  CLAMP restricts the
-// slab to [lo, hi] (first / last slab of a ray that starts or ends inside).
-// op(addr, length, on, jb) sees every piece; `on` = the piece lies inside the
-// grid in z (x and y are covered by the halo); jb lets the counter test x / y.
-template <bool CLAMP, class Op>
+// One slab of the column walk for the R rows a thread owns.  The b (xy)
+// crossing is the same for every row of the column, so the branch on it is
+// taken by the whole warp and its cost is shared by the R rows; the common slab
+// holds one or two pieces per row, split only by the row's own z crossing.  A
+// crossing's slab fraction comes from the wrapped sum g of the fixed-point add:
+// t = (beta - g) / beta = 1 - g / beta.  CLAMP restricts the slab to [lo, hi]
+// (first / last slab of rays that start or end inside).  op(r, addr, length,
+// on, jb) sees every piece of row r; `on` = inside the grid in z (x and y are
+// covered by the zero halo), jb lets the counter test x / y.
+template <int R, bool CLAMP, bool CHECK, class Op>
 __device__ __forceinline__ void column_slab(uint32_t &fb, uint32_t bb, float ib, int &jb, int sb,
-                                            uint32_t &fz, uint32_t bz, float ibz, int &jz,
-                                            int sz, unsigned nz, int &addr, int sp, float lo,
+                                            int &xy, int sp, RowZ (&Z)[R], unsigned nz, float lo,
                                             float hi, Op &op)
 {
-    const uint32_t gz = fz + bz;
-    const bool cz = gz < fz;
-    const float tz = cz ? fmaxf(__fmaf_rn(-__uint2float_rn(gz), ibz, 1.0f), 0.0f) : 1.0f;
-    const bool v0 = (unsigned)jz < nz;
-    const bool v1 = (unsigned)(jz + 1) < nz;
     const uint32_t gb = fb + bb;
     const bool cb = gb < fb;
     if (!cb) {
-        float e = tz;
-        if (CLAMP) e = fminf(fmaxf(e, lo), hi);
-        const float d0 = CLAMP ? __fsub_rn(e, lo) : e;
-        const float d1 = __fsub_rn(CLAMP ? hi : 1.0f, e);
-        op(addr, d0, v0, jb);
-        op(addr + sz, d1, cz && v1, jb);
-        addr += sp + (cz ? sz : 0);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t gz = Z[r].fz + Z[r].bz;
+            const bool cz = gz < Z[r].fz;
+            float e = cz ? fmaxf(__fmaf_rn(-__uint2float_rn(gz), Z[r].ibz, 1.0f), 0.0f) : 1.0f;
+            if (CLAMP) e = fminf(fmaxf(e, lo), hi);
+            const float d0 = CLAMP ? __fsub_rn(e, lo) : e;
+            const float d1 = __fsub_rn(CLAMP ? hi : 1.0f, e);
+            const int z1 = Z[r].zoff + Z[r].sz;
+            op(r, xy + Z[r].zoff, d0, !CHECK || (unsigned)Z[r].zoff < nz, jb);
+            op(r, xy + z1, d1, cz && (!CHECK || (unsigned)z1 < nz), jb);
+            Z[r].fz = gz;
+            if (cz) Z[r].zoff = z1;
+        }
+        xy += sp;
     } else {
         const float tb = fmaxf(__fmaf_rn(-__uint2float_rn(gb), ib, 1.0f), 0.0f);
-        const bool bfirst = tb < tz;
-        float e1 = fminf(tb, tz), e2 = fmaxf(tb, tz);
-        if (CLAMP) {
-            e1 = fminf(fmaxf(e1, lo), hi);
-            e2 = fminf(fmaxf(e2, lo), hi);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t gz = Z[r].fz + Z[r].bz;
+            const bool cz = gz < Z[r].fz;
+            const float tz =
+                cz ? fmaxf(__fmaf_rn(-__uint2float_rn(gz), Z[r].ibz, 1.0f), 0.0f) : 1.0f;
+            const bool bfirst = tb < tz;
+            float e1 = fminf(tb, tz), e2 = fmaxf(tb, tz);
+            if (CLAMP) {
+                e1 = fminf(fmaxf(e1, lo), hi);
+                e2 = fminf(fmaxf(e2, lo), hi);
+            }
+            const float d1 = CLAMP ? __fsub_rn(e1, lo) : e1;
+            const float d2 = __fsub_rn(e2, e1);
+            const float d3 = __fsub_rn(CLAMP ? hi : 1.0f, e2);
+            const int z0 = Z[r].zoff, z1 = z0 + Z[r].sz;
+            const bool v0 = !CHECK || (unsigned)z0 < nz, v1 = !CHECK || (unsigned)z1 < nz;
+            op(r, xy + z0, d1, v0, jb);
+            op(r, bfirst ? xy + sb + z0 : xy + z1, d2, bfirst ? v0 : v1, bfirst ? jb + 1 : jb);
+            op(r, xy + sb + z1, d3, cz && v1, jb + 1);
+            Z[r].fz = gz;
+            if (cz) Z[r].zoff = z1;
         }
-        const float d1 = CLAMP ? __fsub_rn(e1, lo) : e1;
-        const float d2 = __fsub_rn(e2, e1);
-        const float d3 = __fsub_rn(CLAMP ? hi : 1.0f, e2);
-        const int a3 = addr + sb + (cz ? sz : 0);
-        op(addr, d1, v0, jb);
-        op(addr + (bfirst ? sb : sz), d2, bfirst ? v0 : v1, bfirst ? jb + 1 : jb);
-        op(a3, d3, cz && v1, jb + 1);
-        addr = a3 + sp;
+        xy += sp + sb;
         jb += 1;
     }
-    fz = gz;
-    jz += cz ? 1 : 0;
     fb = gb;
 }
 
-// Walk all slabs of one lane: partial first / last slab peeled off, the main
-// loop without clamps.
-template <class Op>
-__device__ __forceinline__ void column_walk(const ColumnTrace &C, const LaneZ &L, unsigned nz,
+// Walk all slabs of a column for R rows: partial first / last slab peeled off;
+// between them the slabs where every row of the warp is inside the grid in z
+// (ka..kb) run without validity tests, the others with them.
+template <int R, class Op>
+__device__ __forceinline__ void column_walk(const ColumnTrace &C, RowZ (&Z)[R], unsigned nz,
                                             Op &op)
 {
-    uint32_t fb = C.fb, fz = L.fz;
-    int jb = C.jb, jz = L.jz, addr = L.addr;
-    const uint32_t bb = C.bb, bz = L.bz;
-    const float ib = C.ib, ibz = L.ibz;
-    const int sb = C.sb, sp = C.sp, sz = L.sz;
-    column_slab<true>(fb, bb, ib, jb, sb, fz, bz, ibz, jz, sz, nz, addr, sp, C.tlo,
-                      C.k0 == C.k1 ? C.thi : 1.0f, op);
-    for (int k = C.k0 + 1; k < C.k1; ++k)
-        column_slab<false>(fb, bb, ib, jb, sb, fz, bz, ibz, jz, sz, nz, addr, sp, 0.0f, 1.0f, op);
+    uint32_t fb = C.fb;
+    int jb = C.jb, xy = C.addr_xy;
+    const uint32_t bb = C.bb;
+    const float ib = C.ib;
+    const int sb = C.sb, sp = C.sp;
+    int kin = -(1 << 30), kout = 1 << 30;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        kin = max(kin, Z[r].kin);
+        kout = min(kout, Z[r].kout);
+    }
+    const int ka = max(__reduce_max_sync(0xffffffffu, kin), C.k0 + 1);
+    const int kb = min(__reduce_min_sync(0xffffffffu, kout), C.k1 - 1);
+    column_slab<R, true, true>(fb, bb, ib, jb, sb, xy, sp, Z, nz, C.tlo,
+                               C.k0 == C.k1 ? C.thi : 1.0f, op);
+    int k = C.k0 + 1;
+    if (ka <= kb) {
+        for (; k < ka; ++k)
+            column_slab<R, false, true>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
+        for (; k <= kb; ++k)
+            column_slab<R, false, false>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
+    }
+    for (; k < C.k1; ++k)
+        column_slab<R, false, true>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
     if (C.k1 > C.k0)
-        column_slab<true>(fb, bb, ib, jb, sb, fz, bz, ibz, jz, sz, nz, addr, sp, 0.0f, C.thi, op);
+        column_slab<R, true, true>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, C.thi, op);
 }
 
+template <int R>
 struct ColumnGather {
     const float *__restrict__ vol;
-    float acc;
-    __device__ __forceinline__ void operator()(int a, float d, bool on, int)
+    float acc[R];
+    __device__ __forceinline__ void operator()(int r, int a, float d, bool on, int)
     {
-        if (on) acc = __fmaf_rn(d, __ldg(vol + a), acc);
+        if (on) acc[r] = __fmaf_rn(d, __ldg(vol + a), acc[r]);
     }
 };
 
+template <int R>
 struct ColumnScatter {
     float *__restrict__ vol;
-    float w;  // ell * y
-    __device__ __forceinline__ void operator()(int a, float d, bool on, int)
+    float w[R];  // ell * y of each row
+    __device__ __forceinline__ void operator()(int r, int a, float d, bool on, int)
     {
-        if (on && d > 0.0f) atomicAdd(vol + a, __fmul_rn(d, w));
+        if (on && d > 0.0f && w[r] != 0.0f) atomicAdd(vol + a, __fmul_rn(d, w[r]));
     }
 };
 
+template <int R>
 struct ColumnCount {
     unsigned n;
-    float thr;
+    float thr[R];
     unsigned nb;
-    __device__ __forceinline__ void operator()(int, float d, bool on, int jb)
+    __device__ __forceinline__ void operator()(int r, int, float d, bool on, int jb)
     {
-        n += (on && (unsigned)jb < nb && d > thr) ? 1u : 0u;
+        n += (on && (unsigned)jb < nb && d > thr[r]) ? 1u : 0u;
     }
 };
 
-constexpr int kColumnsPerBlock = 8;  // 8 warps: 8 columns x 32 rows
+constexpr int kColumnsPerBlock = 8;  // 8 warps: 8 columns, each 32 * R rows
 
-__global__ void __launch_bounds__(256) column_forward_kernel(RayParams P,
+// Rows a thread owns: iv = band * 32R + 32 r + lane, r < R (each load or atomic
+// instruction then covers 32 adjacent rows).
+template <int R>
+__global__ void __launch_bounds__(256, 5) column_forward_kernel(RayParams P,
                                                              const ColumnTrace *__restrict__ T,
                                                              const float *__restrict__ zvol,
                                                              float *__restrict__ sino)
 {
-    __shared__ float tile[32][kColumnsPerBlock + 1];
+    __shared__ float tile[32 * R][kColumnsPerBlock + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int iu = blockIdx.x * kColumnsPerBlock + warp;
     const int view = blockIdx.y;
-    const int iv = blockIdx.z * 32 + lane;
-    float out = 0.0f;
-    if (iu < P.n_u && iv < P.n_v) {
+    const int row0 = blockIdx.z * 32 * R + lane;
+    float out[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) out[r] = 0.0f;
+    if (iu < P.n_u) {
         const ColumnTrace C = T[(long long)view * P.n_u + iu];
         if (C.k0 <= C.k1) {
-            const LaneZ L = column_lane_setup(P, C, iv);
-            ColumnGather op{zvol, 0.0f};
-            column_walk(C, L, (unsigned)P.n[2], op);
-            out = __fmul_rn(op.acc, L.ell);
+            RowZ Z[R];
+            ColumnGather<R> op;
+            op.vol = zvol;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int iv = row0 + 32 * r;
+                Z[r] = iv < P.n_v ? column_row_setup(P, C, iv) : column_row_idle();
+                op.acc[r] = 0.0f;
+            }
+            column_walk<R>(C, Z, (unsigned)P.n[2], op);
+#pragma unroll
+            for (int r = 0; r < R; ++r) out[r] = __fmul_rn(op.acc[r], Z[r].ell);
         }
     }
-    tile[lane][warp] = out;
+#pragma unroll
+    for (int r = 0; r < R; ++r) tile[lane + 32 * r][warp] = out[r];
     __syncthreads();
-    const int r = threadIdx.x / kColumnsPerBlock, c = threadIdx.x % kColumnsPerBlock;
-    const int ivw = blockIdx.z * 32 + r, iuw = blockIdx.x * kColumnsPerBlock + c;
-    if (ivw < P.n_v && iuw < P.n_u)
-        sino[((long long)view * P.n_v + ivw) * P.n_u + iuw] = tile[r][c];
+    for (int e = threadIdx.x; e < 32 * R * kColumnsPerBlock; e += 256) {
+        const int rr = e / kColumnsPerBlock, c = e % kColumnsPerBlock;
+        const int ivw = blockIdx.z * 32 * R + rr, iuw = blockIdx.x * kColumnsPerBlock + c;
+        if (ivw < P.n_v && iuw < P.n_u)
+            sino[((long long)view * P.n_v + ivw) * P.n_u + iuw] = tile[rr][c];
+    }
 }
 
+template <int R>
 __global__ void __launch_bounds__(256) column_backward_kernel(RayParams P,
                                                               const ColumnTrace *__restrict__ T,
                                                               const float *__restrict__ sino,
                                                               float *__restrict__ zvol)
 {
-    __shared__ float tile[32][kColumnsPerBlock + 1];
+    __shared__ float tile[32 * R][kColumnsPerBlock + 1];
     const int view = blockIdx.y;
-    {
-        const int r = threadIdx.x / kColumnsPerBlock, c = threadIdx.x % kColumnsPerBlock;
-        const int ivr = blockIdx.z * 32 + r, iur = blockIdx.x * kColumnsPerBlock + c;
-        tile[r][c] = (ivr < P.n_v && iur < P.n_u)
-                         ? sino[((long long)view * P.n_v + ivr) * P.n_u + iur]
-                         : 0.0f;
+    for (int e = threadIdx.x; e < 32 * R * kColumnsPerBlock; e += 256) {
+        const int rr = e / kColumnsPerBlock, c = e % kColumnsPerBlock;
+        const int ivr = blockIdx.z * 32 * R + rr, iur = blockIdx.x * kColumnsPerBlock + c;
+        tile[rr][c] = (ivr < P.n_v && iur < P.n_u)
+                          ? sino[((long long)view * P.n_v + ivr) * P.n_u + iur]
+                          : 0.0f;
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int iu = blockIdx.x * kColumnsPerBlock + warp;
-    const int iv = blockIdx.z * 32 + lane;
-    const float y = tile[lane][warp];
-    if (iu >= P.n_u || iv >= P.n_v || y == 0.0f) return;
+    if (iu >= P.n_u) return;
     const ColumnTrace C = T[(long long)view * P.n_u + iu];
     if (C.k0 > C.k1) return;
-    const LaneZ L = column_lane_setup(P, C, iv);
-    ColumnScatter op{zvol, __fmul_rn(L.ell, y)};
-    column_walk(C, L, (unsigned)P.n[2], op);
+    const int row0 = blockIdx.z * 32 * R + lane;
+    RowZ Z[R];
+    ColumnScatter<R> op;
+    op.vol = zvol;
+    bool any = false;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int iv = row0 + 32 * r;
+        const float y = tile[lane + 32 * r][warp];
+        Z[r] = (iv < P.n_v && y != 0.0f) ? column_row_setup(P, C, iv) : column_row_idle();
+        op.w[r] = __fmul_rn(Z[r].ell, y);
+        any |= op.w[r] != 0.0f;
+    }
+    if (!__any_sync(0xffffffffu, any)) return;
+    column_walk<R>(C, Z, (unsigned)P.n[2], op);
 }
 
+template <int R>
 __global__ void __launch_bounds__(256) column_count_kernel(RayParams P,
                                                            const ColumnTrace *__restrict__ T,
                                                            unsigned long long *__restrict__ total)
@@ -377,14 +474,22 @@ __global__ void __launch_bounds__(256) column_count_kernel(RayParams P,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int iu = blockIdx.x * kColumnsPerBlock + warp;
     const int view = blockIdx.y;
-    const int iv = blockIdx.z * 32 + lane;
+    const int row0 = blockIdx.z * 32 * R + lane;
     unsigned n = 0;
-    if (iu < P.n_u && iv < P.n_v) {
+    if (iu < P.n_u) {
         const ColumnTrace C = T[(long long)view * P.n_u + iu];
         if (C.k0 <= C.k1) {
-            const LaneZ L = column_lane_setup(P, C, iv);
-            ColumnCount op{0u, __fdiv_rn(P.min_len, L.ell), (unsigned)C.nb};
-            column_walk(C, L, (unsigned)P.n[2], op);
+            RowZ Z[R];
+            ColumnCount<R> op;
+            op.n = 0u;
+            op.nb = (unsigned)C.nb;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int iv = row0 + 32 * r;
+                Z[r] = iv < P.n_v ? column_row_setup(P, C, iv) : column_row_idle();
+                op.thr[r] = Z[r].ell > 0.0f ? __fdiv_rn(P.min_len, Z[r].ell) : 3.0e38f;
+            }
+            column_walk<R>(C, Z, (unsigned)P.n[2], op);
             n = op.n;
         }
     }
@@ -438,6 +543,22 @@ inline size_t column_padded_cells(const RayParams &P)
     return ((size_t)P.n[0] + 2 * kHalo) * ((size_t)P.n[1] + 2 * kHalo) * (size_t)P.n[2];
 }
 
+// Rows per thread.  The shared xy walk is paid once per R rows, at the cost of
+// registers.  The forward gather waits on L2 and wants occupancy: it runs 5
+// blocks of 256 threads per SM (<= 48 registers, a few spilled) with 4 rows.
+// The backward is bound by its atomics' L1/L2 throughput and runs 2 rows
+// without a register cap.  CTP_COLUMN_ROWS_FWD / CTP_COLUMN_ROWS_BWD = 1, 2 or 4
+// override the choice.
+inline int column_rows(const RayParams &P, const char *env_name, int preferred)
+{
+    const char *env = getenv(env_name);
+    if (env && (env[0] == '1' || env[0] == '2' || env[0] == '4') && env[1] == '\0')
+        return env[0] - '0';
+    int r = preferred;
+    while (r > 1 && P.n_v < 24 * r) r /= 2;
+    return r;
+}
+
 // Builds the column table and the two padded working copies (forward: halo
 // zeroed once here and never written again; backward: zeroed per call).
 // Returns 0, 9 (CUDA error) or 11 (scan not eligible for the column path).
@@ -447,6 +568,8 @@ inline int column_plan_build(const RayParams &P, ColumnPlan *plan, void **d_colu
     if ((long long)P.n_views * P.n_u >= (1LL << 31)) return 11;
     if (column_padded_cells(P) >= (1ULL << 31)) return 11;
     plan->n_columns = P.n_views * P.n_u;
+    plan->rows_fwd = column_rows(P, "CTP_COLUMN_ROWS_FWD", 4);
+    plan->rows_bwd = column_rows(P, "CTP_COLUMN_ROWS_BWD", 2);
     const size_t cbytes = sizeof(ColumnTrace) * (size_t)(plan->n_columns > 0 ? plan->n_columns : 1);
     const size_t vbytes = sizeof(float) * column_padded_cells(P);
     int *d_flag = nullptr;
@@ -472,9 +595,10 @@ inline int column_plan_build(const RayParams &P, ColumnPlan *plan, void **d_colu
     return 0;
 }
 
-inline dim3 column_grid(const RayParams &P)
+inline dim3 column_grid(const RayParams &P, int R)
 {
-    return dim3((P.n_u + kColumnsPerBlock - 1) / kColumnsPerBlock, P.n_views, (P.n_v + 31) / 32);
+    return dim3((P.n_u + kColumnsPerBlock - 1) / kColumnsPerBlock, P.n_views,
+                (P.n_v + 32 * R - 1) / (32 * R));
 }
 
 inline dim3 transpose_grid(const RayParams &P)
@@ -482,31 +606,42 @@ inline dim3 transpose_grid(const RayParams &P)
     return dim3((P.n[0] + 31) / 32, (P.n[2] + 31) / 32, P.n[1]);
 }
 
-inline int column_forward(const RayParams &P, const ColumnPlan &, const void *d_columns,
+inline int column_forward(const RayParams &P, const ColumnPlan &plan, const void *d_columns,
                           float *d_zfwd, const float *vol, float *sino, cudaStream_t s)
 {
     xfast_to_zfast_kernel<<<transpose_grid(P), 256, 0, s>>>(vol, d_zfwd, P.n[0], P.n[1], P.n[2]);
-    column_forward_kernel<<<column_grid(P), 256, 0, s>>>(P, (const ColumnTrace *)d_columns, d_zfwd,
-                                                        sino);
+    const ColumnTrace *T = (const ColumnTrace *)d_columns;
+    const int R = plan.rows_fwd;
+    if (R == 4) column_forward_kernel<4><<<column_grid(P, 4), 256, 0, s>>>(P, T, d_zfwd, sino);
+    else if (R == 2) column_forward_kernel<2><<<column_grid(P, 2), 256, 0, s>>>(P, T, d_zfwd, sino);
+    else column_forward_kernel<1><<<column_grid(P, 1), 256, 0, s>>>(P, T, d_zfwd, sino);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 
-inline int column_backward(const RayParams &P, const ColumnPlan &, const void *d_columns,
+inline int column_backward(const RayParams &P, const ColumnPlan &plan, const void *d_columns,
                            float *d_zbwd, const float *sino, float *vol, cudaStream_t s)
 {
     if (cudaMemsetAsync(d_zbwd, 0, sizeof(float) * column_padded_cells(P), s) != cudaSuccess)
         return 9;
-    if ((long long)P.n_views * P.n_u * P.n_v > 0)
-        column_backward_kernel<<<column_grid(P), 256, 0, s>>>(P, (const ColumnTrace *)d_columns,
-                                                             sino, d_zbwd);
+    if ((long long)P.n_views * P.n_u * P.n_v > 0) {
+        const ColumnTrace *T = (const ColumnTrace *)d_columns;
+        const int R = plan.rows_bwd;
+        if (R == 4) column_backward_kernel<4><<<column_grid(P, 4), 256, 0, s>>>(P, T, sino, d_zbwd);
+        else if (R == 2) column_backward_kernel<2><<<column_grid(P, 2), 256, 0, s>>>(P, T, sino, d_zbwd);
+        else column_backward_kernel<1><<<column_grid(P, 1), 256, 0, s>>>(P, T, sino, d_zbwd);
+    }
     zfast_to_xfast_kernel<<<transpose_grid(P), 256, 0, s>>>(d_zbwd, vol, P.n[0], P.n[1], P.n[2]);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 
-inline int column_count(const RayParams &P, const ColumnPlan &, const void *d_columns,
+inline int column_count(const RayParams &P, const ColumnPlan &plan, const void *d_columns,
                         unsigned long long *d_total, cudaStream_t s)
 {
-    column_count_kernel<<<column_grid(P), 256, 0, s>>>(P, (const ColumnTrace *)d_columns, d_total);
+    const ColumnTrace *T = (const ColumnTrace *)d_columns;
+    const int R = plan.rows_bwd;
+    if (R == 4) column_count_kernel<4><<<column_grid(P, 4), 256, 0, s>>>(P, T, d_total);
+    else if (R == 2) column_count_kernel<2><<<column_grid(P, 2), 256, 0, s>>>(P, T, d_total);
+    else column_count_kernel<1><<<column_grid(P, 1), 256, 0, s>>>(P, T, d_total);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 
