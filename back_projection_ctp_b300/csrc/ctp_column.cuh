@@ -38,9 +38,12 @@ struct ColumnTrace {
     int nb;              // extent along b
     float lxy2;          // squared physical xy length per slab
     int pad_;
-    double zc, zd;       // z (cells) at slab k0 of row iv: zc + iv * zd
-    double bc, bd;       // z slope per slab of row iv: bc + iv * bd (signed)
+    // Row iv's z line in fixed point (2^-40 cell): z at slab k0 = Z0 + iv * ZD,
+    // signed z change per slab = B0 + iv * BD.  Exact integer arithmetic per row.
+    long long Z0, ZD, B0, BD;
 };
+
+constexpr int kRowFrac = 40;  // fractional bits of the rows' fixed-point z lines
 
 struct ColumnPlan {
     int n_columns;       // n_views * n_u
@@ -75,7 +78,7 @@ __global__ void column_setup_kernel(RayParams P, ColumnTrace *__restrict__ T,
     C.nb = 1;
     C.lxy2 = 0.0f;
     C.pad_ = 0;
-    C.zc = C.zd = C.bc = C.bd = 0.0;
+    C.Z0 = C.ZD = C.B0 = C.BD = 0;
 
     double P0[3];
 #pragma unroll
@@ -163,21 +166,35 @@ __global__ void column_setup_kernel(RayParams P, ColumnTrace *__restrict__ T,
 
     // z of row iv at slab k0 and its slope per slab.  t(xi) = (xi - A_p) / |w_p|.
     const double lam = __dmul_rn(__dsub_rn(k0, A[p]), inv);
+    double zc, zd, bc, bd;
     if (P.beam == 1) {
         const double wz0 = __dsub_rn(P0[2], V.a[2]);
-        C.zc = __fma_rn(lam, wz0, V.a[2]);
-        C.zd = __dmul_rn(lam, V.dv[2]);
-        C.bc = __dmul_rn(wz0, inv);
-        C.bd = __dmul_rn(V.dv[2], inv);
+        zc = __fma_rn(lam, wz0, V.a[2]);
+        zd = __dmul_rn(lam, V.dv[2]);
+        bc = __dmul_rn(wz0, inv);
+        bd = __dmul_rn(V.dv[2], inv);
     } else {
-        C.zc = __fma_rn(lam, V.a[2], P0[2]);
-        C.zd = V.dv[2];
-        C.bc = __dmul_rn(V.a[2], inv);
-        C.bd = 0.0;
+        zc = __fma_rn(lam, V.a[2], P0[2]);
+        zd = V.dv[2];
+        bc = __dmul_rn(V.a[2], inv);
+        bd = 0.0;
     }
-    // every row must cross at most one z plane per slab
-    const double s0 = fabs(C.bc), s1 = fabs(__fma_rn((double)(P.n_v - 1), C.bd, C.bc));
+    // every row must cross at most one z plane per slab, and the rows' z lines
+    // must fit the fixed-point range (|z| < 2^21 cells at the first slab)
+    const double zl = (double)(P.n_v - 1);
+    const double s0 = fabs(bc), s1 = fabs(__fma_rn(zl, bd, bc));
     if (!(fmax(s0, s1) < 1.0)) atomicOr(flag, 2);
+    if (!(fabs(zc) < 2097152.0 && fabs(__fma_rn(zl, zd, zc)) < 2097152.0 &&
+          fabs(zd) < 32768.0)) {
+        atomicOr(flag, 4);
+        T[col] = C;
+        return;
+    }
+    const double one = 1099511627776.0;  // 2^40
+    C.Z0 = llrint(zc * one);
+    C.ZD = llrint(zd * one);
+    C.B0 = llrint(bc * one);
+    C.BD = llrint(bd * one);
     T[col] = C;
 }
 
@@ -207,49 +224,48 @@ __device__ __forceinline__ RowZ column_row_idle()
     return Z;
 }
 
-// Row set-up: this row's z line at the column's first slab (float64, about ten
-// operations; the shared xy part was built at plan time).
+// Row set-up: this row's z line at the column's first slab, from the column's
+// fixed-point affine forms -- integer arithmetic, then the walk's 2^-32 state.
 __device__ __forceinline__ RowZ column_row_setup(const RayParams &P, const ColumnTrace &C, int iv)
 {
     RowZ Z;
-    const double z = __fma_rn((double)iv, C.zd, C.zc);
-    const double bz = __fma_rn((double)iv, C.bd, C.bc);
-    const bool m = bz < 0.0;
-    const double zm = m ? __dsub_rn((double)P.n[2], z) : z;
-    const double abz = fabs(bz);
-    // rows far outside the grid in z touch no cell; bound their index so the
-    // walk's integer arithmetic stays small
-    const double zcl = fmin(fmax(zm, -65536.0), (double)P.n[2] + 65536.0);
-    const double fjz = floor(zcl);
-    const int jz = (int)fjz;
-    Z.fz = (uint32_t)__dmul_rn(__dsub_rn(zcl, fjz), 4294967296.0);
-    Z.bz = to_fixed_slope(abz);
+    const long long z = C.Z0 + (long long)iv * C.ZD;
+    const long long b = C.B0 + (long long)iv * C.BD;
+    const bool m = b < 0;
+    const long long nzf = (long long)P.n[2] << kRowFrac;
+    const long long absb = m ? -b : b;
+    // rows far outside the grid in z touch no cell; bound them so the walk's
+    // integer arithmetic stays small
+    const long long lim = (long long)(65536 + P.n[2]) << kRowFrac;
+    const long long zm = min(max(m ? nzf - z : z, -lim), lim);
+    const int jz = (int)(zm >> kRowFrac);
+    Z.fz = (uint32_t)(zm >> (kRowFrac - 32));
+    const long long bq = (absb + (1LL << (kRowFrac - 33))) >> (kRowFrac - 32);
+    Z.bz = bq >= 0xffffffffLL ? 0xffffffffu : (uint32_t)bq;
     Z.ibz = Z.bz ? __frcp_rn((float)Z.bz) : 0.0f;
     Z.sz = m ? -1 : 1;
     Z.zoff = m ? P.n[2] - 1 - jz : jz;
-    const float dz = (float)(abz * P.spacing[2]);
+    const float slope = __fmul_rn((float)absb, 9.094947017729282e-13f);  // 2^-40
+    const float dz = __fmul_rn(slope, (float)P.spacing[2]);
     Z.ell = __fsqrt_rn(__fadd_rn(C.lxy2, __fmul_rn(dz, dz)));
     // Slabs k where the walk's mirrored z index j(k) and j(k+1) are both in
-    // [0, nz).  The walk follows zm + (k - k0) |bz| to within 6e-8 cell (slope
-    // quantised to 2^-33 over at most 512 slabs, start to 2^-32), so the line
-    // itself is required to stay 1e-6 cell inside: j(k) >= 0 once
-    // zm + (k - k0) |bz| >= 1e-6, and j(k+1) < nz while
-    // zm + (k + 1 - k0) |bz| <= nz - 1e-6.  A row with slope 0 keeps
-    // j = floor(zm) exactly.
-    const double nz = (double)P.n[2];
-    const double margin = 1e-6;
-    double kin, kout;
-    if (abz > 0.0) {
-        const double inv = __drcp_rn(abz);
-        kin = zm >= margin ? (double)C.k0 : (double)C.k0 + ceil((margin - zm) * inv);
-        kout = (double)C.k0 - 1.0 + floor((nz - margin - zm) * inv);
+    // [0, nz).  The walk follows zm + (k - k0) |b| to within (k1 - k0 + 2) 2^-33
+    // cell (start truncated to 2^-32, slope rounded to 2^-33 per slab), so the line
+    // is required to stay a margin of 1e-6 cell plus that bound inside; the
+    // float32 quotients below err by far less than the one slab added to each side.
+    if (absb > 0) {
+        const long long margin = 1099511LL + ((long long)(C.k1 - C.k0 + 2) << (kRowFrac - 33));
+        const long long lo = margin - zm;
+        const long long hi = nzf - margin - zm;
+        const float q_lo = fminf(__fdiv_rn((float)lo, (float)absb), 1e9f);
+        const float q_hi = fmaxf(fminf(__fdiv_rn((float)hi, (float)absb), 1e9f), -1e9f);
+        Z.kin = lo <= 0 ? C.k0 : C.k0 + (int)ceilf(q_lo) + 1;
+        Z.kout = hi < 0 ? C.k0 - 2 : C.k0 - 1 + (int)floorf(q_hi) - 1;
     } else {
-        const bool inside = zcl >= 0.0 && zcl < nz;
-        kin = inside ? -1e9 : 1e9;
-        kout = inside ? 1e9 : -1e9;
+        const bool inside = jz >= 0 && jz < P.n[2];
+        Z.kin = inside ? -(1 << 30) : (1 << 30);
+        Z.kout = inside ? (1 << 30) : -(1 << 30);
     }
-    Z.kin = (int)fmin(fmax(kin, -1e9), 1e9);
-    Z.kout = (int)fmin(fmax(kout, -1e9), 1e9);
     return Z;
 }
 
