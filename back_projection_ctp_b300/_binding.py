@@ -19,7 +19,7 @@ _LIB_PATH = os.path.join(_HERE, "libctp.so")
 _lib = None
 _lock = threading.Lock()
 
-PATHS = {"auto": 0, "ray": 1, "column": 2}
+PATHS = {"auto": 0, "ray": 1, "column": 2, "plane": 3}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 BEAMS = {"parallel": 0, "divergent": 1}
 

@@ -17,6 +17,7 @@
 
 #include "ctp.h"
 #include "ctp_column.cuh"
+#include "ctp_plane.cuh"
 #include "ctp_internal.h"
 #include "ctp_ray.cuh"
 
@@ -32,11 +33,11 @@ struct ctp_plan {
     std::vector<ctp::ViewFrame> frames;     // host copy
     ctp::ViewFrame *d_frames = nullptr;     // device copy
     unsigned long long *d_counter = nullptr;
-    // column path
+    // column and plane paths
     ctp::ColumnPlan col{};
-    void *d_columns = nullptr;              // ColumnTrace table
-    float *d_zfwd = nullptr;                // padded z-fastest copy read by the forward
-    float *d_zbwd = nullptr;                // padded z-fastest accumulator of the backward
+    void *d_table = nullptr;                // ColumnTrace (column) or PlaneRay (plane) table
+    float *d_work_fwd = nullptr;            // padded working copy read by the forward
+    float *d_work_bwd = nullptr;            // padded accumulator of the backward
     // host-buffer entry points
     float *d_stage_vol = nullptr, *d_stage_sino = nullptr;
     unsigned long long device_bytes = 0;
@@ -106,9 +107,9 @@ void free_plan(ctp_plan_t *p)
     cudaDeviceSynchronize();
     cudaFree(p->d_frames);
     cudaFree(p->d_counter);
-    cudaFree(p->d_columns);
-    cudaFree(p->d_zfwd);
-    cudaFree(p->d_zbwd);
+    cudaFree(p->d_table);
+    cudaFree(p->d_work_fwd);
+    cudaFree(p->d_work_bwd);
     cudaFree(p->d_stage_vol);
     cudaFree(p->d_stage_sino);
     delete p;
@@ -214,7 +215,8 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
     if (!out) return CTP_E_NULL;
     *out = nullptr;
     if (!geom || !vol) return CTP_E_NULL;
-    if (path != CTP_PATH_AUTO && path != CTP_PATH_RAY && path != CTP_PATH_COLUMN)
+    if (path != CTP_PATH_AUTO && path != CTP_PATH_RAY && path != CTP_PATH_COLUMN &&
+        path != CTP_PATH_PLANE)
         return CTP_E_OPTION;
     int st = validate(geom, vol);
     if (st != CTP_OK) return st;
@@ -266,8 +268,10 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
     }
 
     int chosen = path;
-    if (chosen == CTP_PATH_AUTO) chosen = v_is_z ? CTP_PATH_COLUMN : CTP_PATH_RAY;
-    if (chosen == CTP_PATH_COLUMN && !v_is_z) {
+    if (chosen == CTP_PATH_AUTO)
+        chosen = geom->ndim == 2 ? CTP_PATH_PLANE : (v_is_z ? CTP_PATH_COLUMN : CTP_PATH_RAY);
+    if ((chosen == CTP_PATH_COLUMN && (!v_is_z || geom->ndim != 3)) ||
+        (chosen == CTP_PATH_PLANE && geom->ndim != 2)) {
         free_plan(p);
         return CTP_E_OPTION;
     }
@@ -281,17 +285,22 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
         return CTP_E_CUDA;
     }
     p->device_bytes = fbytes + sizeof(unsigned long long);
-    if (chosen == CTP_PATH_COLUMN) {
-        st = ctp::column_plan_build(ray_params(p), &p->col, &p->d_columns, &p->d_zfwd,
-                                    &p->d_zbwd, &p->device_bytes);
+    if (chosen == CTP_PATH_COLUMN || chosen == CTP_PATH_PLANE) {
+        if (chosen == CTP_PATH_COLUMN)
+            st = ctp::column_plan_build(ray_params(p), &p->col, &p->d_table, &p->d_work_fwd,
+                                        &p->d_work_bwd, &p->device_bytes);
+        else
+            st = ctp::plane_plan_build(ray_params(p), &p->d_table, &p->d_work_fwd,
+                                       &p->d_work_bwd, &p->device_bytes);
         if (st == CTP_E_OPTION && path == CTP_PATH_AUTO) {
-            // some rows cross more than one z plane per slab: use the ray path
-            cudaFree(p->d_columns);
-            cudaFree(p->d_zfwd);
-            cudaFree(p->d_zbwd);
-            p->d_columns = nullptr;
-            p->d_zfwd = nullptr;
-            p->d_zbwd = nullptr;
+            // column: some rows cross more than one z plane per slab; plane: some
+            // rays leave the slice plane.  Use the ray path.
+            cudaFree(p->d_table);
+            cudaFree(p->d_work_fwd);
+            cudaFree(p->d_work_bwd);
+            p->d_table = nullptr;
+            p->d_work_fwd = nullptr;
+            p->d_work_bwd = nullptr;
             p->device_bytes = fbytes + sizeof(unsigned long long);
             p->path = CTP_PATH_RAY;
             st = CTP_OK;
@@ -327,8 +336,11 @@ int ctp_forward(const ctp_plan_t *plan, const float *vol_dev, float *sino_dev, v
     if (plan->n_rays == 0) return CTP_OK;
     cudaStream_t s = (cudaStream_t)stream;
     if (plan->path == CTP_PATH_COLUMN)
-        return ctp::column_forward(ray_params(plan), plan->col, plan->d_columns, plan->d_zfwd,
+        return ctp::column_forward(ray_params(plan), plan->col, plan->d_table, plan->d_work_fwd,
                                    vol_dev, sino_dev, s);
+    if (plan->path == CTP_PATH_PLANE)
+        return ctp::plane_forward(ray_params(plan), plan->d_table, plan->d_work_fwd, vol_dev,
+                                  sino_dev, s);
     return launch_ray(plan, 0, vol_dev, sino_dev, s);
 }
 
@@ -339,8 +351,11 @@ int ctp_backward(const ctp_plan_t *plan, const float *sino_dev, float *vol_dev, 
     if (st != CTP_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     if (plan->path == CTP_PATH_COLUMN)
-        return ctp::column_backward(ray_params(plan), plan->col, plan->d_columns, plan->d_zbwd,
+        return ctp::column_backward(ray_params(plan), plan->col, plan->d_table, plan->d_work_bwd,
                                     sino_dev, vol_dev, s);
+    if (plan->path == CTP_PATH_PLANE)
+        return ctp::plane_backward(ray_params(plan), plan->d_table, plan->d_work_bwd, sino_dev,
+                                   vol_dev, s);
     if (cudaMemsetAsync(vol_dev, 0, sizeof(float) * plan->n_cells, s) != cudaSuccess)
         return CTP_E_CUDA;
     if (plan->n_rays == 0) return CTP_OK;
@@ -358,7 +373,9 @@ int ctp_segment_count(const ctp_plan_t *plan, unsigned long long *out, void *str
     if (cudaMemsetAsync(plan->d_counter, 0, sizeof(unsigned long long), s) != cudaSuccess)
         return CTP_E_CUDA;
     if (plan->path == CTP_PATH_COLUMN)
-        st = ctp::column_count(ray_params(plan), plan->col, plan->d_columns, plan->d_counter, s);
+        st = ctp::column_count(ray_params(plan), plan->col, plan->d_table, plan->d_counter, s);
+    else if (plan->path == CTP_PATH_PLANE)
+        st = ctp::plane_count(ray_params(plan), plan->d_table, plan->d_counter, s);
     else
         st = launch_ray(plan, 2, nullptr, nullptr, s);
     if (st != CTP_OK) return st;

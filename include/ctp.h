@@ -65,9 +65,18 @@ typedef enum ctp_status {
 
 typedef enum ctp_beam { CTP_PARALLEL = 0, CTP_DIVERGENT = 1 } ctp_beam;
 
-/* Traversal path.  AUTO picks COLUMN when every view's detector v axis is
- * exactly +-z (then all rays of a detector column share one xy trace), else RAY. */
-typedef enum ctp_path { CTP_PATH_AUTO = 0, CTP_PATH_RAY = 1, CTP_PATH_COLUMN = 2 } ctp_path;
+/* Traversal path.  AUTO picks PLANE for 2-D scans (rays in the slice plane),
+ * COLUMN for 3-D scans whose detector v axis is exactly +-z in every view (then
+ * all rays of a detector column share one xy trace), else RAY; it falls back to
+ * RAY when a scan does not meet PLANE's or COLUMN's conditions (rays leaving the
+ * slice; rows crossing more than one z plane per slab).  All paths compute the
+ * same operator; they differ in work layout only. */
+typedef enum ctp_path {
+    CTP_PATH_AUTO = 0,
+    CTP_PATH_RAY = 1,
+    CTP_PATH_COLUMN = 2,
+    CTP_PATH_PLANE = 3
+} ctp_path;
 
 typedef struct ctp_geometry {
     int ndim;                 /* 2 or 3 */

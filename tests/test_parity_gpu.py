@@ -65,7 +65,8 @@ def test_small_cases_match_oracle(torch, ctp, oracle_mod, idx, path):
     g_ref = oracle_mod.backward(scan, y_clean.ravel())
 
     plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w), path)
-    assert plan.path == ("column" if (path == "auto" and w.ndim == 3) else "ray")
+    expected = {"auto": "column" if w.ndim == 3 else "plane", "ray": "ray"}[path]
+    assert plan.path == expected
     p, g = _run_pair(torch, ctp, plan, vol, y_clean)
     assert rel_l2(p[~amb], p_ref[~amb]) <= TOL_FORWARD
     assert rel_l2(g, g_ref) <= TOL_BACKWARD
@@ -94,6 +95,52 @@ def test_ray_and_column_paths_agree(torch, ctp, idx):
         out[path] = _run_pair(torch, ctp, plan, vol, y)
     assert rel_l2(out["column"][0], out["ray"][0]) <= TOL_FORWARD
     assert rel_l2(out["column"][1], out["ray"][1]) <= TOL_BACKWARD
+
+
+@pytest.mark.parametrize("idx", [1, 2])
+def test_ray_and_plane_paths_agree(torch, ctp, idx):
+    w = SMALL[idx]
+    f = ci.frames(w)
+    vol = ci.phantom(w)
+    y = ci.sinogram_noise(w)
+    out = {}
+    for path in ("ray", "plane"):
+        plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w), path)
+        assert plan.path == path
+        out[path] = _run_pair(torch, ctp, plan, vol, y)
+    assert rel_l2(out["plane"][0], out["ray"][0]) <= TOL_FORWARD
+    assert rel_l2(out["plane"][1], out["ray"][1]) <= TOL_BACKWARD
+
+
+@pytest.mark.parametrize("mode", ["t", "r"])
+def test_plane_backward_variants_match_oracle(torch, ctp, oracle_mod, monkeypatch, mode):
+    """The plane backward's two work layouts (shared-memory tiles for small
+    scans, privatised global accumulators for larger ones) on the same scan."""
+    monkeypatch.setenv("CTP_PLANE_BACKWARD", mode)
+    w = SMALL[2]
+    f = ci.frames(w)
+    scan = oracle_mod.Scan.from_workload(w, f)
+    y = ci.sinogram_noise(w)
+    g_ref = oracle_mod.backward(scan, y.ravel())
+    plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w), "plane")
+    _, g = _run_pair(torch, ctp, plan, ci.phantom(w), y)
+    assert rel_l2(g, g_ref) <= TOL_BACKWARD
+
+
+def test_tilted_2d_frames_fall_back_to_ray_path(torch, ctp, oracle_mod):
+    # a 2-D scan whose rays leave the slice plane is not a plane-path scan
+    w = SMALL[2]
+    f = {k: v.copy() for k, v in ci.frames(w).items()}
+    f["src"][:, 2] = 0.3
+    plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w))
+    assert plan.path == "ray"
+    with pytest.raises(ctp.CtpError):
+        ctp.ctp_plan(geometry_of(w, f), volume_of(w), "plane")
+    scan = oracle_mod.Scan.from_workload(w, f)
+    vol = ci.phantom(w)
+    p_ref = oracle_mod.forward(scan, vol)
+    p, _ = _run_pair(torch, ctp, plan, vol, ci.sinogram_noise(w))
+    assert rel_l2(p, p_ref) <= TOL_FORWARD
 
 
 def test_host_entry_points_match_device(torch, ctp):
