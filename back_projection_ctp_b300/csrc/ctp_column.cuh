@@ -204,9 +204,18 @@ struct RowZ {
     float ibz;           // 1 / bz (0 when the row never crosses a z plane)
     int zoff;            // z index of the current cell (inside the grid iff 0 <= zoff < nz)
     int sz;              // +-1: step of zoff at a z crossing
-    float ell;           // physical length per slab
     int kin, kout;       // slabs k in [kin, kout]: the row and its next z cell are inside
 };
+
+// Physical length per slab of a row with fixed-point z slope bz (2^-32 cell per
+// slab); forward, backward and the counter all take it from here.
+__device__ __forceinline__ float column_row_ell(const RayParams &P, const ColumnTrace &C,
+                                                uint32_t bz)
+{
+    const float slope = __fmul_rn(__uint2float_rn(bz), 2.3283064365386963e-10f);  // 2^-32
+    const float dz = __fmul_rn(slope, (float)P.spacing[2]);
+    return __fsqrt_rn(__fadd_rn(C.lxy2, __fmul_rn(dz, dz)));
+}
 
 // A row that contributes nothing (beyond the detector, or zero weight): it stays
 // in z cell 0 (a valid address) and its weight / result is zero or discarded.
@@ -218,7 +227,6 @@ __device__ __forceinline__ RowZ column_row_idle()
     Z.ibz = 0.0f;
     Z.zoff = 0;
     Z.sz = 1;
-    Z.ell = 0.0f;
     Z.kin = -(1 << 30);
     Z.kout = 1 << 30;
     return Z;
@@ -245,9 +253,6 @@ __device__ __forceinline__ RowZ column_row_setup(const RayParams &P, const Colum
     Z.ibz = Z.bz ? __frcp_rn((float)Z.bz) : 0.0f;
     Z.sz = m ? -1 : 1;
     Z.zoff = m ? P.n[2] - 1 - jz : jz;
-    const float slope = __fmul_rn((float)absb, 9.094947017729282e-13f);  // 2^-40
-    const float dz = __fmul_rn(slope, (float)P.spacing[2]);
-    Z.ell = __fsqrt_rn(__fadd_rn(C.lxy2, __fmul_rn(dz, dz)));
     // Slabs k where the walk's mirrored z index j(k) and j(k+1) are both in
     // [0, nz).  The walk follows zm + (k - k0) |b| to within (k1 - k0 + 2) 2^-33
     // cell (start truncated to 2^-32, slope rounded to 2^-33 per slab), so the line
@@ -430,7 +435,8 @@ __global__ void __launch_bounds__(256, 5) column_forward_kernel(RayParams P,
             }
             column_walk<R>(C, Z, (unsigned)P.n[2], op);
 #pragma unroll
-            for (int r = 0; r < R; ++r) out[r] = __fmul_rn(op.acc[r], Z[r].ell);
+            for (int r = 0; r < R; ++r)
+                out[r] = __fmul_rn(op.acc[r], column_row_ell(P, C, Z[r].bz));
         }
     }
 #pragma unroll
@@ -474,8 +480,9 @@ __global__ void __launch_bounds__(256) column_backward_kernel(RayParams P,
     for (int r = 0; r < R; ++r) {
         const int iv = row0 + 32 * r;
         const float y = tile[lane + 32 * r][warp];
-        Z[r] = (iv < P.n_v && y != 0.0f) ? column_row_setup(P, C, iv) : column_row_idle();
-        op.w[r] = __fmul_rn(Z[r].ell, y);
+        const bool live = iv < P.n_v && y != 0.0f;
+        Z[r] = live ? column_row_setup(P, C, iv) : column_row_idle();
+        op.w[r] = live ? __fmul_rn(column_row_ell(P, C, Z[r].bz), y) : 0.0f;
         any |= op.w[r] != 0.0f;
     }
     if (!__any_sync(0xffffffffu, any)) return;
@@ -502,8 +509,9 @@ __global__ void __launch_bounds__(256) column_count_kernel(RayParams P,
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int iv = row0 + 32 * r;
-                Z[r] = iv < P.n_v ? column_row_setup(P, C, iv) : column_row_idle();
-                op.thr[r] = Z[r].ell > 0.0f ? __fdiv_rn(P.min_len, Z[r].ell) : 3.0e38f;
+                const bool live = iv < P.n_v;
+                Z[r] = live ? column_row_setup(P, C, iv) : column_row_idle();
+                op.thr[r] = live ? __fdiv_rn(P.min_len, column_row_ell(P, C, Z[r].bz)) : 3.0e38f;
             }
             column_walk<R>(C, Z, (unsigned)P.n[2], op);
             n = op.n;
