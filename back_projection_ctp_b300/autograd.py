@@ -1,0 +1,89 @@
+"""PyTorch autograd over the C ABI: differentiable projection and backprojection.
+
+The forward projector A and the backprojector A^T of one plan are each other's
+gradient (the pair is matched, so d<A x, g>/dx = A^T g and d<A^T y, h>/dy = A h),
+which also makes second derivatives -- Hessian-vector products of data losses --
+available through ordinary autograd.  Leading batch / channel dimensions loop
+over the C calls; every call runs in the CUDA library (diffct's
+ProjectorFunction / BackprojectorFunction pair, README "Matched operators":
+volume and sinogram gradients and Hessian-vector products; CHANGELOG 2.3.0:
+leading batch and channel dimensions, including empty batches).
+"""
+
+from __future__ import annotations
+
+import torch
+
+from ._binding import Geometry, Plan, Volume, ctp_backward, ctp_forward, ctp_plan
+
+
+class Projector:
+    """A plan plus differentiable ``project`` (A) and ``backproject`` (A^T).
+
+    ``project(vol)``: vol of shape (..., D, H, W) -> sinogram (..., n_views, n_v, n_u).
+    ``backproject(sino)``: the transpose.  Inputs are moved to the plan's device
+    and made contiguous float32; outputs are float32 on that device.
+    """
+
+    def __init__(self, geometry: Geometry, volume: Volume, path: str = "auto"):
+        self.plan: Plan = ctp_plan(geometry, volume, path)
+        self.device = torch.device("cuda", self.plan.device)
+
+    @property
+    def vol_shape(self):
+        return self.plan.vol_shape
+
+    @property
+    def sino_shape(self):
+        return self.plan.sino_shape
+
+    def project(self, vol: torch.Tensor) -> torch.Tensor:
+        return _Project.apply(vol, self)
+
+    def backproject(self, sino: torch.Tensor) -> torch.Tensor:
+        return _Backproject.apply(sino, self)
+
+    __call__ = project
+
+
+def _batched(x: torch.Tensor, inner: tuple, name: str):
+    if tuple(x.shape[-len(inner):]) != tuple(inner):
+        raise ValueError(f"{name} must end with shape {tuple(inner)}, got {tuple(x.shape)}")
+    return x.shape[:-len(inner)]
+
+
+def _apply(proj: Projector, x: torch.Tensor, in_shape, out_shape, fn):
+    lead = _batched(x, in_shape, "input")
+    x = x.detach().to(device=proj.device, dtype=torch.float32).contiguous()
+    flat = x.reshape((-1,) + tuple(in_shape))
+    out = torch.empty((flat.shape[0],) + tuple(out_shape), dtype=torch.float32, device=proj.device)
+    stream = torch.cuda.current_stream(proj.device)
+    for i in range(flat.shape[0]):
+        fn(proj.plan, flat[i], out[i], stream)
+    return out.reshape(tuple(lead) + tuple(out_shape))
+
+
+class _Project(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, vol, proj):
+        ctx.proj = proj
+        ctx.in_dtype, ctx.in_device = vol.dtype, vol.device
+        return _apply(proj, vol, proj.vol_shape, proj.sino_shape, ctp_forward)
+
+    @staticmethod
+    def backward(ctx, grad):
+        g = _Backproject.apply(grad, ctx.proj)
+        return g.to(dtype=ctx.in_dtype, device=ctx.in_device), None
+
+
+class _Backproject(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, sino, proj):
+        ctx.proj = proj
+        ctx.in_dtype, ctx.in_device = sino.dtype, sino.device
+        return _apply(proj, sino, proj.sino_shape, proj.vol_shape, ctp_backward)
+
+    @staticmethod
+    def backward(ctx, grad):
+        g = _Project.apply(grad, ctx.proj)
+        return g.to(dtype=ctx.in_dtype, device=ctx.in_device), None

@@ -1,0 +1,71 @@
+"""Differentiable wrapper: gradients are the matched operators, batch dims loop,
+second derivatives work (data Hessian-vector products)."""
+
+import numpy as np
+import pytest
+
+from cases import ci, geometry_of, rel_l2, volume_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def proj():
+    import torch  # noqa: F401
+    from back_projection_ctp_b300.autograd import Projector
+    w = ci.small_cases()[3]
+    return Projector(geometry_of(w, ci.frames(w)), volume_of(w))
+
+
+def test_gradient_of_projection_is_backprojection(proj):
+    import torch
+    x = torch.randn(proj.vol_shape, device="cuda", requires_grad=True)
+    g = torch.randn(proj.sino_shape, device="cuda")
+    (proj.project(x) * g).sum().backward()
+    ref = proj.backproject(g)
+    assert rel_l2(x.grad.cpu().numpy(), ref.cpu().numpy()) <= 1e-6
+
+
+def test_gradient_of_backprojection_is_projection(proj):
+    import torch
+    y = torch.randn(proj.sino_shape, device="cuda", requires_grad=True)
+    h = torch.randn(proj.vol_shape, device="cuda")
+    (proj.backproject(y) * h).sum().backward()
+    ref = proj.project(h)
+    assert rel_l2(y.grad.cpu().numpy(), ref.cpu().numpy()) <= 1e-6
+
+
+def test_batch_and_channel_dims_and_empty_batch(proj):
+    import torch
+    x = torch.randn((2, 3) + proj.vol_shape, device="cuda")
+    p = proj.project(x)
+    assert p.shape == (2, 3) + proj.sino_shape
+    for i in range(2):
+        for j in range(3):
+            assert torch.equal(p[i, j], proj.project(x[i, j]))
+    e = proj.project(torch.zeros((0,) + proj.vol_shape, device="cuda"))
+    assert e.shape == (0,) + proj.sino_shape
+    with pytest.raises(ValueError):
+        proj.project(torch.zeros((4, 5, 6), device="cuda"))
+
+
+def test_hessian_vector_product_of_least_squares(proj):
+    """loss = 0.5 ||A x - b||^2: grad = A^T (A x - b), Hessian-vector product = A^T A v."""
+    import torch
+    x = torch.randn(proj.vol_shape, device="cuda", requires_grad=True)
+    b = torch.randn(proj.sino_shape, device="cuda")
+    v = torch.randn(proj.vol_shape, device="cuda")
+    loss = 0.5 * ((proj.project(x) - b) ** 2).sum()
+    (grad,) = torch.autograd.grad(loss, x, create_graph=True)
+    (hv,) = torch.autograd.grad((grad * v).sum(), x)
+    ref = proj.backproject(proj.project(v))
+    assert rel_l2(hv.cpu().numpy(), ref.cpu().numpy()) <= 1e-5
+    ref_g = proj.backproject(proj.project(x.detach()) - b)
+    assert rel_l2(grad.detach().cpu().numpy(), ref_g.cpu().numpy()) <= 1e-5
+
+
+def test_double_precision_inputs_keep_their_dtype_for_gradients(proj):
+    import torch
+    x = torch.randn(proj.vol_shape, device="cuda", dtype=torch.float64, requires_grad=True)
+    proj.project(x).sum().backward()
+    assert x.grad.dtype == torch.float64
