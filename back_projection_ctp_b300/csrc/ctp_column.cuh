@@ -571,13 +571,12 @@ inline size_t column_padded_cells(const RayParams &P)
 // registers.  The forward gather waits on L2 and wants occupancy: it runs 5
 // blocks of 256 threads per SM (<= 48 registers, a few spilled) with 4 rows.
 // The backward is bound by its atomics' L1/L2 throughput and runs 2 rows
-// without a register cap.  CTP_COLUMN_ROWS_FWD / CTP_COLUMN_ROWS_BWD = 1, 2 or 4
+// without a register cap.  CTP_COLUMN_ROWS_FWD / CTP_COLUMN_ROWS_BWD = 1, 2, 3 or 4
 // override the choice.
 inline int column_rows(const RayParams &P, const char *env_name, int preferred)
 {
     const char *env = getenv(env_name);
-    if (env && (env[0] == '1' || env[0] == '2' || env[0] == '4') && env[1] == '\0')
-        return env[0] - '0';
+    if (env && env[0] >= '1' && env[0] <= '4' && env[1] == '\0') return env[0] - '0';
     int r = preferred;
     while (r > 1 && P.n_v < 24 * r) r /= 2;
     return r;
@@ -637,6 +636,7 @@ inline int column_forward(const RayParams &P, const ColumnPlan &plan, const void
     const ColumnTrace *T = (const ColumnTrace *)d_columns;
     const int R = plan.rows_fwd;
     if (R == 4) column_forward_kernel<4><<<column_grid(P, 4), 256, 0, s>>>(P, T, d_zfwd, sino);
+    else if (R == 3) column_forward_kernel<3><<<column_grid(P, 3), 256, 0, s>>>(P, T, d_zfwd, sino);
     else if (R == 2) column_forward_kernel<2><<<column_grid(P, 2), 256, 0, s>>>(P, T, d_zfwd, sino);
     else column_forward_kernel<1><<<column_grid(P, 1), 256, 0, s>>>(P, T, d_zfwd, sino);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
@@ -651,6 +651,7 @@ inline int column_backward(const RayParams &P, const ColumnPlan &plan, const voi
         const ColumnTrace *T = (const ColumnTrace *)d_columns;
         const int R = plan.rows_bwd;
         if (R == 4) column_backward_kernel<4><<<column_grid(P, 4), 256, 0, s>>>(P, T, sino, d_zbwd);
+        else if (R == 3) column_backward_kernel<3><<<column_grid(P, 3), 256, 0, s>>>(P, T, sino, d_zbwd);
         else if (R == 2) column_backward_kernel<2><<<column_grid(P, 2), 256, 0, s>>>(P, T, sino, d_zbwd);
         else column_backward_kernel<1><<<column_grid(P, 1), 256, 0, s>>>(P, T, sino, d_zbwd);
     }
@@ -664,6 +665,7 @@ inline int column_count(const RayParams &P, const ColumnPlan &plan, const void *
     const ColumnTrace *T = (const ColumnTrace *)d_columns;
     const int R = plan.rows_bwd;
     if (R == 4) column_count_kernel<4><<<column_grid(P, 4), 256, 0, s>>>(P, T, d_total);
+    else if (R == 3) column_count_kernel<3><<<column_grid(P, 3), 256, 0, s>>>(P, T, d_total);
     else if (R == 2) column_count_kernel<2><<<column_grid(P, 2), 256, 0, s>>>(P, T, d_total);
     else column_count_kernel<1><<<column_grid(P, 1), 256, 0, s>>>(P, T, d_total);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
