@@ -40,6 +40,9 @@ struct ctp_plan {
     float *d_work_bwd = nullptr;            // padded accumulator of the backward
     // host-buffer entry points
     float *d_stage_vol = nullptr, *d_stage_sino = nullptr;
+    cudaStream_t copy_stream = nullptr;     // sinogram chunks move here, beside the walk
+    cudaEvent_t ev_start = nullptr;         // work queued on the caller's stream before a call
+    cudaEvent_t ev_chunk[64] = {};          // chunk c walked (forward) or staged (backward)
     unsigned long long device_bytes = 0;
 };
 
@@ -80,25 +83,106 @@ ctp::RayParams ray_params(const ctp_plan_t *plan)
     P.stride[2] = plan->n[0] * plan->n[1];
     P.min_len = (float)(1e-5 * std::fmin(plan->spacing[0],
                                          std::fmin(plan->spacing[1], plan->spacing[2])));
+    P.view0 = 0;
+    P.view_count = plan->n_views;
+    return P;
+}
+
+// Parameters of a launch over views [v0, v0 + nv).
+ctp::RayParams view_range(const ctp_plan_t *plan, int v0, int nv)
+{
+    ctp::RayParams P = ray_params(plan);
+    P.view0 = v0;
+    P.view_count = nv;
     return P;
 }
 
 // Threads of one ray block: 32 (u) x 4 (v) for 3-D scans, 128 (u) for single-row detectors.
-int launch_ray(const ctp_plan_t *plan, int which, const float *in, float *out, cudaStream_t s)
+int launch_ray(const ctp::RayParams &P, int which, const float *in, float *out,
+               unsigned long long *counter, cudaStream_t s)
 {
-    const ctp::RayParams P = ray_params(plan);
-    if (plan->n_v == 1) {
-        dim3 grid((plan->n_u + 127) / 128, plan->n_views, 1), block(128);
+    if (P.view_count <= 0) return CTP_OK;
+    if (P.n_v == 1) {
+        dim3 grid((P.n_u + 127) / 128, P.view_count, 1), block(128);
         if (which == 0) ctp::ray_forward_kernel<128, 1><<<grid, block, 0, s>>>(P, in, out);
         else if (which == 1) ctp::ray_backward_kernel<128, 1><<<grid, block, 0, s>>>(P, in, out);
-        else ctp::ray_count_kernel<128, 1><<<grid, block, 0, s>>>(P, plan->d_counter);
+        else ctp::ray_count_kernel<128, 1><<<grid, block, 0, s>>>(P, counter);
     } else {
-        dim3 grid((plan->n_u + 31) / 32, plan->n_views, (plan->n_v + 3) / 4), block(128);
+        dim3 grid((P.n_u + 31) / 32, P.view_count, (P.n_v + 3) / 4), block(128);
         if (which == 0) ctp::ray_forward_kernel<32, 4><<<grid, block, 0, s>>>(P, in, out);
         else if (which == 1) ctp::ray_backward_kernel<32, 4><<<grid, block, 0, s>>>(P, in, out);
-        else ctp::ray_count_kernel<32, 4><<<grid, block, 0, s>>>(P, plan->d_counter);
+        else ctp::ray_count_kernel<32, 4><<<grid, block, 0, s>>>(P, counter);
     }
     return cudaGetLastError() == cudaSuccess ? CTP_OK : CTP_E_CUDA;
+}
+
+// Stages of the two operators, shared by the device- and host-buffer entry
+// points.  Forward: forward_in (layout of the volume) then forward_walk over
+// view ranges.  Backward: backward_in (zero the accumulator), backward_walk over
+// view ranges, backward_out (fold the accumulator into the output volume).
+// The walks index the sinogram by absolute view, so a range's launch reads or
+// writes only that range's rows.
+int forward_in(const ctp_plan_t *plan, const float *vol, cudaStream_t s)
+{
+    const ctp::RayParams P = ray_params(plan);
+    if (plan->path == CTP_PATH_COLUMN)
+        return ctp::column_layout_in(P, plan->d_work_fwd, vol, s) ? CTP_E_CUDA : CTP_OK;
+    if (plan->path == CTP_PATH_PLANE)
+        return ctp::plane_layout_in(P, plan->d_work_fwd, vol, s) ? CTP_E_CUDA : CTP_OK;
+    return CTP_OK;
+}
+
+int forward_walk(const ctp_plan_t *plan, int v0, int nv, const float *vol, float *sino,
+                 cudaStream_t s)
+{
+    const ctp::RayParams P = view_range(plan, v0, nv);
+    if (plan->path == CTP_PATH_COLUMN)
+        return ctp::column_walk_forward(P, plan->col, plan->d_table, plan->d_work_fwd, sino, s)
+                   ? CTP_E_CUDA : CTP_OK;
+    if (plan->path == CTP_PATH_PLANE)
+        return ctp::plane_walk_forward(P, plan->d_table, plan->d_work_fwd, sino, s) ? CTP_E_CUDA
+                                                                                    : CTP_OK;
+    return launch_ray(P, 0, vol, sino, nullptr, s);
+}
+
+// Small 2-D scans take a single tiled launch over all views instead.
+bool backward_whole(const ctp_plan_t *plan)
+{
+    return plan->path == CTP_PATH_PLANE && ctp::plane_backward_tiled(ray_params(plan));
+}
+
+int backward_in(const ctp_plan_t *plan, float *vol, cudaStream_t s)
+{
+    const ctp::RayParams P = ray_params(plan);
+    if (plan->path == CTP_PATH_COLUMN)
+        return ctp::column_backward_prepare(P, plan->d_work_bwd, s) ? CTP_E_CUDA : CTP_OK;
+    if (plan->path == CTP_PATH_PLANE)
+        return ctp::plane_backward_prepare(P, plan->d_work_bwd, s) ? CTP_E_CUDA : CTP_OK;
+    return cudaMemsetAsync(vol, 0, sizeof(float) * plan->n_cells, s) == cudaSuccess ? CTP_OK
+                                                                                     : CTP_E_CUDA;
+}
+
+int backward_walk(const ctp_plan_t *plan, int v0, int nv, const float *sino, float *vol,
+                  cudaStream_t s)
+{
+    const ctp::RayParams P = view_range(plan, v0, nv);
+    if (plan->path == CTP_PATH_COLUMN)
+        return ctp::column_walk_backward(P, plan->col, plan->d_table, sino, plan->d_work_bwd, s)
+                   ? CTP_E_CUDA : CTP_OK;
+    if (plan->path == CTP_PATH_PLANE)
+        return ctp::plane_walk_backward(P, plan->d_table, sino, plan->d_work_bwd, s) ? CTP_E_CUDA
+                                                                                     : CTP_OK;
+    return launch_ray(P, 1, sino, vol, nullptr, s);
+}
+
+int backward_out(const ctp_plan_t *plan, float *vol, cudaStream_t s)
+{
+    const ctp::RayParams P = ray_params(plan);
+    if (plan->path == CTP_PATH_COLUMN)
+        return ctp::column_layout_out(P, plan->d_work_bwd, vol, s) ? CTP_E_CUDA : CTP_OK;
+    if (plan->path == CTP_PATH_PLANE)
+        return ctp::plane_layout_out(P, plan->d_work_bwd, vol, s) ? CTP_E_CUDA : CTP_OK;
+    return CTP_OK;
 }
 
 void free_plan(ctp_plan_t *p)
@@ -112,6 +196,10 @@ void free_plan(ctp_plan_t *p)
     cudaFree(p->d_work_bwd);
     cudaFree(p->d_stage_vol);
     cudaFree(p->d_stage_sino);
+    if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
+    if (p->ev_start) cudaEventDestroy(p->ev_start);
+    for (cudaEvent_t e : p->ev_chunk)
+        if (e) cudaEventDestroy(e);
     delete p;
 }
 
@@ -335,13 +423,8 @@ int ctp_forward(const ctp_plan_t *plan, const float *vol_dev, float *sino_dev, v
     if (st != CTP_OK) return st;
     if (plan->n_rays == 0) return CTP_OK;
     cudaStream_t s = (cudaStream_t)stream;
-    if (plan->path == CTP_PATH_COLUMN)
-        return ctp::column_forward(ray_params(plan), plan->col, plan->d_table, plan->d_work_fwd,
-                                   vol_dev, sino_dev, s);
-    if (plan->path == CTP_PATH_PLANE)
-        return ctp::plane_forward(ray_params(plan), plan->d_table, plan->d_work_fwd, vol_dev,
-                                  sino_dev, s);
-    return launch_ray(plan, 0, vol_dev, sino_dev, s);
+    if ((st = forward_in(plan, vol_dev, s)) != CTP_OK) return st;
+    return forward_walk(plan, 0, plan->n_views, vol_dev, sino_dev, s);
 }
 
 int ctp_backward(const ctp_plan_t *plan, const float *sino_dev, float *vol_dev, void *stream)
@@ -350,16 +433,13 @@ int ctp_backward(const ctp_plan_t *plan, const float *sino_dev, float *vol_dev, 
     int st = check_device(plan);
     if (st != CTP_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    if (plan->path == CTP_PATH_COLUMN)
-        return ctp::column_backward(ray_params(plan), plan->col, plan->d_table, plan->d_work_bwd,
-                                    sino_dev, vol_dev, s);
-    if (plan->path == CTP_PATH_PLANE)
-        return ctp::plane_backward(ray_params(plan), plan->d_table, plan->d_work_bwd, sino_dev,
-                                   vol_dev, s);
-    if (cudaMemsetAsync(vol_dev, 0, sizeof(float) * plan->n_cells, s) != cudaSuccess)
-        return CTP_E_CUDA;
-    if (plan->n_rays == 0) return CTP_OK;
-    return launch_ray(plan, 1, sino_dev, vol_dev, s);
+    if (backward_whole(plan))
+        return ctp::plane_backward_whole(ray_params(plan), plan->d_table, sino_dev, vol_dev, s)
+                   ? CTP_E_CUDA : CTP_OK;
+    if ((st = backward_in(plan, vol_dev, s)) != CTP_OK) return st;
+    if (plan->n_rays > 0 && (st = backward_walk(plan, 0, plan->n_views, sino_dev, vol_dev, s)) != CTP_OK)
+        return st;
+    return backward_out(plan, vol_dev, s);
 }
 
 int ctp_segment_count(const ctp_plan_t *plan, unsigned long long *out, void *stream)
@@ -372,13 +452,14 @@ int ctp_segment_count(const ctp_plan_t *plan, unsigned long long *out, void *str
     if (plan->n_rays == 0) return CTP_OK;
     if (cudaMemsetAsync(plan->d_counter, 0, sizeof(unsigned long long), s) != cudaSuccess)
         return CTP_E_CUDA;
+    const ctp::RayParams P = ray_params(plan);
     if (plan->path == CTP_PATH_COLUMN)
-        st = ctp::column_count(ray_params(plan), plan->col, plan->d_table, plan->d_counter, s);
+        st = ctp::column_count(P, plan->col, plan->d_table, plan->d_counter, s);
     else if (plan->path == CTP_PATH_PLANE)
-        st = ctp::plane_count(ray_params(plan), plan->d_table, plan->d_counter, s);
+        st = ctp::plane_count(P, plan->d_table, plan->d_counter, s);
     else
-        st = launch_ray(plan, 2, nullptr, nullptr, s);
-    if (st != CTP_OK) return st;
+        st = launch_ray(P, 2, nullptr, nullptr, plan->d_counter, s);
+    if (st != CTP_OK) return CTP_E_CUDA;
     if (cudaMemcpyAsync(out, plan->d_counter, sizeof(unsigned long long), cudaMemcpyDeviceToHost,
                         s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
@@ -398,9 +479,50 @@ static int ensure_stage(ctp_plan_t *plan)
             return CTP_E_CUDA;
         plan->device_bytes += sizeof(float) * plan->n_rays;
     }
+    if (!plan->copy_stream) {
+        if (cudaStreamCreateWithFlags(&plan->copy_stream, cudaStreamNonBlocking) != cudaSuccess)
+            return CTP_E_CUDA;
+        if (cudaEventCreateWithFlags(&plan->ev_start, cudaEventDisableTiming) != cudaSuccess)
+            return CTP_E_CUDA;
+        for (cudaEvent_t &e : plan->ev_chunk)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+                return CTP_E_CUDA;
+    }
     return CTP_OK;
 }
 
+// Number of view chunks the host-buffer entry points pipeline: one per 64 MiB
+// of sinogram, at most 8 (each chunk's walk still fills the GPU many times
+// over), at most one per view.  CTP_HOST_CHUNKS = 1..64 overrides.
+static int host_chunks(const ctp_plan_t *plan)
+{
+    long long c = (long long)(sizeof(float) * (unsigned long long)plan->n_rays >> 26);
+    if (c > 8) c = 8;
+    if (const char *env = getenv("CTP_HOST_CHUNKS")) {
+        const long long e = atoll(env);
+        if (e >= 1 && e <= 64) c = e;
+    }
+    if (c > plan->n_views) c = plan->n_views;
+    return c < 1 ? 1 : (int)c;
+}
+
+static int chunk_begin(const ctp_plan_t *plan, int c, int chunks)
+{
+    return (int)((long long)plan->n_views * c / chunks);
+}
+
+// Ends a failed host-buffer call: copies already queued still read or write the
+// caller's buffers, so wait for them before returning.
+static int host_fail(ctp_plan_t *plan, cudaStream_t s, int st)
+{
+    cudaStreamSynchronize(plan->copy_stream);
+    cudaStreamSynchronize(s);
+    return st;
+}
+
+// Forward over host buffers.  The volume goes up on the caller's stream; the
+// walk runs in view chunks on the caller's stream and each finished chunk's
+// sinogram rows go down on the plan's copy stream while the next chunk walks.
 int ctp_forward_host(ctp_plan_t *plan, const float *vol_host, float *sino_host, void *stream)
 {
     if (!plan || !vol_host || !sino_host) return CTP_E_NULL;
@@ -408,35 +530,81 @@ int ctp_forward_host(ctp_plan_t *plan, const float *vol_host, float *sino_host, 
     if (st != CTP_OK) return st;
     if (plan->n_rays == 0) return CTP_OK;
     if ((st = ensure_stage(plan)) != CTP_OK) return st;
-    cudaStream_t s = (cudaStream_t)stream;
+    cudaStream_t s = (cudaStream_t)stream, cs = plan->copy_stream;
+    const size_t row = (size_t)plan->n_u * plan->n_v;     // sinogram floats of one view
+    // the copy stream starts after whatever the caller queued on s before this call
+    if (cudaEventRecord(plan->ev_start, s) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, plan->ev_start, 0) != cudaSuccess)
+        return host_fail(plan, s, CTP_E_CUDA);
     if (cudaMemcpyAsync(plan->d_stage_vol, vol_host, sizeof(float) * plan->n_cells,
                         cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return CTP_E_CUDA;
-    if ((st = ctp_forward(plan, plan->d_stage_vol, plan->d_stage_sino, stream)) != CTP_OK) return st;
-    if (cudaMemcpyAsync(sino_host, plan->d_stage_sino, sizeof(float) * plan->n_rays,
-                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess)
-        return CTP_E_CUDA;
+        return host_fail(plan, s, CTP_E_CUDA);
+    if ((st = forward_in(plan, plan->d_stage_vol, s)) != CTP_OK) return host_fail(plan, s, st);
+    const int chunks = host_chunks(plan);
+    // all walks first: with pageable host memory a device-to-host copy returns
+    // only once it is done, and the walks queued behind it would wait for it
+    for (int c = 0; c < chunks; ++c) {
+        const int v0 = chunk_begin(plan, c, chunks), v1 = chunk_begin(plan, c + 1, chunks);
+        if ((st = forward_walk(plan, v0, v1 - v0, plan->d_stage_vol, plan->d_stage_sino, s)) !=
+                CTP_OK ||
+            cudaEventRecord(plan->ev_chunk[c], s) != cudaSuccess)
+            return host_fail(plan, s, st != CTP_OK ? st : CTP_E_CUDA);
+    }
+    for (int c = 0; c < chunks; ++c) {
+        const int v0 = chunk_begin(plan, c, chunks), v1 = chunk_begin(plan, c + 1, chunks);
+        if (cudaStreamWaitEvent(cs, plan->ev_chunk[c], 0) != cudaSuccess ||
+            cudaMemcpyAsync(sino_host + row * v0, plan->d_stage_sino + row * v0,
+                            sizeof(float) * row * (v1 - v0), cudaMemcpyDeviceToHost,
+                            cs) != cudaSuccess)
+            return host_fail(plan, s, CTP_E_CUDA);
+    }
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return host_fail(plan, s, CTP_E_CUDA);
     return CTP_OK;
 }
 
+// Backward over host buffers.  Each view chunk's sinogram rows go up on the
+// plan's copy stream and that chunk's walk waits only for them; the volume
+// comes down on the caller's stream at the end.
 int ctp_backward_host(ctp_plan_t *plan, const float *sino_host, float *vol_host, void *stream)
 {
     if (!plan || !vol_host || (!sino_host && plan->n_rays > 0)) return CTP_E_NULL;
     int st = check_device(plan);
     if (st != CTP_OK) return st;
     if ((st = ensure_stage(plan)) != CTP_OK) return st;
-    cudaStream_t s = (cudaStream_t)stream;
-    if (plan->n_rays > 0 &&
-        cudaMemcpyAsync(plan->d_stage_sino, sino_host, sizeof(float) * plan->n_rays,
-                        cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return CTP_E_CUDA;
-    const float *sino = plan->n_rays > 0 ? plan->d_stage_sino : plan->d_stage_vol;
-    if ((st = ctp_backward(plan, sino, plan->d_stage_vol, stream)) != CTP_OK) return st;
-    if (cudaMemcpyAsync(vol_host, plan->d_stage_vol, sizeof(float) * plan->n_cells,
-                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+    cudaStream_t s = (cudaStream_t)stream, cs = plan->copy_stream;
+    const size_t row = (size_t)plan->n_u * plan->n_v;
+    float *vol = plan->d_stage_vol;
+    if (backward_whole(plan)) {
+        if (plan->n_rays > 0 &&
+            cudaMemcpyAsync(plan->d_stage_sino, sino_host, sizeof(float) * plan->n_rays,
+                            cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return host_fail(plan, s, CTP_E_CUDA);
+        const float *sino = plan->n_rays > 0 ? plan->d_stage_sino : vol;
+        if (ctp::plane_backward_whole(ray_params(plan), plan->d_table, sino, vol, s))
+            return host_fail(plan, s, CTP_E_CUDA);
+    } else {
+        if (cudaEventRecord(plan->ev_start, s) != cudaSuccess ||
+            cudaStreamWaitEvent(cs, plan->ev_start, 0) != cudaSuccess)
+            return host_fail(plan, s, CTP_E_CUDA);
+        if ((st = backward_in(plan, vol, s)) != CTP_OK) return host_fail(plan, s, st);
+        const int chunks = plan->n_rays > 0 ? host_chunks(plan) : 0;
+        for (int c = 0; c < chunks; ++c) {
+            const int v0 = chunk_begin(plan, c, chunks), v1 = chunk_begin(plan, c + 1, chunks);
+            if (cudaMemcpyAsync(plan->d_stage_sino + row * v0, sino_host + row * v0,
+                                sizeof(float) * row * (v1 - v0), cudaMemcpyHostToDevice,
+                                cs) != cudaSuccess ||
+                cudaEventRecord(plan->ev_chunk[c], cs) != cudaSuccess ||
+                cudaStreamWaitEvent(s, plan->ev_chunk[c], 0) != cudaSuccess)
+                return host_fail(plan, s, CTP_E_CUDA);
+            if ((st = backward_walk(plan, v0, v1 - v0, plan->d_stage_sino, vol, s)) != CTP_OK)
+                return host_fail(plan, s, st);
+        }
+        if ((st = backward_out(plan, vol, s)) != CTP_OK) return host_fail(plan, s, st);
+    }
+    if (cudaMemcpyAsync(vol_host, vol, sizeof(float) * plan->n_cells, cudaMemcpyDeviceToHost,
+                        s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
-        return CTP_E_CUDA;
+        return host_fail(plan, s, CTP_E_CUDA);
     return CTP_OK;
 }
 
@@ -544,6 +712,8 @@ extern "C" int ctp_forward_static(const ctp_geometry *geom, const ctp_volume *vo
     P.stride[1] = vol->nx;
     P.stride[2] = vol->nx * vol->ny;
     P.min_len = (float)(1e-5 * std::fmin(vol->dx, std::fmin(vol->dy, vol->dz)));
+    P.view0 = 0;
+    P.view_count = geom->n_views;
     if (geom->n_v == 1) {
         dim3 grid((geom->n_u + 127) / 128, geom->n_views, 1);
         ctp::ray_forward_kernel<128, 1><<<grid, 128, 0, s>>>(P, vol_dev, sino_dev);

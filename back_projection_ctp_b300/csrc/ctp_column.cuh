@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(256, 5) column_forward_kernel(RayParams P,
     __shared__ float tile[32 * R][kColumnsPerBlock + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int iu = blockIdx.x * kColumnsPerBlock + warp;
-    const int view = blockIdx.y;
+    const int view = P.view0 + (int)blockIdx.y;
     const int row0 = blockIdx.z * 32 * R + lane;
     float out[R];
 #pragma unroll
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(256) column_backward_kernel(RayParams P,
                                                               float *__restrict__ zvol)
 {
     __shared__ float tile[32 * R][kColumnsPerBlock + 1];
-    const int view = blockIdx.y;
+    const int view = P.view0 + (int)blockIdx.y;
     for (int e = threadIdx.x; e < 32 * R * kColumnsPerBlock; e += 256) {
         const int rr = e / kColumnsPerBlock, c = e % kColumnsPerBlock;
         const int ivr = blockIdx.z * 32 * R + rr, iur = blockIdx.x * kColumnsPerBlock + c;
@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(256) column_count_kernel(RayParams P,
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int iu = blockIdx.x * kColumnsPerBlock + warp;
-    const int view = blockIdx.y;
+    const int view = P.view0 + (int)blockIdx.y;
     const int row0 = blockIdx.z * 32 * R + lane;
     unsigned n = 0;
     if (iu < P.n_u) {
@@ -620,7 +620,7 @@ inline int column_plan_build(const RayParams &P, ColumnPlan *plan, void **d_colu
 
 inline dim3 column_grid(const RayParams &P, int R)
 {
-    return dim3((P.n_u + kColumnsPerBlock - 1) / kColumnsPerBlock, P.n_views,
+    return dim3((P.n_u + kColumnsPerBlock - 1) / kColumnsPerBlock, P.view_count,
                 (P.n_v + 32 * R - 1) / (32 * R));
 }
 
@@ -629,10 +629,19 @@ inline dim3 transpose_grid(const RayParams &P)
     return dim3((P.n[0] + 31) / 32, (P.n[2] + 31) / 32, P.n[1]);
 }
 
-inline int column_forward(const RayParams &P, const ColumnPlan &plan, const void *d_columns,
-                          float *d_zfwd, const float *vol, float *sino, cudaStream_t s)
+// Stages of a call: layout in (forward), walk over P's view range, layout out
+// (backward).  ctp_forward / ctp_backward run them over all views; the host-
+// buffer entry points run the walk in view chunks overlapped with copies.
+inline int column_layout_in(const RayParams &P, float *d_zfwd, const float *vol, cudaStream_t s)
 {
     xfast_to_zfast_kernel<<<transpose_grid(P), 256, 0, s>>>(vol, d_zfwd, P.n[0], P.n[1], P.n[2]);
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+inline int column_walk_forward(const RayParams &P, const ColumnPlan &plan, const void *d_columns,
+                               const float *d_zfwd, float *sino, cudaStream_t s)
+{
+    if (P.view_count <= 0) return 0;
     const ColumnTrace *T = (const ColumnTrace *)d_columns;
     const int R = plan.rows_fwd;
     if (R == 4) column_forward_kernel<4><<<column_grid(P, 4), 256, 0, s>>>(P, T, d_zfwd, sino);
@@ -642,19 +651,26 @@ inline int column_forward(const RayParams &P, const ColumnPlan &plan, const void
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 
-inline int column_backward(const RayParams &P, const ColumnPlan &plan, const void *d_columns,
-                           float *d_zbwd, const float *sino, float *vol, cudaStream_t s)
+inline int column_backward_prepare(const RayParams &P, float *d_zbwd, cudaStream_t s)
 {
-    if (cudaMemsetAsync(d_zbwd, 0, sizeof(float) * column_padded_cells(P), s) != cudaSuccess)
-        return 9;
-    if ((long long)P.n_views * P.n_u * P.n_v > 0) {
-        const ColumnTrace *T = (const ColumnTrace *)d_columns;
-        const int R = plan.rows_bwd;
-        if (R == 4) column_backward_kernel<4><<<column_grid(P, 4), 256, 0, s>>>(P, T, sino, d_zbwd);
-        else if (R == 3) column_backward_kernel<3><<<column_grid(P, 3), 256, 0, s>>>(P, T, sino, d_zbwd);
-        else if (R == 2) column_backward_kernel<2><<<column_grid(P, 2), 256, 0, s>>>(P, T, sino, d_zbwd);
-        else column_backward_kernel<1><<<column_grid(P, 1), 256, 0, s>>>(P, T, sino, d_zbwd);
-    }
+    return cudaMemsetAsync(d_zbwd, 0, sizeof(float) * column_padded_cells(P), s) == cudaSuccess ? 0 : 9;
+}
+
+inline int column_walk_backward(const RayParams &P, const ColumnPlan &plan, const void *d_columns,
+                                const float *sino, float *d_zbwd, cudaStream_t s)
+{
+    if (P.view_count <= 0 || P.n_u <= 0 || P.n_v <= 0) return 0;
+    const ColumnTrace *T = (const ColumnTrace *)d_columns;
+    const int R = plan.rows_bwd;
+    if (R == 4) column_backward_kernel<4><<<column_grid(P, 4), 256, 0, s>>>(P, T, sino, d_zbwd);
+    else if (R == 3) column_backward_kernel<3><<<column_grid(P, 3), 256, 0, s>>>(P, T, sino, d_zbwd);
+    else if (R == 2) column_backward_kernel<2><<<column_grid(P, 2), 256, 0, s>>>(P, T, sino, d_zbwd);
+    else column_backward_kernel<1><<<column_grid(P, 1), 256, 0, s>>>(P, T, sino, d_zbwd);
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+inline int column_layout_out(const RayParams &P, const float *d_zbwd, float *vol, cudaStream_t s)
+{
     zfast_to_xfast_kernel<<<transpose_grid(P), 256, 0, s>>>(d_zbwd, vol, P.n[0], P.n[1], P.n[2]);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }

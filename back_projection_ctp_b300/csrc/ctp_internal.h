@@ -24,6 +24,8 @@ struct RayParams {
     int stride[3];        // element stride of x, y, z in the (nz, ny, nx) buffer
     double spacing[3];    // dx, dy, dz
     float min_len;        // segment counter: pieces longer than this (physical units)
+    int view0;            // first view of a launch (grid row y handles view view0 + y)
+    int view_count;       // views of a launch
 };
 
 }  // namespace ctp

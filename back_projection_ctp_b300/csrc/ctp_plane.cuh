@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(32 * CH) plane_forward_kernel(RayParams P,
     __shared__ float part[CH][32];
     const int lane = threadIdx.x & 31, chunk = threadIdx.x >> 5;
     const int iu = blockIdx.x * 32 + lane;
-    const long long ray = (long long)blockIdx.y * P.n_u + iu;
+    const long long ray = (long long)(P.view0 + (int)blockIdx.y) * P.n_u + iu;
     float acc = 0.0f;
     PlaneRay R;
     R.k0 = 0;
@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(32 * CH) plane_backward_kernel(RayParams P,
     const int lane = threadIdx.x & 31, chunk = threadIdx.x >> 5;
     const int iu = blockIdx.x * 32 + lane;
     if (iu >= P.n_u) return;
-    const long long ray = (long long)blockIdx.y * P.n_u + iu;
+    const int view = P.view0 + (int)blockIdx.y;
+    const long long ray = (long long)view * P.n_u + iu;
     const float y = sino[ray];
     if (y == 0.0f) return;
     const PlaneRay R = T[ray];
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(32 * CH) plane_backward_kernel(RayParams P,
     const int ka = R.k0 + chunk * len;
     const int kb = min(ka + len - 1, R.k1);
     if (ka > kb) return;
-    PlaneScatter op{img + (long long)(blockIdx.y % copies) * copy_cells, __fmul_rn(R.ell, y)};
+    PlaneScatter op{img + (long long)(view % copies) * copy_cells, __fmul_rn(R.ell, y)};
     plane_walk_range(R, ka, kb, op);
 }
 
@@ -321,7 +322,8 @@ __global__ void __launch_bounds__(kPlaneBlock) plane_count_kernel(RayParams P,
                                                                   const PlaneRay *__restrict__ T,
                                                                   unsigned long long *__restrict__ total)
 {
-    const long long ray = (long long)blockIdx.y * P.n_u + blockIdx.x * kPlaneBlock + threadIdx.x;
+    const long long ray =
+        (long long)(P.view0 + (int)blockIdx.y) * P.n_u + blockIdx.x * kPlaneBlock + threadIdx.x;
     unsigned n = 0;
     if (blockIdx.x * kPlaneBlock + threadIdx.x < P.n_u) {
         const PlaneRay R = T[ray];
@@ -568,7 +570,7 @@ inline int plane_plan_build(const RayParams &P, void **d_rays, float **d_fwd, fl
 
 inline dim3 plane_grid(const RayParams &P)
 {
-    return dim3((P.n_u + kPlaneBlock - 1) / kPlaneBlock, P.n_views, 1);
+    return dim3((P.n_u + kPlaneBlock - 1) / kPlaneBlock, P.view_count, 1);
 }
 
 // Chunks per ray: enough threads for about four waves of the whole GPU.
@@ -583,7 +585,7 @@ inline int plane_chunks(const RayParams &P)
 
 inline dim3 plane_chunk_grid(const RayParams &P)
 {
-    return dim3((P.n_u + 31) / 32, P.n_views, 1);
+    return dim3((P.n_u + 31) / 32, P.view_count, 1);
 }
 
 inline dim3 plane_tgrid(const PlaneLayout &G)
@@ -591,11 +593,29 @@ inline dim3 plane_tgrid(const PlaneLayout &G)
     return dim3((G.nx + 31) / 32, (G.ny + 31) / 32, 1);
 }
 
-inline int plane_forward(const RayParams &P, const void *d_rays, float *d_fwd, const float *img,
-                         float *sino, cudaStream_t s)
+// Stages of a call (see the column path): layout in, walk over P's view range,
+// layout out.  Small scans (launch- and latency-bound) use the shared-memory
+// tiled backward, which walks all views in one launch (plane_backward_whole).
+// Larger ones use fire-and-forget global reductions into the privatised padded
+// copies, which measured faster than shared-memory float atomics (C2: 0.46 vs
+// 0.66 ms).  CTP_PLANE_BACKWARD = t / r forces either.
+inline bool plane_backward_tiled(const RayParams &P)
+{
+    const char *mode = getenv("CTP_PLANE_BACKWARD");
+    return mode ? mode[0] == 't' : (long long)P.n_views * P.n_u <= 65536;
+}
+
+inline int plane_layout_in(const RayParams &P, float *d_fwd, const float *img, cudaStream_t s)
 {
     const PlaneLayout G = plane_layout(P);
     plane_pack_kernel<<<plane_tgrid(G), 256, 0, s>>>(G, img, d_fwd);
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+inline int plane_walk_forward(const RayParams &P, const void *d_rays, const float *d_fwd,
+                              float *sino, cudaStream_t s)
+{
+    if (P.view_count <= 0) return 0;
     const PlaneRay *T = (const PlaneRay *)d_rays;
     switch (plane_chunks(P)) {
     case 8: plane_forward_kernel<8><<<plane_chunk_grid(P), 256, 0, s>>>(P, T, d_fwd, sino); break;
@@ -606,45 +626,54 @@ inline int plane_forward(const RayParams &P, const void *d_rays, float *d_fwd, c
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 
-inline int plane_backward(const RayParams &P, const void *d_rays, float *d_bwd, const float *sino,
-                          float *img, cudaStream_t s)
+// Privatised-accumulator backward: prepare, walk view ranges, layout out.
+inline int plane_backward_prepare(const RayParams &P, float *d_bwd, cudaStream_t s)
 {
-    // Small scans (launch- and latency-bound): shared-memory tiles.  Larger ones:
-    // fire-and-forget global reductions into the privatised padded copies, which
-    // measured faster than shared-memory float atomics (C2: 0.46 vs 0.66 ms).
-    // CTP_PLANE_BACKWARD = t / r forces either.
-    const char *mode = getenv("CTP_PLANE_BACKWARD");
-    const bool tiled = mode ? mode[0] == 't' : (long long)P.n_views * P.n_u <= 65536;
-    if (tiled) {
-        // tiled: zero the output, one block per (tile, view group)
-        if (cudaMemsetAsync(img, 0, sizeof(float) * (size_t)P.n[0] * P.n[1], s) != cudaSuccess)
-            return 9;
-        if ((long long)P.n_views * P.n_u == 0) return 0;
-        const int tiles = ((P.n[0] + kTile - 1) / kTile) * ((P.n[1] + kTile - 1) / kTile);
-        int groups = (4 * 148 + tiles - 1) / tiles;
-        groups = max(1, min(groups, (P.n_views + 7) / 8));
-        const int vpb = (P.n_views + groups - 1) / groups;
-        groups = (P.n_views + vpb - 1) / vpb;
-        plane_backward_tiled_kernel<<<dim3(tiles, groups), 256, 0, s>>>(
-            P, (const PlaneRay *)d_rays, sino, img, vpb);
-        return cudaGetLastError() == cudaSuccess ? 0 : 9;
-    }
+    const PlaneLayout G = plane_layout(P);
+    const size_t bytes = sizeof(float) * plane_buffer_cells(G) * plane_copies(P, G);
+    return cudaMemsetAsync(d_bwd, 0, bytes, s) == cudaSuccess ? 0 : 9;
+}
+
+inline int plane_walk_backward(const RayParams &P, const void *d_rays, const float *sino,
+                               float *d_bwd, cudaStream_t s)
+{
+    if (P.view_count <= 0 || P.n_u <= 0) return 0;
     const PlaneLayout G = plane_layout(P);
     const int copies = plane_copies(P, G);
     const long long copy_cells = (long long)plane_buffer_cells(G);
-    if (cudaMemsetAsync(d_bwd, 0, sizeof(float) * plane_buffer_cells(G) * copies, s) != cudaSuccess)
-        return 9;
-    if ((long long)P.n_views * P.n_u > 0) {
-        const PlaneRay *T = (const PlaneRay *)d_rays;
-        const dim3 g = plane_chunk_grid(P);
-        switch (plane_chunks(P)) {
-        case 8: plane_backward_kernel<8><<<g, 256, 0, s>>>(P, T, sino, d_bwd, copies, copy_cells); break;
-        case 4: plane_backward_kernel<4><<<g, 128, 0, s>>>(P, T, sino, d_bwd, copies, copy_cells); break;
-        case 2: plane_backward_kernel<2><<<g, 64, 0, s>>>(P, T, sino, d_bwd, copies, copy_cells); break;
-        default: plane_backward_kernel<1><<<g, 32, 0, s>>>(P, T, sino, d_bwd, copies, copy_cells); break;
-        }
+    const PlaneRay *T = (const PlaneRay *)d_rays;
+    const dim3 g = plane_chunk_grid(P);
+    switch (plane_chunks(P)) {
+    case 8: plane_backward_kernel<8><<<g, 256, 0, s>>>(P, T, sino, d_bwd, copies, copy_cells); break;
+    case 4: plane_backward_kernel<4><<<g, 128, 0, s>>>(P, T, sino, d_bwd, copies, copy_cells); break;
+    case 2: plane_backward_kernel<2><<<g, 64, 0, s>>>(P, T, sino, d_bwd, copies, copy_cells); break;
+    default: plane_backward_kernel<1><<<g, 32, 0, s>>>(P, T, sino, d_bwd, copies, copy_cells); break;
     }
-    plane_unpack_kernel<<<plane_tgrid(G), 256, 0, s>>>(G, d_bwd, img, copies, copy_cells);
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+inline int plane_layout_out(const RayParams &P, const float *d_bwd, float *img, cudaStream_t s)
+{
+    const PlaneLayout G = plane_layout(P);
+    plane_unpack_kernel<<<plane_tgrid(G), 256, 0, s>>>(G, d_bwd, img, plane_copies(P, G),
+                                                        (long long)plane_buffer_cells(G));
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+// Small scans: zero the output, one block per (tile, view group), all views.
+inline int plane_backward_whole(const RayParams &P, const void *d_rays, const float *sino,
+                                float *img, cudaStream_t s)
+{
+    if (cudaMemsetAsync(img, 0, sizeof(float) * (size_t)P.n[0] * P.n[1], s) != cudaSuccess)
+        return 9;
+    if ((long long)P.n_views * P.n_u == 0) return 0;
+    const int tiles = ((P.n[0] + kTile - 1) / kTile) * ((P.n[1] + kTile - 1) / kTile);
+    int groups = (4 * 148 + tiles - 1) / tiles;
+    groups = max(1, min(groups, (P.n_views + 7) / 8));
+    const int vpb = (P.n_views + groups - 1) / groups;
+    groups = (P.n_views + vpb - 1) / vpb;
+    plane_backward_tiled_kernel<<<dim3(tiles, groups), 256, 0, s>>>(
+        P, (const PlaneRay *)d_rays, sino, img, vpb);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 

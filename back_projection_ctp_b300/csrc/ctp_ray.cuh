@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(TU *TV) ray_forward_kernel(RayParams P,
 {
     const int iu = blockIdx.x * TU + (int)(threadIdx.x % TU);
     const int iv = blockIdx.z * TV + (int)(threadIdx.x / TU);
-    const int view = blockIdx.y;
+    const int view = P.view0 + (int)blockIdx.y;
     if (iu >= P.n_u || iv >= P.n_v) return;
     float out = 0.0f;
     SlabRay R;
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(TU *TV) ray_backward_kernel(RayParams P,
 {
     const int iu = blockIdx.x * TU + (int)(threadIdx.x % TU);
     const int iv = blockIdx.z * TV + (int)(threadIdx.x / TU);
-    const int view = blockIdx.y;
+    const int view = P.view0 + (int)blockIdx.y;
     if (iu >= P.n_u || iv >= P.n_v) return;
     const float y = sino[((long long)view * P.n_v + iv) * P.n_u + iu];
     if (y == 0.0f) return;
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(TU *TV) ray_count_kernel(RayParams P,
 {
     const int iu = blockIdx.x * TU + (int)(threadIdx.x % TU);
     const int iv = blockIdx.z * TV + (int)(threadIdx.x / TU);
-    const int view = blockIdx.y;
+    const int view = P.view0 + (int)blockIdx.y;
     unsigned n = 0;
     if (iu < P.n_u && iv < P.n_v) {
         SlabRay R;

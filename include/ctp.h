@@ -155,10 +155,19 @@ int ctp_segment_count(const ctp_plan_t *plan, unsigned long long *out, void *str
 
 /*
  * Host-buffer variants (end-to-end): copy the input from host memory, run the
- * operator, copy the result back, and wait for the stream.  Host buffers may be
- * pageable or pinned (pinned copies overlap better).  The plan allocates one
- * device volume and one device sinogram on the first host-buffer call (do that
- * first call before any stream capture) and reuses them.
+ * operator, copy the result back, and return once the result is in host memory.
+ * Results equal the device calls' (the forward bit for bit, the backward up to
+ * its atomics' summation order).  Host buffers may be pageable or pinned; with
+ * pinned buffers the sinogram transfer overlaps the walk: the walk runs in view
+ * chunks on `stream` (one chunk per 64 MiB of sinogram, at most 8; the
+ * environment variable CTP_HOST_CHUNKS = 1..64 overrides) and each chunk's
+ * sinogram rows move on a second stream owned by the plan -- down as soon as the
+ * chunk is walked (forward), up just before it is walked (backward).  The
+ * volume moves on `stream`.  The plan allocates one device volume, one device
+ * sinogram, the copy stream and its events on the first host-buffer call and
+ * reuses them; these calls cannot be captured into a CUDA graph.  Calls on one
+ * plan must not run concurrently.  Errors as ctp_forward; after an error the
+ * call has waited for every copy it queued.
  */
 int ctp_forward_host(ctp_plan_t *plan, const float *vol_host, float *sino_host, void *stream);
 int ctp_backward_host(ctp_plan_t *plan, const float *sino_host, float *vol_host, void *stream);

@@ -143,19 +143,42 @@ def test_tilted_2d_frames_fall_back_to_ray_path(torch, ctp, oracle_mod):
     assert rel_l2(p, p_ref) <= TOL_FORWARD
 
 
-def test_host_entry_points_match_device(torch, ctp):
-    w = SMALL[3]
+@pytest.mark.parametrize("idx,path,backward", [(3, "auto", None), (3, "ray", None),
+                                               (2, "auto", "r"), (2, "auto", "t"),
+                                               (5, "auto", None)])
+@pytest.mark.parametrize("chunks", [None, "1", "3", "7"])
+@pytest.mark.parametrize("pinned", [False, True])
+def test_host_entry_points_match_device(torch, ctp, monkeypatch, idx, path, backward, chunks,
+                                        pinned):
+    """The host-buffer calls (view-chunked, copies overlapped with the walk)
+    give the device calls' results: the forward bit for bit, the backward up to
+    the order of its float atomics."""
+    if backward:
+        monkeypatch.setenv("CTP_PLANE_BACKWARD", backward)
+    if chunks:
+        monkeypatch.setenv("CTP_HOST_CHUNKS", chunks)
+    w = SMALL[idx]
     f = ci.frames(w)
-    plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w))
+    plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w), path)
     vol = ci.phantom(w)
     y = ci.sinogram_noise(w)
     p_dev, g_dev = _run_pair(torch, ctp, plan, vol, y)
-    p_host = np.empty(plan.sino_shape, np.float32)
-    ctp.ctp_forward_host(plan, vol, p_host)
-    g_host = np.empty(plan.vol_shape, np.float32)
-    ctp.ctp_backward_host(plan, y, g_host)
-    assert np.array_equal(p_host, p_dev)
-    assert rel_l2(g_host, g_dev) <= 1e-6
+
+    def buf(shape, fill=None):
+        t = torch.empty(shape, dtype=torch.float32, pin_memory=pinned)
+        a = t.numpy()
+        a[...] = np.nan if fill is None else fill
+        return t, a
+
+    _, vol_h = buf(plan.vol_shape, vol)
+    _, y_h = buf(plan.sino_shape, y)
+    _, p_host = buf(plan.sino_shape)
+    _, g_host = buf(plan.vol_shape)
+    for _ in range(2):   # the second call reuses the staging buffers, stream and events
+        ctp.ctp_forward_host(plan, vol_h, p_host)
+        ctp.ctp_backward_host(plan, y_h, g_host)
+        assert np.array_equal(p_host, p_dev)
+        assert rel_l2(g_host, g_dev) <= 1e-6
 
 
 # ------------------------------------------------------------------ edge cases
