@@ -102,8 +102,11 @@ class Scan:
     the world (x, y, z) of the min corner of voxel (0, 0, 0)."""
 
     def __init__(self, beam, src, det_centre, det_u, det_v, n_u, n_v, pitch_u, pitch_v,
-                 shape, spacing, origin, offset_u=0.0, offset_v=0.0):
+                 shape, spacing, origin, offset_u=0.0, offset_v=0.0, ndim=3):
         self.beam = beam
+        self.ndim = int(ndim)
+        self.pitch_u, self.pitch_v = float(pitch_u), float(pitch_v)
+        self.offset_u, self.offset_v = float(offset_u), float(offset_v)
         self.arrays = [np.ascontiguousarray(a, dtype=np.float32).reshape(-1, 3)
                        for a in (src, det_centre, det_u, det_v)]
         self.n_views = self.arrays[0].shape[0]
@@ -128,7 +131,7 @@ class Scan:
     def from_workload(cls, w, frames):
         return cls(w.beam, frames["src"], frames["det_centre"], frames["det_u"],
                    frames["det_v"], w.n_u, w.n_v, w.pitch_u, w.pitch_v, w.shape,
-                   w.spacing, w.origin, w.offset_u, w.offset_v)
+                   w.spacing, w.origin, w.offset_u, w.offset_v, w.ndim)
 
     @property
     def n_rays(self):
