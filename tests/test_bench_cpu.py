@@ -46,20 +46,22 @@ import bench
 world, rank, local = bench.dist_setup(2)
 bench.barrier(world)
 v = bench.max_over_ranks(float(rank + 1) * 1.5, world)
-print(json.dumps({{"rank": rank, "max": v}}))
+# one file per rank: lines printed by two processes to one pipe can interleave
+with open(os.path.join({out!r}, f"rank{{rank}}.json"), "w") as fh:
+    fh.write(json.dumps({{"rank": rank, "max": v}}))
 dist.destroy_process_group()
 """
 
 
 def test_max_over_ranks_two_gloo_ranks(tmp_path):
     script = tmp_path / "worker.py"
-    script.write_text(_WORKER.format(root=ROOT))
+    script.write_text(_WORKER.format(root=ROOT, out=str(tmp_path)))
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), str(script)]
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
     out = subprocess.run(cmd, capture_output=True, text=True, timeout=300, env=env)
     assert out.returncode == 0, out.stderr[-2000:]
-    recs = [json.loads(l) for l in out.stdout.splitlines() if l.startswith("{")]
+    recs = [json.loads((tmp_path / f"rank{r}.json").read_text()) for r in (0, 1)]
     assert sorted(r["rank"] for r in recs) == [0, 1]
     assert all(r["max"] == 3.0 for r in recs)
 
