@@ -52,7 +52,10 @@ class _PlanInfo(ctypes.Structure):
 
 EXPORTS = ("ctp_plan", "ctp_destroy", "ctp_plan_info_get", "ctp_forward", "ctp_backward",
            "ctp_segment_count", "ctp_forward_host", "ctp_backward_host", "ctp_status_string",
-           "ctp_forward_static")
+           "ctp_forward_static", "ctp_ramp_filter", "ctp_weighted_backproject",
+           "ctp_weighted_backproject_transpose", "ctp_fdk")
+
+RAMPS = {"ramlak": 0, "shepp_logan": 1}
 
 
 def load_library(path: str | None = None):
@@ -77,6 +80,10 @@ def load_library(path: str | None = None):
         lib.ctp_segment_count.argtypes = [P, ctypes.POINTER(ctypes.c_ulonglong), P]
         lib.ctp_forward_static.argtypes = [ctypes.POINTER(_Geometry), ctypes.POINTER(_Volume),
                                            P, P, P]
+        lib.ctp_ramp_filter.argtypes = [P, P, P, P, I, I, P]
+        lib.ctp_weighted_backproject.argtypes = [P, P, P, P]
+        lib.ctp_weighted_backproject_transpose.argtypes = [P, P, P, P]
+        lib.ctp_fdk.argtypes = [P, P, P, P, P, I, P]
         lib.ctp_status_string.argtypes = [I]
         lib.ctp_status_string.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -294,3 +301,55 @@ def ctp_backward_host(plan: Plan, sino_host, vol_host, stream=None):
 
 def ctp_destroy(plan: Plan):
     plan.destroy()
+
+
+# --------------------------------------------------------------- analytical operators
+def _view_weight(plan: Plan, view_weight):
+    if view_weight is None:
+        return None
+    return _device_f32(view_weight, (plan.sino_shape[0],), "view_weight")
+
+
+def ctp_ramp_filter(plan: Plan, sino, out, view_weight=None, ramp: str = "ramlak",
+                    transpose: bool = False, stream=None):
+    """out <- ramp filter along u of the cosine-weighted sino, times the view
+    weights (transpose: the transposed operator).  ``out`` may be ``sino``."""
+    _check(load_library().ctp_ramp_filter(
+        plan.handle, _device_f32(sino, plan.sino_shape, "sino"),
+        _device_f32(out, plan.sino_shape, "out"), _view_weight(plan, view_weight),
+        RAMPS[ramp], int(bool(transpose)), _stream_ptr(stream)), "ctp_ramp_filter")
+    return out
+
+
+def ctp_weighted_backproject(plan: Plan, sino, vol, stream=None):
+    """vol <- voxel-driven weighted gather of (filtered) sino (vol overwritten)."""
+    _check(load_library().ctp_weighted_backproject(
+        plan.handle, _device_f32(sino, plan.sino_shape, "sino"),
+        _device_f32(vol, plan.vol_shape, "vol"), _stream_ptr(stream)),
+        "ctp_weighted_backproject")
+    return vol
+
+
+def ctp_weighted_backproject_transpose(plan: Plan, vol, sino, stream=None):
+    """sino <- transpose of the weighted gather applied to vol (sino overwritten)."""
+    _check(load_library().ctp_weighted_backproject_transpose(
+        plan.handle, _device_f32(vol, plan.vol_shape, "vol"),
+        _device_f32(sino, plan.sino_shape, "sino"), _stream_ptr(stream)),
+        "ctp_weighted_backproject_transpose")
+    return sino
+
+
+def ctp_fdk(plan: Plan, sino, work, vol, view_weight=None, ramp: str = "ramlak", stream=None):
+    """vol <- FBP / FDK of sino: ramp filter into ``work`` (may be ``sino``), then the
+    weighted gather."""
+    _check(load_library().ctp_fdk(
+        plan.handle, _device_f32(sino, plan.sino_shape, "sino"),
+        _device_f32(work, plan.sino_shape, "work"), _device_f32(vol, plan.vol_shape, "vol"),
+        _view_weight(plan, view_weight), RAMPS[ramp], _stream_ptr(stream)), "ctp_fdk")
+    return vol
+
+
+def full_scan_view_weights(n_views: int):
+    """View weights of a full 2 pi scan with equally spaced views: pi / n_views
+    (the angular step, halved because every line is measured twice)."""
+    return np.full(int(n_views), np.pi / max(int(n_views), 1), dtype=np.float32)

@@ -14,7 +14,9 @@ from __future__ import annotations
 
 import torch
 
-from ._binding import Geometry, Plan, Volume, ctp_backward, ctp_forward, ctp_plan
+from ._binding import (Geometry, Plan, Volume, ctp_backward, ctp_forward, ctp_plan,
+                       ctp_ramp_filter, ctp_weighted_backproject,
+                       ctp_weighted_backproject_transpose)
 
 
 class Projector:
@@ -42,6 +44,18 @@ class Projector:
 
     def backproject(self, sino: torch.Tensor) -> torch.Tensor:
         return _Backproject.apply(sino, self)
+
+    def fdk(self, sino: torch.Tensor, view_weight: torch.Tensor | None = None,
+            ramp: str = "ramlak") -> torch.Tensor:
+        """Differentiable FBP / FDK: ramp filter (cosine and view weights) then the
+        weighted gather; the gradient is the transposed filter of the gather's
+        transpose (diffct README "Differentiable FBP and FDK": sinogram gradients
+        through the transposed interpolation stencil).  ``view_weight``: (n_views,)
+        tensor, e.g. ``full_scan_view_weights``; no gradient flows to it."""
+        vw = None
+        if view_weight is not None:
+            vw = view_weight.detach().to(device=self.device, dtype=torch.float32).contiguous()
+        return _Gather.apply(_Filter.apply(sino, self, vw, ramp), self)
 
     __call__ = project
 
@@ -86,4 +100,51 @@ class _Backproject(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad):
         g = _Project.apply(grad, ctx.proj)
+        return g.to(dtype=ctx.in_dtype, device=ctx.in_device), None
+
+
+def _filter_fn(vw, ramp, transpose):
+    def fn(plan, x, out, stream):
+        ctp_ramp_filter(plan, x, out, vw, ramp, transpose, stream)
+    return fn
+
+
+class _Filter(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, sino, proj, vw, ramp, transpose=False):
+        ctx.proj, ctx.vw, ctx.ramp, ctx.transpose = proj, vw, ramp, transpose
+        ctx.in_dtype, ctx.in_device = sino.dtype, sino.device
+        return _apply(proj, sino, proj.sino_shape, proj.sino_shape,
+                      _filter_fn(vw, ramp, transpose))
+
+    @staticmethod
+    def backward(ctx, grad):
+        g = _Filter.apply(grad, ctx.proj, ctx.vw, ctx.ramp, not ctx.transpose)
+        return g.to(dtype=ctx.in_dtype, device=ctx.in_device), None, None, None, None
+
+
+class _Gather(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, sino, proj):
+        ctx.proj = proj
+        ctx.in_dtype, ctx.in_device = sino.dtype, sino.device
+        return _apply(proj, sino, proj.sino_shape, proj.vol_shape, ctp_weighted_backproject)
+
+    @staticmethod
+    def backward(ctx, grad):
+        g = _GatherT.apply(grad, ctx.proj)
+        return g.to(dtype=ctx.in_dtype, device=ctx.in_device), None
+
+
+class _GatherT(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, vol, proj):
+        ctx.proj = proj
+        ctx.in_dtype, ctx.in_device = vol.dtype, vol.device
+        return _apply(proj, vol, proj.vol_shape, proj.sino_shape,
+                      ctp_weighted_backproject_transpose)
+
+    @staticmethod
+    def backward(ctx, grad):
+        g = _Gather.apply(grad, ctx.proj)
         return g.to(dtype=ctx.in_dtype, device=ctx.in_device), None

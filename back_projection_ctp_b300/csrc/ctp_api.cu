@@ -17,6 +17,7 @@
 
 #include "ctp.h"
 #include "ctp_column.cuh"
+#include "ctp_fdk.cuh"
 #include "ctp_plane.cuh"
 #include "ctp_internal.h"
 #include "ctp_ray.cuh"
@@ -43,6 +44,11 @@ struct ctp_plan {
     cudaStream_t copy_stream = nullptr;     // sinogram chunks move here, beside the walk
     cudaEvent_t ev_start = nullptr;         // work queued on the caller's stream before a call
     cudaEvent_t ev_chunk[64] = {};          // chunk c walked (forward) or staged (backward)
+    // analytical operators
+    int fdk_status = CTP_E_GEOMETRY;
+    ctp::FdkParams fdk{};
+    ctp::FdkView *d_fdk = nullptr;
+    float *d_ramp[2] = {nullptr, nullptr};  // Ram-Lak, Shepp-Logan kernels (2 n_u - 1)
     unsigned long long device_bytes = 0;
 };
 
@@ -196,6 +202,9 @@ void free_plan(ctp_plan_t *p)
     cudaFree(p->d_work_bwd);
     cudaFree(p->d_stage_vol);
     cudaFree(p->d_stage_sino);
+    cudaFree(p->d_fdk);
+    cudaFree(p->d_ramp[0]);
+    cudaFree(p->d_ramp[1]);
     if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
     if (p->ev_start) cudaEventDestroy(p->ev_start);
     for (cudaEvent_t e : p->ev_chunk)
@@ -274,6 +283,47 @@ int validate(const ctp_geometry *g, const ctp_volume *v)
     return CTP_OK;
 }
 
+// Tables of the analytical operators (small: one FdkView per view and the two
+// ramp kernels).  A scan outside their class only records CTP_E_GEOMETRY.
+int fdk_setup(ctp_plan_t *p, const ctp_geometry *g, const ctp_volume *v)
+{
+    std::vector<ctp::FdkView> views;
+    const int n[3] = {v->nx, v->ny, v->nz};
+    const double d[3] = {v->dx, v->dy, v->dz}, o[3] = {v->ox, v->oy, v->oz};
+    const int st = ctp::fdk_build(g->ndim, g->beam, g->n_views, g->n_u, g->n_v, g->src,
+                                  g->det_centre, g->det_u, g->det_v, g->pitch_u, g->pitch_v,
+                                  g->offset_u, g->offset_v, n, d, o, views, p->fdk);
+    if (st != 0) {
+        p->fdk_status = CTP_E_GEOMETRY;
+        return CTP_OK;
+    }
+    const size_t vbytes = sizeof(ctp::FdkView) * views.size();
+    if (cudaMalloc(&p->d_fdk, vbytes) != cudaSuccess ||
+        cudaMemcpy(p->d_fdk, views.data(), vbytes, cudaMemcpyHostToDevice) != cudaSuccess)
+        return CTP_E_CUDA;
+    p->device_bytes += vbytes;
+    p->fdk.views = p->d_fdk;
+    if (g->n_u <= ctp::kFilterMaxU) {
+        for (int kind = 0; kind < 2; ++kind) {
+            std::vector<float> h;
+            ctp::fdk_ramp_kernel(g->n_u, g->pitch_u, kind, h);
+            const size_t hb = sizeof(float) * h.size();
+            if (cudaMalloc(&p->d_ramp[kind], hb) != cudaSuccess ||
+                cudaMemcpy(p->d_ramp[kind], h.data(), hb, cudaMemcpyHostToDevice) != cudaSuccess)
+                return CTP_E_CUDA;
+            p->device_bytes += hb;
+        }
+    }
+    p->fdk_status = CTP_OK;
+    return CTP_OK;
+}
+
+int fdk_check(const ctp_plan_t *plan)
+{
+    const int st = check_device(plan);
+    return st != CTP_OK ? st : plan->fdk_status;
+}
+
 }  // namespace
 
 extern "C" {
@@ -294,6 +344,8 @@ const char *ctp_status_string(int status)
     case CTP_E_DEVICE: return "current CUDA device differs from the plan's";
     case CTP_E_OPTION: return "unknown ndim, beam or path";
     case CTP_E_LIMIT: return "request exceeds a fixed limit of this entry point";
+    case CTP_E_GEOMETRY:
+        return "scan outside the analytical operators' class (3-D needs v = +-z, u horizontal)";
     default: return "unknown status";
     }
 }
@@ -397,6 +449,10 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
             free_plan(p);
             return st;
         }
+    }
+    if ((st = fdk_setup(p, geom, vol)) != CTP_OK) {
+        free_plan(p);
+        return st;
     }
     *out = p;
     return CTP_OK;
@@ -606,6 +662,53 @@ int ctp_backward_host(ctp_plan_t *plan, const float *sino_host, float *vol_host,
         cudaStreamSynchronize(s) != cudaSuccess)
         return host_fail(plan, s, CTP_E_CUDA);
     return CTP_OK;
+}
+
+int ctp_ramp_filter(const ctp_plan_t *plan, const float *sino_dev, float *out_dev,
+                    const float *view_weight_dev, int ramp, int transpose, void *stream)
+{
+    if (!plan) return CTP_E_NULL;
+    if (plan->n_rays > 0 && (!sino_dev || !out_dev)) return CTP_E_NULL;
+    if (ramp != CTP_RAMLAK && ramp != CTP_SHEPP_LOGAN) return CTP_E_OPTION;
+    int st = fdk_check(plan);
+    if (st != CTP_OK) return st;
+    if (!plan->d_ramp[ramp]) return CTP_E_LIMIT;
+    return ctp::fdk_filter(plan->fdk, plan->d_ramp[ramp], sino_dev, out_dev, view_weight_dev,
+                           transpose ? 1 : 0, (cudaStream_t)stream)
+               ? CTP_E_CUDA : CTP_OK;
+}
+
+int ctp_weighted_backproject(const ctp_plan_t *plan, const float *sino_dev, float *vol_dev,
+                             void *stream)
+{
+    if (!plan || !vol_dev || (plan->n_rays > 0 && !sino_dev)) return CTP_E_NULL;
+    int st = fdk_check(plan);
+    if (st != CTP_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (plan->n_rays == 0)
+        return cudaMemsetAsync(vol_dev, 0, sizeof(float) * plan->n_cells, s) == cudaSuccess
+                   ? CTP_OK : CTP_E_CUDA;
+    return ctp::fdk_gather(plan->fdk, sino_dev, vol_dev, s) ? CTP_E_CUDA : CTP_OK;
+}
+
+int ctp_weighted_backproject_transpose(const ctp_plan_t *plan, const float *vol_dev,
+                                       float *sino_dev, void *stream)
+{
+    if (!plan || !vol_dev || (plan->n_rays > 0 && !sino_dev)) return CTP_E_NULL;
+    int st = fdk_check(plan);
+    if (st != CTP_OK) return st;
+    if (plan->n_rays == 0) return CTP_OK;
+    return ctp::fdk_scatter(plan->fdk, vol_dev, sino_dev, (cudaStream_t)stream) ? CTP_E_CUDA
+                                                                                : CTP_OK;
+}
+
+int ctp_fdk(const ctp_plan_t *plan, const float *sino_dev, float *work_dev, float *vol_dev,
+            const float *view_weight_dev, int ramp, void *stream)
+{
+    if (!plan || !vol_dev || (plan->n_rays > 0 && (!sino_dev || !work_dev))) return CTP_E_NULL;
+    int st = ctp_ramp_filter(plan, sino_dev, work_dev, view_weight_dev, ramp, 0, stream);
+    if (st != CTP_OK) return st;
+    return ctp_weighted_backproject(plan, work_dev, vol_dev, stream);
 }
 
 }  // extern "C"

@@ -1,0 +1,618 @@
+// Analytical FBP / FDK operators on a plan's geometry: the ramp filter (with
+// its cosine and view weights), the voxel-driven weighted gather with bilinear
+// interpolation, and the gather's exact transpose.
+//
+// What they compute (diffct release pages, my.diffend.io): the analytical
+// helpers -- ramp filters (Ram-Lak and Shepp-Logan among them), fan / cone
+// weights and FBP / FDK backprojection (diffct 2.1.0 -> 2.2.1, README
+// "Analytical helpers"); a voxel-driven gather, one thread per output voxel,
+// with the analytical constant 1/(2 pi) (parallel) or SDD/(2 pi SID) per view
+// (fan, cone), and a dedicated transpose of the same interpolation stencil
+// (diffct 2.1.0 -> 2.2.1 and 2.4.3 -> 2.4.4, diffct/analytical.py,
+// `_analytical_transpose_raw`; README "Differentiable FBP and FDK").
+//
+//   filter:    q[k,iv,i] = post * tau * sum_j h[i-j] * pre * p[k,iv,j]
+//              (forward: pre = cosine weight SDD/|P_pix - a|, post = view
+//              weight w_k; transpose: pre = w_k, post = cosine weight)
+//   gather:    g(x) = sum_k s_k (SID_k / U_k(x))^2 I(q_k; u_k(x), v_k(x))
+//   transpose: scatter of s_k W_k g(x) onto the same bilinear stencil.
+//
+// B300 design.  Per view the detector coordinates of a voxel centre are ratios
+// of affine functions of the voxel index, u = Nu / E and v = Nv / E with E =
+// depth / SID.  For scans whose detector v axis is +-z and whose u axis is
+// horizontal (the circular and helical cone scans, and every 2-D scan), E and
+// Nu do not depend on z: a thread owns K voxels of one (x, y) column, and per
+// view it evaluates the affine forms exactly in 64-bit fixed point (2^-40) and
+// divides exactly (float estimate of the floor, integer remainder), so the
+// interpolation fractions are good to ~1e-7 pixel without float64 arithmetic,
+// which runs at a small fraction of the float32 rate on this part.  Along the
+// column v advances by the fixed step Nv_z / E, split into integer and
+// fractional parts.  Lanes of a warp are consecutive x, so the four stencil
+// loads of a warp touch neighbouring pixels of two detector rows.
+#pragma once
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+namespace ctp {
+
+constexpr double kFixOne = 1099511627776.0;  // 2^40
+constexpr float kFixInv = 9.094947017729282e-13f;  // 2^-40
+
+// Per-view constants, fixed point 2^-40 for the affine forms in voxel indices
+// (i, j, k) = (x, y, z).
+struct FdkView {
+    long long e[3];    // depth / SID = e0 + e1 i + e2 j (parallel: 1)
+    long long nu[3];   // u * depth / SID
+    long long nv[4];   // v * depth / SID, including the z term nv[3] k
+    float scale;       // SDD / (2 pi SID); parallel 1 / (2 pi)
+    float sdd;         // cosine weight SDD / |P_pix - a| (parallel: unused)
+    float g[6];        // |c-a|^2, (c-a).u, (c-a).v, u.v, |u|^2, |v|^2
+};
+
+struct FdkParams {
+    const FdkView *views;
+    int n_views, n_u, n_v;
+    int n[3];
+    int ndim, beam;
+    float pitch_u, pitch_v;
+    float cu, cv;      // pixel index of the detector centre: (n - 1)/2 - offset
+    int tx;            // warp tile width in x (32, 16, 8 or 4)
+};
+
+// Warp tile width: CTP_FDK_TX = 32, 16, 8 or 4 overrides the default 8.
+inline int fdk_tile_x()
+{
+    const char *env = getenv("CTP_FDK_TX");
+    if (env) {
+        const int t = atoi(env);
+        if (t == 32 || t == 16 || t == 8 || t == 4) return t;
+    }
+    return 8;
+}
+
+// A 64-bit integer as float from its two 32-bit halves (relative error below
+// 2^-23): 32-bit conversions, where a 64-bit conversion would run on the slow
+// float64 pipe.
+__device__ __forceinline__ float i64_to_float(long long x)
+{
+    return __fmaf_rn(__int2float_rn((int)(x >> 32)), 4294967296.0f,
+                     __uint2float_rn((unsigned)(x & 0xffffffffLL)));
+}
+
+// floor(num / den) and its fraction, exactly up to the final float rounding of
+// the fraction; den > 0, rden ~ 1 / den.  False when |num / den| >= 2^20 (far
+// off the detector).
+__device__ __forceinline__ bool fix_floor_div(long long num, long long den, float rden, int &q,
+                                              float &f)
+{
+    const float qf = floorf(i64_to_float(num) * rden);
+    if (!(fabsf(qf) < 1048576.0f)) return false;
+    q = (int)qf;
+    long long r = num - (long long)q * den;
+    // the float estimate is off by at most one
+    if (r < 0) {
+        r += den;
+        q -= 1;
+    } else if (r >= den) {
+        r -= den;
+        q += 1;
+    }
+    f = fminf(i64_to_float(r) * rden, 0.99999994f);
+    return true;
+}
+
+// Per (column, view) set-up shared by the gather and the scatter.  Returns false
+// when the view contributes nothing to this column.
+struct ColumnView {
+    int iu, iv, dvi;
+    float fu, fv, dvf, w;
+    bool c0, c1;
+};
+
+__device__ __forceinline__ bool fdk_column_view(const FdkParams &F, const FdkView &V, int i, int j,
+                                                int k0, ColumnView &C)
+{
+    const long long den = V.e[0] + V.e[1] * i + V.e[2] * j;
+    if (den < (1LL << 20)) return false;  // depth below 1e-6 SID: behind or at the source
+    const float denf = i64_to_float(den);
+    const float rden = __frcp_rn(denf);
+    if (!fix_floor_div(V.nu[0] + V.nu[1] * i + V.nu[2] * j, den, rden, C.iu, C.fu)) return false;
+    if (C.iu < -1 || C.iu >= F.n_u) return false;
+    const float ef = denf * kFixInv;
+    C.w = __fdividef(V.scale, ef * ef);
+    C.c0 = C.iu >= 0;
+    C.c1 = C.iu + 1 < F.n_u;
+    if (F.ndim == 2) {
+        C.iv = 0;
+        C.fv = 0.0f;
+        C.dvi = 0;
+        C.dvf = 0.0f;
+        return true;
+    }
+    if (!fix_floor_div(V.nv[0] + V.nv[1] * i + V.nv[2] * j + V.nv[3] * k0, den, rden, C.iv, C.fv))
+        return false;
+    return fix_floor_div(V.nv[3], den, rden, C.dvi, C.dvf);
+}
+
+// Column (i, j) of a thread.  A block covers 32 x 8 columns; a warp covers tx x
+// (32 / tx) of them (tx = 32, 16, 8 or 4), so that in every view the warp's
+// stencils stay close on the detector: along a ray parallel to x the 32 columns
+// of a 32 x 1 warp lie at 32 different depths and, away from the mid-plane,
+// on as many different detector rows.
+__device__ __forceinline__ void fdk_column_of(int tx, int &i, int &j)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int wx = 32 / tx;                  // warps across x
+    i = blockIdx.x * 32 + (warp % wx) * tx + lane % tx;
+    j = blockIdx.y * 8 + (warp / wx) * (32 / tx) + lane / tx;
+}
+
+// One thread per (x, y) column and K consecutive z; blocks of 32 x 8 columns.
+template <int K>
+__global__ void __launch_bounds__(256) wbp_gather_kernel(FdkParams F, const float *__restrict__ q,
+                                                         float *__restrict__ vol)
+{
+    int i, j;
+    fdk_column_of(F.tx, i, j);
+    const int k0 = blockIdx.z * K;
+    if (i >= F.n[0] || j >= F.n[1]) return;
+    float acc[K];
+#pragma unroll
+    for (int t = 0; t < K; ++t) acc[t] = 0.0f;
+    const long long plane = (long long)F.n_u * F.n_v;
+    for (int s = 0; s < F.n_views; ++s) {
+        ColumnView C;
+        if (!fdk_column_view(F, F.views[s], i, j, k0, C)) continue;
+        const float *base = q + s * plane;
+        if (F.ndim == 2) {
+            const float a0 = C.c0 ? __ldg(base + C.iu) : 0.0f;
+            const float a1 = C.c1 ? __ldg(base + C.iu + 1) : 0.0f;
+            acc[0] = __fmaf_rn(C.w, __fmaf_rn(C.fu, a1 - a0, a0), acc[0]);
+            continue;
+        }
+        int iv = C.iv;
+        float fv = C.fv;
+        // rows of step t lie in [iv + t dvi, iv + t (dvi + 1)]
+        const bool inside = C.c0 && C.c1 && iv + (K - 1) * min(C.dvi, 0) >= 0 &&
+                            iv + (K - 1) * max(C.dvi + 1, 0) + 1 < F.n_v;
+        if (inside) {
+            const float *col = base + C.iu;
+#pragma unroll
+            for (int t = 0; t < K; ++t) {
+                const float *row = col + (long long)iv * F.n_u;
+                const float a0 = __ldg(row), a1 = __ldg(row + 1);
+                const float b0 = __ldg(row + F.n_u), b1 = __ldg(row + F.n_u + 1);
+                const float a = __fmaf_rn(C.fu, a1 - a0, a0);
+                const float b = __fmaf_rn(C.fu, b1 - b0, b0);
+                acc[t] = __fmaf_rn(C.w, __fmaf_rn(fv, b - a, a), acc[t]);
+                fv += C.dvf;
+                iv += C.dvi;
+                if (fv >= 1.0f) {
+                    fv -= 1.0f;
+                    iv += 1;
+                }
+            }
+            continue;
+        }
+#pragma unroll
+        for (int t = 0; t < K; ++t) {
+            const bool r0 = (unsigned)iv < (unsigned)F.n_v;
+            const bool r1 = (unsigned)(iv + 1) < (unsigned)F.n_v;
+            if (r0 || r1) {
+                const float *row = base + (long long)iv * F.n_u + C.iu;
+                const float a0 = (r0 && C.c0) ? __ldg(row) : 0.0f;
+                const float a1 = (r0 && C.c1) ? __ldg(row + 1) : 0.0f;
+                const float b0 = (r1 && C.c0) ? __ldg(row + F.n_u) : 0.0f;
+                const float b1 = (r1 && C.c1) ? __ldg(row + F.n_u + 1) : 0.0f;
+                const float a = __fmaf_rn(C.fu, a1 - a0, a0);
+                const float b = __fmaf_rn(C.fu, b1 - b0, b0);
+                acc[t] = __fmaf_rn(C.w, __fmaf_rn(fv, b - a, a), acc[t]);
+            }
+            fv += C.dvf;
+            iv += C.dvi;
+            if (fv >= 1.0f) {
+                fv -= 1.0f;
+                iv += 1;
+            }
+        }
+    }
+    const int kn = F.ndim == 2 ? 1 : K;
+#pragma unroll
+    for (int t = 0; t < K; ++t)
+        if (t < kn && k0 + t < F.n[2])
+            vol[((long long)(k0 + t) * F.n[1] + j) * F.n[0] + i] = acc[t];
+}
+
+// Transpose: the same stencil, each voxel's s_k W_k g scattered with float atomics
+// into a zeroed sinogram.
+template <int K>
+__global__ void __launch_bounds__(256) wbp_scatter_kernel(FdkParams F,
+                                                          const float *__restrict__ vol,
+                                                          float *__restrict__ q)
+{
+    int i, j;
+    fdk_column_of(F.tx, i, j);
+    const int k0 = blockIdx.z * K;
+    if (i >= F.n[0] || j >= F.n[1]) return;
+    const int kn = F.ndim == 2 ? 1 : K;
+    float g[K];
+#pragma unroll
+    for (int t = 0; t < K; ++t)
+        g[t] = (t < kn && k0 + t < F.n[2])
+                   ? vol[((long long)(k0 + t) * F.n[1] + j) * F.n[0] + i] : 0.0f;
+    const long long plane = (long long)F.n_u * F.n_v;
+    for (int s = 0; s < F.n_views; ++s) {
+        ColumnView C;
+        if (!fdk_column_view(F, F.views[s], i, j, k0, C)) continue;
+        float *base = q + s * plane;
+        if (F.ndim == 2) {
+            const float val = C.w * g[0];
+            if (val != 0.0f) {
+                if (C.c0) atomicAdd(base + C.iu, val * (1.0f - C.fu));
+                if (C.c1) atomicAdd(base + C.iu + 1, val * C.fu);
+            }
+            continue;
+        }
+        int iv = C.iv;
+        float fv = C.fv;
+#pragma unroll
+        for (int t = 0; t < K; ++t) {
+            const bool r0 = (unsigned)iv < (unsigned)F.n_v;
+            const bool r1 = (unsigned)(iv + 1) < (unsigned)F.n_v;
+            const float val = C.w * g[t];
+            if ((r0 || r1) && val != 0.0f) {
+                float *row = base + (long long)iv * F.n_u + C.iu;
+                const float va = val * (1.0f - fv), vb = val * fv;
+                if (r0 && C.c0) atomicAdd(row, va * (1.0f - C.fu));
+                if (r0 && C.c1) atomicAdd(row + 1, va * C.fu);
+                if (r1 && C.c0) atomicAdd(row + F.n_u, vb * (1.0f - C.fu));
+                if (r1 && C.c1) atomicAdd(row + F.n_u + 1, vb * C.fu);
+            }
+            fv += C.dvf;
+            iv += C.dvi;
+            if (fv >= 1.0f) {
+                fv -= 1.0f;
+                iv += 1;
+            }
+        }
+    }
+}
+
+// Cosine of pixel (iu, iv)'s ray to the detector normal: SDD / |P_pix - a|.
+__device__ __forceinline__ float fdk_cosine(const FdkParams &F, const FdkView &V, int iu, int iv)
+{
+    if (F.beam != 1) return 1.0f;
+    const float al = ((float)iu - F.cu) * F.pitch_u;
+    const float be = F.ndim == 2 ? 0.0f : ((float)iv - F.cv) * F.pitch_v;
+    const float d2 = V.g[0] + 2.0f * al * V.g[1] + 2.0f * be * V.g[2] + 2.0f * al * be * V.g[3] +
+                     al * al * V.g[4] + be * be * V.g[5];
+    return __fdiv_rn(V.sdd, __fsqrt_rn(d2));
+}
+
+// Ramp filter along u: RB detector rows per block staged in shared memory with
+// the kernel h; each thread forms 4 outputs (stride blockDim) of every row, so
+// per input sample it issues RB + 4 shared loads (the row values are warp
+// broadcasts, the kernel values consecutive) for 4 RB fused multiply-adds.
+template <int RB>
+__global__ void ramp_filter_kernel(FdkParams F, const float *__restrict__ h,
+                                   const float *__restrict__ x, float *__restrict__ out,
+                                   const float *__restrict__ view_weight, int transpose,
+                                   long long n_rows)
+{
+    extern __shared__ float sm[];
+    const int nu = F.n_u;
+    float *xs = sm;
+    float *hs = sm + RB * nu;
+    const long long row0 = (long long)blockIdx.x * RB;
+    for (int t = threadIdx.x; t < 2 * nu - 1; t += blockDim.x) hs[t] = h[t];
+    for (int t = threadIdx.x; t < RB * nu; t += blockDim.x) {
+        const int r = t / nu, jj = t - r * nu;
+        const long long row = row0 + r;
+        float val = 0.0f;
+        if (row < n_rows) {
+            const int view = (int)(row / F.n_v), iv = (int)(row - (long long)view * F.n_v);
+            const float pre = transpose ? (view_weight ? view_weight[view] : 1.0f)
+                                        : fdk_cosine(F, F.views[view], jj, iv);
+            val = x[row * nu + jj] * pre;
+        }
+        xs[t] = val;
+    }
+    __syncthreads();
+    const int T = blockDim.x;
+    for (int i0 = threadIdx.x; i0 < nu; i0 += 4 * T) {
+        float acc[RB][4];
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) acc[r][m] = 0.0f;
+        int hoff[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) hoff[m] = min(i0 + m * T, nu - 1) + nu - 1;
+        for (int jj = 0; jj < nu; ++jj) {
+            float hv[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) hv[m] = hs[hoff[m] - jj];
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                const float xv = xs[r * nu + jj];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) acc[r][m] = __fmaf_rn(hv[m], xv, acc[r][m]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            const long long row = row0 + r;
+            if (row >= n_rows) continue;
+            const int view = (int)(row / F.n_v), iv = (int)(row - (long long)view * F.n_v);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int i = i0 + m * T;
+                if (i >= nu) continue;
+                const float post = transpose ? fdk_cosine(F, F.views[view], i, iv)
+                                             : (view_weight ? view_weight[view] : 1.0f);
+                out[row * nu + i] = __fmul_rn(__fmul_rn(acc[r][m], F.pitch_u), post);
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------- host side
+// Plan-time tables.  Returns 0, or 13 when the geometry is outside the class
+// these kernels handle (3-D: a view's depth or u coordinate depends on z, i.e.
+// the detector v axis is not +-z or its u axis not horizontal; a source not in
+// front of the isocentre; affine forms beyond the fixed-point range).
+inline int fdk_build(int ndim, int beam, int n_views, int n_u, int n_v, const float *src,
+                     const float *det_centre, const float *det_u, const float *det_v,
+                     double pitch_u, double pitch_v, double offset_u, double offset_v,
+                     const int n[3], const double d[3], const double o[3],
+                     std::vector<FdkView> &out, FdkParams &P)
+{
+    const double kPi = 3.14159265358979323846;
+    out.assign(n_views > 0 ? n_views : 1, FdkView{});
+    P.n_views = n_views;
+    P.n_u = n_u;
+    P.n_v = n_v;
+    for (int a = 0; a < 3; ++a) P.n[a] = n[a];
+    P.ndim = ndim;
+    P.beam = beam;
+    P.pitch_u = (float)pitch_u;
+    P.pitch_v = (float)pitch_v;
+    const double cu = 0.5 * (n_u - 1) - offset_u, cv = 0.5 * (n_v - 1) - offset_v;
+    P.cu = (float)cu;
+    P.cv = (float)cv;
+    P.tx = fdk_tile_x();
+    const double iso[3] = {o[0] + 0.5 * n[0] * d[0], o[1] + 0.5 * n[1] * d[1],
+                           o[2] + 0.5 * n[2] * d[2]};
+    const double x0[3] = {o[0] + 0.5 * d[0], o[1] + 0.5 * d[1], o[2] + 0.5 * d[2]};
+    auto dot = [](const double *p, const double *q) { return p[0] * q[0] + p[1] * q[1] + p[2] * q[2]; };
+    auto cross = [](const double *p, const double *q, double *r) {
+        r[0] = p[1] * q[2] - p[2] * q[1];
+        r[1] = p[2] * q[0] - p[0] * q[2];
+        r[2] = p[0] * q[1] - p[1] * q[0];
+    };
+    // fixed point with a range check: |value| * (largest index + 1) < 2^61
+    bool ok = true;
+    auto fix = [&](double value, int extent) -> long long {
+        const double f = value * kFixOne;
+        if (!std::isfinite(f) || std::fabs(f) * (double)(extent + 1) >= 2305843009213693952.0) {
+            ok = false;
+            return 0;
+        }
+        return (long long)std::llrint(f);
+    };
+    for (int s = 0; s < n_views; ++s) {
+        double A[3], C[3], U[3], V[3], N[3], US[3], VS[3], cr[3];
+        for (int q = 0; q < 3; ++q) {
+            A[q] = src[3 * s + q];
+            C[q] = det_centre[3 * s + q];
+            U[q] = det_u[3 * s + q];
+            V[q] = det_v[3 * s + q];
+        }
+        cross(U, V, N);
+        const double nn = std::sqrt(dot(N, N));
+        for (double &t : N) t /= nn;
+        double side;
+        if (beam == 1) {
+            const double ca[3] = {C[0] - A[0], C[1] - A[1], C[2] - A[2]};
+            side = dot(ca, N);
+        } else {
+            side = dot(A, N);
+        }
+        if (!(side != 0.0)) return 13;
+        if (side < 0)
+            for (double &t : N) t = -t;
+        cross(U, V, cr);
+        const double triple = dot(cr, N);
+        cross(V, N, US);
+        cross(N, U, VS);
+        for (int q = 0; q < 3; ++q) {
+            US[q] /= triple;
+            VS[q] /= triple;
+        }
+        FdkView &F = out[s];
+        // depth / SID, u and v numerators as affine forms of the voxel centre
+        double e0, ex[3], u0, ux[3], v0, vx[3], scale;
+        if (beam == 1) {
+            const double ca[3] = {C[0] - A[0], C[1] - A[1], C[2] - A[2]};
+            const double ia[3] = {iso[0] - A[0], iso[1] - A[1], iso[2] - A[2]};
+            const double xa[3] = {x0[0] - A[0], x0[1] - A[1], x0[2] - A[2]};
+            const double sdd = dot(ca, N), sid = dot(ia, N);
+            if (!(sdd > 0.0) || !(sid > 0.0)) return 13;
+            e0 = dot(xa, N) / sid;
+            for (int q = 0; q < 3; ++q) ex[q] = d[q] * N[q] / sid;
+            const double au = cu - dot(ca, US) / pitch_u, bu = sdd / (pitch_u * sid);
+            const double av = cv - dot(ca, VS) / pitch_v, bv = sdd / (pitch_v * sid);
+            u0 = au * e0 + bu * dot(xa, US);
+            v0 = av * e0 + bv * dot(xa, VS);
+            for (int q = 0; q < 3; ++q) {
+                ux[q] = au * ex[q] + bu * d[q] * US[q];
+                vx[q] = av * ex[q] + bv * d[q] * VS[q];
+            }
+            scale = sdd / (2.0 * kPi * sid);
+            F.sdd = (float)sdd;
+            F.g[0] = (float)dot(ca, ca);
+            F.g[1] = (float)dot(ca, U);
+            F.g[2] = (float)dot(ca, V);
+        } else {
+            const double an = std::sqrt(dot(A, A));
+            const double R[3] = {A[0] / an, A[1] / an, A[2] / an};
+            const double rn = dot(R, N);
+            double WU[3], WV[3];
+            for (int q = 0; q < 3; ++q) {
+                WU[q] = US[q] - N[q] * dot(R, US) / rn;
+                WV[q] = VS[q] - N[q] * dot(R, VS) / rn;
+            }
+            const double xc[3] = {x0[0] - C[0], x0[1] - C[1], x0[2] - C[2]};
+            e0 = 1.0;
+            ex[0] = ex[1] = ex[2] = 0.0;
+            u0 = cu + dot(xc, WU) / pitch_u;
+            v0 = cv + dot(xc, WV) / pitch_v;
+            for (int q = 0; q < 3; ++q) {
+                ux[q] = d[q] * WU[q] / pitch_u;
+                vx[q] = d[q] * WV[q] / pitch_v;
+            }
+            scale = 1.0 / (2.0 * kPi);
+            F.sdd = 1.0f;
+            F.g[0] = F.g[1] = F.g[2] = 0.0f;
+        }
+        F.g[3] = (float)dot(U, V);
+        F.g[4] = (float)dot(U, U);
+        F.g[5] = (float)dot(V, V);
+        F.scale = (float)scale;
+        if (ndim == 3) {
+            // the column walk needs depth and u independent of z
+            const double tol = 1e-12 * (std::fabs(e0) + std::fabs(u0) + 1.0);
+            if (std::fabs(ex[2]) > tol || std::fabs(ux[2]) > tol) return 13;
+        } else {
+            // 2-D: one slice at k = 0; v is not used
+            v0 = 0.0;
+            vx[0] = vx[1] = vx[2] = 0.0;
+        }
+        F.e[0] = fix(e0, 0);
+        F.e[1] = fix(ex[0], n[0]);
+        F.e[2] = fix(ex[1], n[1]);
+        F.nu[0] = fix(u0, 0);
+        F.nu[1] = fix(ux[0], n[0]);
+        F.nu[2] = fix(ux[1], n[1]);
+        F.nv[0] = fix(v0, 0);
+        F.nv[1] = fix(vx[0], n[0]);
+        F.nv[2] = fix(vx[1], n[1]);
+        F.nv[3] = fix(vx[2], n[2]);
+        // the sum of the terms must stay in range as well
+        const double umax = std::fabs(u0) + std::fabs(ux[0]) * n[0] + std::fabs(ux[1]) * n[1];
+        const double vmax = std::fabs(v0) + std::fabs(vx[0]) * n[0] + std::fabs(vx[1]) * n[1] +
+                            std::fabs(vx[2]) * n[2];
+        const double emax = std::fabs(e0) + std::fabs(ex[0]) * n[0] + std::fabs(ex[1]) * n[1];
+        fix(umax, 1);
+        fix(vmax, 1);
+        fix(emax, 1);
+        if (!ok) return 13;
+    }
+    return 0;
+}
+
+// Ramp kernels h[m], m = -(n-1) .. n-1, with frequency response |omega|
+// (radians per unit length; Ram-Lak) or (2/tau)|sin(omega tau / 2)| (Shepp-Logan).
+inline void fdk_ramp_kernel(int n, double tau, int kind, std::vector<float> &h)
+{
+    const double kPi = 3.14159265358979323846;
+    h.assign(2 * n - 1, 0.0f);
+    for (int t = 0; t < 2 * n - 1; ++t) {
+        const long long m = t - (n - 1);
+        double v;
+        if (kind == 0) {
+            if (m == 0) v = kPi / (2.0 * tau * tau);
+            else if (m % 2 != 0) v = -2.0 / (kPi * (double)m * (double)m * tau * tau);
+            else v = 0.0;
+        } else {
+            v = -4.0 / (kPi * tau * tau * (4.0 * (double)m * (double)m - 1.0));
+        }
+        h[t] = (float)v;
+    }
+}
+
+inline dim3 fdk_grid(const FdkParams &F, int K)
+{
+    const int kz = F.ndim == 2 ? 1 : (F.n[2] + K - 1) / K;
+    return dim3((F.n[0] + 31) / 32, (F.n[1] + 7) / 8, kz);
+}
+
+constexpr int kFdkK = 16;  // z voxels per thread of the scatter
+
+// z voxels per thread of the gather: the per-(column, view) set-up is shared by
+// K voxels, at the cost of registers.  CTP_FDK_K = 8, 16 or 32 overrides the
+// default 16.
+inline int fdk_gather_k()
+{
+    const char *env = getenv("CTP_FDK_K");
+    if (env) {
+        const int k = atoi(env);
+        if (k == 8 || k == 16 || k == 32) return k;
+    }
+    return 16;
+}
+
+inline int fdk_gather(const FdkParams &F, const float *q, float *vol, cudaStream_t s)
+{
+    if (F.ndim == 2) {
+        wbp_gather_kernel<1><<<fdk_grid(F, 1), 256, 0, s>>>(F, q, vol);
+    } else {
+        const int K = fdk_gather_k();
+        if (K == 8) wbp_gather_kernel<8><<<fdk_grid(F, 8), 256, 0, s>>>(F, q, vol);
+        else if (K == 16) wbp_gather_kernel<16><<<fdk_grid(F, 16), 256, 0, s>>>(F, q, vol);
+        else wbp_gather_kernel<32><<<fdk_grid(F, 32), 256, 0, s>>>(F, q, vol);
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+inline int fdk_scatter(const FdkParams &F, const float *vol, float *q, cudaStream_t s)
+{
+    const size_t bytes = sizeof(float) * (size_t)F.n_views * F.n_u * F.n_v;
+    if (cudaMemsetAsync(q, 0, bytes, s) != cudaSuccess) return 9;
+    if (F.n_views == 0) return 0;
+    if (F.ndim == 2) wbp_scatter_kernel<1><<<fdk_grid(F, 1), 256, 0, s>>>(F, vol, q);
+    else wbp_scatter_kernel<kFdkK><<<fdk_grid(F, kFdkK), 256, 0, s>>>(F, vol, q);
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+// Largest detector row this filter takes (shared memory: one row and the kernel).
+constexpr int kFilterMaxU = 16384;
+
+template <int RB>
+inline int ramp_launch(const FdkParams &F, const float *h, const float *x, float *out,
+                       const float *view_weight, int transpose, cudaStream_t s)
+{
+    const long long rows = (long long)F.n_views * F.n_v;
+    const size_t smem = sizeof(float) * ((size_t)RB * F.n_u + 2 * (size_t)F.n_u);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(ramp_filter_kernel<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return 9;
+    int threads = (F.n_u + 3) / 4;
+    threads = ((threads + 31) / 32) * 32;
+    threads = threads < 32 ? 32 : (threads > 256 ? 256 : threads);
+    const long long blocks = (rows + RB - 1) / RB;
+    ramp_filter_kernel<RB><<<(unsigned)blocks, threads, smem, s>>>(F, h, x, out, view_weight,
+                                                                   transpose, rows);
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+inline int fdk_filter(const FdkParams &F, const float *h, const float *x, float *out,
+                      const float *view_weight, int transpose, cudaStream_t s)
+{
+    if ((long long)F.n_views * F.n_v == 0) return 0;
+    // rows per block: as many as fit 48 KB of shared memory, at most 8
+    const size_t per_row = sizeof(float) * (size_t)F.n_u;
+    const size_t hbytes = 2 * per_row;
+    if (hbytes + 8 * per_row <= 48 * 1024) return ramp_launch<8>(F, h, x, out, view_weight, transpose, s);
+    if (hbytes + 4 * per_row <= 48 * 1024) return ramp_launch<4>(F, h, x, out, view_weight, transpose, s);
+    if (hbytes + 2 * per_row <= 48 * 1024) return ramp_launch<2>(F, h, x, out, view_weight, transpose, s);
+    return ramp_launch<1>(F, h, x, out, view_weight, transpose, s);
+}
+
+}  // namespace ctp

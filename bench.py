@@ -372,6 +372,156 @@ def run_gpu(args, w, world, rank, local):
     return 0
 
 
+# ------------------------------------------------------ analytical FDK (second op)
+FDK_METRIC = "FDK voxel-view updates/s (ramp filter + weighted gather) on 1 B300"
+FDK_UNIT = "Gvox-view/s"
+# FP32 lanes x 2 flops x clock: 148 SMs x 128 lanes x 2 x 2.032 GHz (no tensor cores)
+FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+# algorithmic float32 flops of one voxel-view update: three linear interpolations
+# (a subtract and a multiply-add each: 3 flops) and the weighted accumulate (a
+# multiply-add: 2 flops)
+FDK_FLOPS_PER_UPDATE = 11
+
+
+def oracle_fdk_rate(w, p, budget_s):
+    """The float64 FDK oracle on a bounded sample: the first m views, filtered and
+    gathered over the central z slice.  Returns (Gvox-view/s, sample text, cores)."""
+    import oracle
+    from oracle import fdk as ofdk
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    scan = oracle.Scan.from_workload(w, ci.frames(w))
+    D, H, W = w.shape
+    kc = D // 2
+    vox = np.stack(np.meshgrid([kc], np.arange(H), np.arange(W), indexing="ij"), -1).reshape(-1, 3)
+    vw = np.full(w.n_views, np.pi / w.n_views)
+
+    def run(m):
+        sub = oracle.Scan(w.beam, *(a[:m] for a in scan.arrays), w.n_u, w.n_v, w.pitch_u,
+                          w.pitch_v, w.shape, w.spacing, w.origin, w.offset_u, w.offset_v, w.ndim)
+        t = time.perf_counter()
+        q = ofdk.filter_sinogram(sub, p[:m], vw[:m])
+        ofdk.weighted_backproject(sub, q, voxels=vox)
+        return time.perf_counter() - t
+
+    probe = run(1)
+    m = int(max(1, min(w.n_views, budget_s // max(probe, 1e-3))))
+    dt = run(m)
+    sample = (f"views 0..{m - 1} of {w.n_views}: ramp filter of those views and weighted gather "
+              f"over the central z slice ({H * W} voxels), float64 numpy oracle, {dt:.1f} s")
+    return H * W * m / dt / 1e9, sample, cores
+
+
+def run_fdk(args, w, world, rank, local):
+    """Time K FDK reconstructions (ramp filter + weighted gather) of the workload."""
+    import torch
+    import back_projection_ctp_b300 as ctp
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    frames = ci.frames(w)
+    p_h = ci.sinogram_noise(w).reshape(w.n_views, w.n_v, w.n_u)
+    plan = ctp.ctp_plan(geometry_of(w, frames), volume_of(w), args.path)
+    stream = torch.cuda.current_stream(dev)
+    d_p = torch.from_numpy(p_h).to(dev)
+    d_q = torch.empty_like(d_p)
+    d_vol = torch.empty(plan.vol_shape, dtype=torch.float32, device=dev)
+    d_vw = torch.from_numpy(ctp.full_scan_view_weights(w.n_views)).to(dev)
+    for _ in range(args.warmup):
+        ctp.ctp_fdk(plan, d_p, d_q, d_vol, d_vw, "ramlak", stream)
+    torch.cuda.synchronize(dev)
+
+    def capture(body):
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side), torch.cuda.graph(graph, stream=side):
+            cur = torch.cuda.current_stream(dev)
+            for _ in range(args.steps):
+                body(cur)
+        torch.cuda.synchronize(dev)
+        return graph
+
+    g_steps = capture(lambda st: ctp.ctp_fdk(plan, d_p, d_q, d_vol, d_vw, "ramlak", st))
+    g_filter = capture(lambda st: ctp.ctp_ramp_filter(plan, d_p, d_q, d_vw, "ramlak", False, st))
+    g_gather = capture(lambda st: ctp.ctp_weighted_backproject(plan, d_q, d_vol, st))
+    g_steps.replay()
+    torch.cuda.synchronize(dev)
+
+    def timed(graph):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    total_ms = timed(g_steps)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(total_ms, world)
+    filter_ms = timed(g_filter) / args.steps
+    gather_ms = timed(g_gather) / args.steps
+    ms_per_step = total_ms / args.steps
+    updates = w.n_voxels * w.n_views
+    value = world * updates / (ms_per_step * 1e-3) / 1e9
+
+    # end to end: pinned sinogram up, FDK, volume down, every step
+    p_pin = torch.from_numpy(p_h).pin_memory()
+    v_pin = torch.empty(plan.vol_shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 3))
+    for it in range(e2e_steps + 1):
+        if it == 1:
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+        d_p.copy_(p_pin, non_blocking=True)
+        ctp.ctp_fdk(plan, d_p, d_q, d_vol, d_vw, "ramlak", stream)
+        v_pin.copy_(d_vol, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+    e2e_value = world * updates / e2e_s / 1e9
+
+    achieved = FDK_FLOPS_PER_UPDATE * updates / (gather_ms * 1e-3) / 1e12
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            rate, sample, cores = oracle_fdk_rate(w, p_h, args.ref_budget)
+            cpu = {"value": rate, "unit": FDK_UNIT, "cores": cores, "kind": "oracle",
+                   "sample": sample}
+        line = {
+            "metric": FDK_METRIC, "value": value, "unit": FDK_UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "op": "fdk", "shape_DHW": list(w.shape),
+                       "views": w.n_views, "detector_vu": [w.n_v, w.n_u], "ramp": "ramlak",
+                       "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (no flush)" if 4 * w.n_rays > 126e6
+                       else "inputs smaller than L2 (no flush)",
+                       "filter_ms": filter_ms, "gather_ms": gather_ms},
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS,
+                         "unit": "TFLOP/s", "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,
+                         "kernel": "wbp_gather_kernel", "call": "gather",
+                         "note": f"{FDK_FLOPS_PER_UPDATE} float32 flops per voxel-view update "
+                                 "over the gather's event time; peak = 148 SMs x 128 lanes x 2 "
+                                 "x 2.032 GHz (derived from unit counts and clock)"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": FDK_UNIT, "h2d_bytes_per_step": 4 * w.n_rays,
+                    "d2h_bytes_per_step": 4 * w.n_voxels, "ms_per_step": e2e_s * 1e3},
+            "gpu_launches": 2 * args.steps,
+            "timing": "one CUDA graph of K steps replayed between CUDA events on the calls' stream",
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    plan.destroy()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -385,6 +535,9 @@ def main(argv=None):
     ap.add_argument("--path", default="auto", choices=["auto", "ray", "column"])
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="siddon", choices=["siddon", "fdk"],
+                    help="siddon: the projector pair (default); fdk: the analytical "
+                         "filtered backprojection on the same workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -396,6 +549,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             return run_reference(args, w, world, rank)
+        if args.op == "fdk":
+            return run_fdk(args, w, world, rank, local)
         return run_gpu(args, w, world, rank, local)
     finally:
         if world > 1:

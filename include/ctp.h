@@ -60,7 +60,8 @@ typedef enum ctp_status {
     CTP_E_CUDA = 9,        /* a CUDA runtime call failed */
     CTP_E_DEVICE = 10,     /* called with a different current device than the plan's */
     CTP_E_OPTION = 11,     /* unknown beam / ndim / path value */
-    CTP_E_LIMIT = 12       /* request beyond a fixed size limit of this entry point */
+    CTP_E_LIMIT = 12,      /* request beyond a fixed size limit of this entry point */
+    CTP_E_GEOMETRY = 13    /* scan outside the analytical operators' class (see ctp_fdk) */
 } ctp_status;
 
 typedef enum ctp_beam { CTP_PARALLEL = 0, CTP_DIVERGENT = 1 } ctp_beam;
@@ -194,6 +195,62 @@ int ctp_backward_host(ctp_plan_t *plan, const float *sino_host, float *vol_host,
  */
 int ctp_forward_static(const ctp_geometry *geom, const ctp_volume *vol, const float *vol_dev,
                        float *sino_dev, void *stream);
+
+/*
+ * Analytical FBP / FDK operators on the plan's geometry (diffct release diff
+ * 2.1.0 -> 2.2.1, README "Analytical helpers" and "Differentiable FBP and FDK";
+ * diffct/analytical.py: voxel-driven weighted gathers with the analytical
+ * constant 1/(2 pi) or SDD/(2 pi SID), and their dedicated transposes; the
+ * per-view SDD/(2 pi SID) of release diff 2.4.3 -> 2.4.4).  The pages give the
+ * structure and the constants; the rest is the textbook flat-detector FBP:
+ *
+ *   isocentre  the volume centre; n_s the unit detector normal pointing away
+ *              from the source (parallel: along the rays); SDD_s = (c_s - a_s).n_s,
+ *              SID_s = (iso - a_s).n_s, a_s = src[s], c_s = det_centre[s].
+ *   ramp       q[s,iv,i] = post * pitch_u * sum_j h[i-j] * pre * p[s,iv,j] along u,
+ *              h the Ram-Lak kernel (frequency response |omega|, radians per unit
+ *              length) or Shepp-Logan ((2/tau)|sin(omega tau/2)|), tau = pitch_u.
+ *              Forward: pre = SDD_s / |pixel - a_s| (cosine weight; parallel 1),
+ *              post = view_weight[s].  Transpose: pre and post swapped.
+ *   gather     g(x) = sum_s k_s (SID_s / U_s(x))^2 I(q_s; u_s(x), v_s(x)): x the
+ *              voxel centre, (u_s, v_s) the pixel coordinates where the ray from
+ *              the source through x (parallel: along the rays) meets the detector
+ *              plane (the inverse of the pixel-centre convention above), U_s(x) =
+ *              (x - a_s).n_s the depth, I bilinear interpolation with zeros
+ *              outside the detector (2-D: linear along u), k_s = SDD_s/(2 pi SID_s)
+ *              (parallel: 1/(2 pi), weight 1).  Voxels at or behind a source get
+ *              nothing from that view.
+ *   transpose  the exact transpose of the gather (same stencil, float atomics).
+ *
+ * With view weights pi / n_views (a full 2 pi scan: half the angular step),
+ * ctp_fdk reconstructs the image whose line integrals are the sinogram.
+ *
+ * Supported scans: every 2-D scan, and 3-D scans whose every view has the
+ * detector v axis along +-z and the u axis horizontal (circular and helical cone
+ * or parallel beams), with each divergent view's isocentre in front of its source;
+ * others return CTP_E_GEOMETRY from these calls (the plan itself is still valid for
+ * the projector pair).  ctp_ramp_filter needs n_u <= 16384 (else CTP_E_LIMIT).
+ *
+ * Buffers: device float32, layouts as above; view_weight_dev: device float32
+ * (n_views), or NULL for all ones.  ramp: CTP_RAMLAK or CTP_SHEPP_LOGAN.
+ * transpose: 0 or 1.  ctp_ramp_filter may run in place (out_dev == sino_dev).
+ * ctp_weighted_backproject overwrites vol_dev; ctp_weighted_backproject_transpose
+ * overwrites sino_dev (zeroed, then accumulated with float atomics).  ctp_fdk =
+ * ramp filter of sino_dev into work_dev (n_views, n_v, n_u floats; may equal
+ * sino_dev, which is then overwritten) followed by the gather into vol_dev.
+ * Errors: CTP_E_NULL, CTP_E_DEVICE, CTP_E_OPTION (unknown ramp), CTP_E_GEOMETRY,
+ * CTP_E_LIMIT, CTP_E_CUDA.  All are asynchronous on `stream`.
+ */
+typedef enum ctp_ramp { CTP_RAMLAK = 0, CTP_SHEPP_LOGAN = 1 } ctp_ramp;
+
+int ctp_ramp_filter(const ctp_plan_t *plan, const float *sino_dev, float *out_dev,
+                    const float *view_weight_dev, int ramp, int transpose, void *stream);
+int ctp_weighted_backproject(const ctp_plan_t *plan, const float *sino_dev, float *vol_dev,
+                             void *stream);
+int ctp_weighted_backproject_transpose(const ctp_plan_t *plan, const float *vol_dev,
+                                       float *sino_dev, void *stream);
+int ctp_fdk(const ctp_plan_t *plan, const float *sino_dev, float *work_dev, float *vol_dev,
+            const float *view_weight_dev, int ramp, void *stream);
 
 /* Static English text of a status code. */
 const char *ctp_status_string(int status);

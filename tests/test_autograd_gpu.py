@@ -69,3 +69,32 @@ def test_double_precision_inputs_keep_their_dtype_for_gradients(proj):
     x = torch.randn(proj.vol_shape, device="cuda", dtype=torch.float64, requires_grad=True)
     proj.project(x).sum().backward()
     assert x.grad.dtype == torch.float64
+
+
+def test_fdk_gradient_is_the_transposed_pipeline(proj, oracle_mod):
+    """d<FDK(y), h>/dy = F^T B^T h, checked against the float64 oracle's transposes."""
+    import torch
+    from oracle import fdk as ofdk
+    import back_projection_ctp_b300 as ctp
+    w = ci.small_cases()[3]
+    scan = oracle_mod.Scan.from_workload(w, ci.frames(w))
+    vw_h = ctp.full_scan_view_weights(w.n_views)
+    vw = torch.from_numpy(vw_h).cuda()
+    y = torch.randn(proj.sino_shape, device="cuda", requires_grad=True)
+    h = torch.randn(proj.vol_shape, device="cuda")
+    out = proj.fdk(y, vw)
+    ref_fwd = ofdk.fdk(scan, y.detach().cpu().numpy(), vw_h)
+    assert rel_l2(out.detach().cpu().numpy(), ref_fwd) <= 1e-5
+    (out * h).sum().backward()
+    hh = h.cpu().numpy().astype(np.float64)
+    ref = ofdk.filter_sinogram_transpose(scan, ofdk.weighted_backproject_transpose(scan, hh), vw_h)
+    assert rel_l2(y.grad.cpu().numpy(), ref) <= 1e-4
+
+
+def test_fdk_batch_dims(proj):
+    import torch
+    y = torch.randn((2,) + proj.sino_shape, device="cuda")
+    out = proj.fdk(y)
+    assert out.shape == (2,) + proj.vol_shape
+    one = proj.fdk(y[1])
+    assert rel_l2(out[1].cpu().numpy(), one.cpu().numpy()) == 0.0
