@@ -31,6 +31,7 @@
 // loads of a warp touch neighbouring pixels of two detector rows.
 #pragma once
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -136,7 +137,14 @@ __device__ __forceinline__ bool fdk_column_view(const FdkParams &F, const FdkVie
     }
     if (!fix_floor_div(V.nv[0] + V.nv[1] * i + V.nv[2] * j + V.nv[3] * k0, den, rden, C.iv, C.fv))
         return false;
-    return fix_floor_div(V.nv[3], den, rden, C.dvi, C.dvf);
+    // the step per z voxel needs no exact division: its float rounding (2^-24
+    // relative) accumulates over at most K steps from the exact start
+    const float dv = i64_to_float(V.nv[3]) * rden;
+    if (!(fabsf(dv) < 1048576.0f)) return false;
+    const float dfl = floorf(dv);
+    C.dvi = (int)dfl;
+    C.dvf = fminf(dv - dfl, 0.99999994f);
+    return true;
 }
 
 // Column (i, j) of a thread.  A block covers 32 x 8 columns; a warp covers tx x
@@ -152,7 +160,73 @@ __device__ __forceinline__ void fdk_column_of(int tx, int &i, int &j)
     j = blockIdx.y * 8 + (warp / wx) * (32 / tx) + lane / tx;
 }
 
-// One thread per (x, y) column and K consecutive z; blocks of 32 x 8 columns.
+// The K updates of one column in one view, stencil values read straight from
+// the filtered sinogram.  Rows of step t lie in [iv + t dvi, iv + t (dvi + 1)];
+// when the stencils of all K steps are on the detector the loop runs without
+// tests.
+template <int K>
+__device__ __forceinline__ void gather_column(const FdkParams &F, const ColumnView &C,
+                                              const float *__restrict__ base, float (&acc)[K])
+{
+    int iv = C.iv;
+    float fv = C.fv;
+    const bool inside = C.c0 && C.c1 && iv + (K - 1) * min(C.dvi, 0) >= 0 &&
+                        iv + (K - 1) * max(C.dvi + 1, 0) + 1 < F.n_v;
+    if (inside) {
+        const float *col = base + C.iu;
+#pragma unroll
+        for (int t = 0; t < K; ++t) {
+            const float *row = col + (long long)iv * F.n_u;
+            const float a0 = __ldg(row), a1 = __ldg(row + 1);
+            const float b0 = __ldg(row + F.n_u), b1 = __ldg(row + F.n_u + 1);
+            const float a = __fmaf_rn(C.fu, a1 - a0, a0);
+            const float b = __fmaf_rn(C.fu, b1 - b0, b0);
+            acc[t] = __fmaf_rn(C.w, __fmaf_rn(fv, b - a, a), acc[t]);
+            fv += C.dvf;
+            iv += C.dvi;
+            if (fv >= 1.0f) {
+                fv -= 1.0f;
+                iv += 1;
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int t = 0; t < K; ++t) {
+        const bool r0 = (unsigned)iv < (unsigned)F.n_v;
+        const bool r1 = (unsigned)(iv + 1) < (unsigned)F.n_v;
+        if (r0 || r1) {
+            const float *row = base + (long long)iv * F.n_u + C.iu;
+            const float a0 = (r0 && C.c0) ? __ldg(row) : 0.0f;
+            const float a1 = (r0 && C.c1) ? __ldg(row + 1) : 0.0f;
+            const float b0 = (r1 && C.c0) ? __ldg(row + F.n_u) : 0.0f;
+            const float b1 = (r1 && C.c1) ? __ldg(row + F.n_u + 1) : 0.0f;
+            const float a = __fmaf_rn(C.fu, a1 - a0, a0);
+            const float b = __fmaf_rn(C.fu, b1 - b0, b0);
+            acc[t] = __fmaf_rn(C.w, __fmaf_rn(fv, b - a, a), acc[t]);
+        }
+        fv += C.dvf;
+        iv += C.dvi;
+        if (fv >= 1.0f) {
+            fv -= 1.0f;
+            iv += 1;
+        }
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void store_column(const FdkParams &F, int i, int j, int k0,
+                                             const float (&acc)[K], float *__restrict__ vol)
+{
+    const int kn = F.ndim == 2 ? 1 : K;
+#pragma unroll
+    for (int t = 0; t < K; ++t)
+        if (t < kn && k0 + t < F.n[2])
+            vol[((long long)(k0 + t) * F.n[1] + j) * F.n[0] + i] = acc[t];
+}
+
+// One thread per (x, y) column and K consecutive z; blocks of 32 x 8 columns;
+// stencil values straight from global memory (2-D scans, and a tuning override).
 template <int K>
 __global__ void __launch_bounds__(256) wbp_gather_kernel(FdkParams F, const float *__restrict__ q,
                                                          float *__restrict__ vol)
@@ -175,57 +249,9 @@ __global__ void __launch_bounds__(256) wbp_gather_kernel(FdkParams F, const floa
             acc[0] = __fmaf_rn(C.w, __fmaf_rn(C.fu, a1 - a0, a0), acc[0]);
             continue;
         }
-        int iv = C.iv;
-        float fv = C.fv;
-        // rows of step t lie in [iv + t dvi, iv + t (dvi + 1)]
-        const bool inside = C.c0 && C.c1 && iv + (K - 1) * min(C.dvi, 0) >= 0 &&
-                            iv + (K - 1) * max(C.dvi + 1, 0) + 1 < F.n_v;
-        if (inside) {
-            const float *col = base + C.iu;
-#pragma unroll
-            for (int t = 0; t < K; ++t) {
-                const float *row = col + (long long)iv * F.n_u;
-                const float a0 = __ldg(row), a1 = __ldg(row + 1);
-                const float b0 = __ldg(row + F.n_u), b1 = __ldg(row + F.n_u + 1);
-                const float a = __fmaf_rn(C.fu, a1 - a0, a0);
-                const float b = __fmaf_rn(C.fu, b1 - b0, b0);
-                acc[t] = __fmaf_rn(C.w, __fmaf_rn(fv, b - a, a), acc[t]);
-                fv += C.dvf;
-                iv += C.dvi;
-                if (fv >= 1.0f) {
-                    fv -= 1.0f;
-                    iv += 1;
-                }
-            }
-            continue;
-        }
-#pragma unroll
-        for (int t = 0; t < K; ++t) {
-            const bool r0 = (unsigned)iv < (unsigned)F.n_v;
-            const bool r1 = (unsigned)(iv + 1) < (unsigned)F.n_v;
-            if (r0 || r1) {
-                const float *row = base + (long long)iv * F.n_u + C.iu;
-                const float a0 = (r0 && C.c0) ? __ldg(row) : 0.0f;
-                const float a1 = (r0 && C.c1) ? __ldg(row + 1) : 0.0f;
-                const float b0 = (r1 && C.c0) ? __ldg(row + F.n_u) : 0.0f;
-                const float b1 = (r1 && C.c1) ? __ldg(row + F.n_u + 1) : 0.0f;
-                const float a = __fmaf_rn(C.fu, a1 - a0, a0);
-                const float b = __fmaf_rn(C.fu, b1 - b0, b0);
-                acc[t] = __fmaf_rn(C.w, __fmaf_rn(fv, b - a, a), acc[t]);
-            }
-            fv += C.dvf;
-            iv += C.dvi;
-            if (fv >= 1.0f) {
-                fv -= 1.0f;
-                iv += 1;
-            }
-        }
+        gather_column<K>(F, C, base, acc);
     }
-    const int kn = F.ndim == 2 ? 1 : K;
-#pragma unroll
-    for (int t = 0; t < K; ++t)
-        if (t < kn && k0 + t < F.n[2])
-            vol[((long long)(k0 + t) * F.n[1] + j) * F.n[0] + i] = acc[t];
+    store_column<K>(F, i, j, k0, acc, vol);
 }
 
 // Transpose: the same stencil, each voxel's s_k W_k g scattered with float atomics
@@ -545,14 +571,14 @@ inline dim3 fdk_grid(const FdkParams &F, int K)
 constexpr int kFdkK = 16;  // z voxels per thread of the scatter
 
 // z voxels per thread of the gather: the per-(column, view) set-up is shared by
-// K voxels, at the cost of registers.  CTP_FDK_K = 8, 16 or 32 overrides the
-// default 16.
+// K voxels, at the cost of registers.  CTP_FDK_K = 8, 16, 32 or 64 overrides
+// the default 16.
 inline int fdk_gather_k()
 {
     const char *env = getenv("CTP_FDK_K");
     if (env) {
         const int k = atoi(env);
-        if (k == 8 || k == 16 || k == 32) return k;
+        if (k == 8 || k == 16 || k == 32 || k == 64) return k;
     }
     return 16;
 }
@@ -564,8 +590,9 @@ inline int fdk_gather(const FdkParams &F, const float *q, float *vol, cudaStream
     } else {
         const int K = fdk_gather_k();
         if (K == 8) wbp_gather_kernel<8><<<fdk_grid(F, 8), 256, 0, s>>>(F, q, vol);
-        else if (K == 16) wbp_gather_kernel<16><<<fdk_grid(F, 16), 256, 0, s>>>(F, q, vol);
-        else wbp_gather_kernel<32><<<fdk_grid(F, 32), 256, 0, s>>>(F, q, vol);
+        else if (K == 32) wbp_gather_kernel<32><<<fdk_grid(F, 32), 256, 0, s>>>(F, q, vol);
+        else if (K == 64) wbp_gather_kernel<64><<<fdk_grid(F, 64), 256, 0, s>>>(F, q, vol);
+        else wbp_gather_kernel<16><<<fdk_grid(F, 16), 256, 0, s>>>(F, q, vol);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
