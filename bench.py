@@ -444,6 +444,8 @@ def run_fdk(args, w, world, rank, local):
     g_steps = capture(lambda st: ctp.ctp_fdk(plan, d_p, d_q, d_vol, d_vw, "ramlak", st))
     g_filter = capture(lambda st: ctp.ctp_ramp_filter(plan, d_p, d_q, d_vw, "ramlak", False, st))
     g_gather = capture(lambda st: ctp.ctp_weighted_backproject(plan, d_q, d_vol, st))
+    d_t = torch.empty_like(d_p)
+    g_transpose = capture(lambda st: ctp.ctp_weighted_backproject_transpose(plan, d_vol, d_t, st))
     g_steps.replay()
     torch.cuda.synchronize(dev)
 
@@ -467,6 +469,7 @@ def run_fdk(args, w, world, rank, local):
     total_ms = max_over_ranks(total_ms, world)
     filter_ms = timed(g_filter) / args.steps
     gather_ms = timed(g_gather) / args.steps
+    transpose_ms = timed(g_transpose) / args.steps
     ms_per_step = total_ms / args.steps
     updates = w.n_voxels * w.n_views
     value = world * updates / (ms_per_step * 1e-3) / 1e9
@@ -503,7 +506,8 @@ def run_fdk(args, w, world, rank, local):
                        "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (no flush)" if 4 * w.n_rays > 126e6
                        else "inputs smaller than L2 (no flush)",
-                       "filter_ms": filter_ms, "gather_ms": gather_ms},
+                       "filter_ms": filter_ms, "gather_ms": gather_ms,
+                       "gather_transpose_ms": transpose_ms},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS,
                          "unit": "TFLOP/s", "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,
                          "kernel": "wbp_gather_kernel", "call": "gather",
