@@ -22,6 +22,9 @@ Functions and what pins them (the tests under ``tests/test_oracle_*.py``):
 * :func:`segment_count` -- pieces longer than 1e-5 of the smallest cell width
   (the benchmark's unit); pinned by :func:`brute_count`.
 * :func:`ambiguous` -- rays lying on a cell-face plane; pinned on hand-built rays.
+* :func:`geometry_vjp` -- first-order gradients of the path sums with respect to
+  the per-view frames; pinned by central finite differences of :func:`forward`
+  and by the invariance of chords under sliding a ray's end points along it.
 """
 
 from __future__ import annotations
@@ -87,6 +90,7 @@ def _load():
                 "ora_ambiguous": [C, D, P, I],
                 "ora_supersampled": [C, P, P, L, L, P, I],
                 "ora_trace_ray": [C, L, P, P],
+                "ora_geometry_vjp": [C, P, P, P, I],
             }
             for name, args in sigs.items():
                 fn = getattr(lib, name)
@@ -263,3 +267,16 @@ def trace_ray(scan: Scan, ray: int):
     if m < 0:
         raise MemoryError("ora_trace_ray failed")
     return cells[:m], lens[:m]
+
+
+def geometry_vjp(scan: Scan, vol, weights, threads=0):
+    """Float64 first-order geometry gradient: (n_views, 4, 3) array of
+    sum over the view's rays of weights[ray] * d p(ray) / d frame, frames in the
+    order src, det_centre, det_u, det_v (the sum of crossing terms written out in
+    ``siddon_oracle.c``)."""
+    vol = _f32(vol, scan.shape)
+    w = _f32(weights, (scan.n_rays,))
+    out = np.zeros((scan.n_views, 4, 3), dtype=np.float64)
+    _check(_load().ora_geometry_vjp(scan.ref(), vol.ctypes.data, w.ctypes.data,
+                                    out.ctypes.data, threads), "ora_geometry_vjp")
+    return out

@@ -617,3 +617,183 @@ int ora_trace_ray(const ora_ctx *c, long ray, long *cells, double *lens)
     free(buf);
     return n;
 }
+
+/*
+ * Geometry vector-Jacobian product: first-order gradients of the path sums
+ * with respect to each view's frame ("first-order source / centre / axis
+ * gradients", diffct 2.4.1 -> 2.4.2, docs/video/README.md, shot "Geometry";
+ * trajectory tensors that require gradients receive geometry gradients,
+ * diffct 2.1.0 -> 2.2.1, README "Arbitrary trajectories").
+ *
+ *     out[view * 12 + m] = sum over rays R of the view of w[R] * d p(R) / d theta_m,
+ *     theta = (src[3], det_centre[3], det_u[3], det_v[3]).
+ *
+ * For the line X0 + t r, t in [tlo, thi] (divergent: X0 = source, r = pixel -
+ * source, t in [0, 1]; parallel: X0 = pixel, r = src, t free), the path sum of
+ * the cell-constant image is p = |r| sum_j (t_{j+1} - t_j) f_j.  Its pieces end
+ * where the line crosses a plane x_a = const of the grid (or the ray's own end
+ * point, which does not move with the planes).  A crossing at t_k moves by
+ * dt_k = -(dX0_a + t_k dr_a) / r_a, so
+ *     dp/dX0_a = -|r| sum_{k on axis a} (f_before - f_after)_k / r_a,
+ *     dp/dr_a  = -|r| sum_{k on axis a} (f_before - f_after)_k t_k / r_a + p r_a / |r|^2,
+ * with the value outside the volume 0 at the box faces.  The chain rule to the
+ * frame: pixel = centre + alpha u + beta v (alpha, beta the pixel offsets times
+ * the pitches); divergent: source = X0, pixel = X0 + r; parallel: pixel = X0,
+ * src = r.  Configurations where two crossings coincide (a ray through a cell
+ * edge or corner) are kinks of p and have no gradient; whatever the merge
+ * order gives there is accepted.  Views run in parallel (each view's sums are
+ * owned by one thread).
+ */
+int ora_geometry_vjp(const ora_ctx *c, const float *vol, const float *w, double *out,
+                     int nthreads)
+{
+    int T = ora_threads(nthreads);
+    int B = ora_buf_len(c);
+    long per_view = (long)c->n_u * c->n_v;
+    int err = 0;
+#pragma omp parallel num_threads(T)
+    {
+        double *buf = (double *)malloc(sizeof(double) * B);
+        if (!buf) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int view = 0; view < c->n_views; ++view) {
+                double g[12] = {0};
+                for (long pix = 0; pix < per_view; ++pix) {
+                    long ray = view * per_view + pix;
+                    double wr = (double)w[ray];
+                    if (wr == 0.0) continue;
+                    double X0[3], r[3], tlo, thi;
+                    ora_ray(c, ray, X0, r, &tlo, &thi);
+                    /* clip to the grid, remembering which face plane bounds it */
+                    double amin = tlo, amax = thi;
+                    int ain = -1, aout = -1, empty = 0;
+                    for (int ax = 0; ax < 3; ++ax) {
+                        double p0 = c->o[ax], p1 = c->o[ax] + (double)c->n[ax] * c->d[ax];
+                        if (r[ax] == 0.0) {
+                            if (!(X0[ax] >= p0 && X0[ax] < p1)) empty = 1;
+                            continue;
+                        }
+                        double t0 = (p0 - X0[ax]) / r[ax], t1 = (p1 - X0[ax]) / r[ax];
+                        double e0 = fmin(t0, t1), e1 = fmax(t0, t1);
+                        if (e0 > amin) { amin = e0; ain = ax; }
+                        if (e1 < amax) { amax = e1; aout = ax; }
+                    }
+                    if (empty || !(amin < amax)) continue;
+                    /* interior crossings per axis, merged in increasing t */
+                    double *seq[3];
+                    int len[3], pos[3];
+                    double *next = buf;
+                    for (int ax = 0; ax < 3; ++ax) {
+                        seq[ax] = next;
+                        len[ax] = 0;
+                        pos[ax] = 0;
+                        if (r[ax] == 0.0) continue;
+                        for (int m = 0; m <= c->n[ax]; ++m) {
+                            int k = r[ax] > 0.0 ? m : c->n[ax] - m;
+                            double t = (c->o[ax] + (double)k * c->d[ax] - X0[ax]) / r[ax];
+                            if (t > amin && t < amax) seq[ax][len[ax]++] = t;
+                        }
+                        next += len[ax];
+                    }
+                    double norm = ora_norm(r);
+                    double sum_df[3] = {0, 0, 0}, sum_dft[3] = {0, 0, 0};
+                    double p = 0.0, prev = amin, f_prev = 0.0;
+                    int first = 1;
+                    for (;;) {
+                        double t = amax;
+                        int which = -1;
+                        for (int ax = 0; ax < 3; ++ax)
+                            if (pos[ax] < len[ax] && seq[ax][pos[ax]] < t) {
+                                t = seq[ax][pos[ax]];
+                                which = ax;
+                            }
+                        /* the piece [prev, t) and its value (midpoint cell) */
+                        double mid = 0.5 * (prev + t), f = 0.0;
+                        if (t > prev) {
+                            long idx[3];
+                            for (int ax = 0; ax < 3; ++ax) {
+                                long q = (long)floor((X0[ax] + mid * r[ax] - c->o[ax]) / c->d[ax]);
+                                if (q < 0) q = 0;
+                                if (q > c->n[ax] - 1) q = c->n[ax] - 1;
+                                idx[ax] = q;
+                            }
+                            f = (double)vol[(idx[2] * c->n[1] + idx[1]) * c->n[0] + idx[0]];
+                            p += (t - prev) * f;
+                        } else {
+                            f = f_prev;  /* zero-length piece: no value change */
+                        }
+                        if (first) {
+                            /* entry through a face plane: outside value 0 */
+                            if (ain >= 0) {
+                                sum_df[ain] += 0.0 - f;
+                                sum_dft[ain] += (0.0 - f) * amin;
+                            }
+                            first = 0;
+                        } else {
+                            /* the crossing at prev, recorded when it was consumed */
+                        }
+                        f_prev = f;
+                        if (which < 0) break;
+                        /* crossing of axis `which` at t: value before f, after = next piece */
+                        double t_next = amax;
+                        for (int ax = 0; ax < 3; ++ax) {
+                            int pp = pos[ax] + (ax == which ? 1 : 0);
+                            if (pp < len[ax] && seq[ax][pp] < t_next) t_next = seq[ax][pp];
+                        }
+                        double f_after = f;
+                        if (t_next > t) {
+                            double m2 = 0.5 * (t + t_next);
+                            long idx[3];
+                            for (int ax = 0; ax < 3; ++ax) {
+                                long q = (long)floor((X0[ax] + m2 * r[ax] - c->o[ax]) / c->d[ax]);
+                                if (q < 0) q = 0;
+                                if (q > c->n[ax] - 1) q = c->n[ax] - 1;
+                                idx[ax] = q;
+                            }
+                            f_after = (double)vol[(idx[2] * c->n[1] + idx[1]) * c->n[0] + idx[0]];
+                        }
+                        sum_df[which] += f - f_after;
+                        sum_dft[which] += (f - f_after) * t;
+                        pos[which]++;
+                        prev = t;
+                    }
+                    /* exit through a face plane: outside value 0 */
+                    if (aout >= 0) {
+                        sum_df[aout] += f_prev - 0.0;
+                        sum_dft[aout] += (f_prev - 0.0) * amax;
+                    }
+                    p *= norm;
+                    double gx[3], gr[3];
+                    for (int ax = 0; ax < 3; ++ax) {
+                        gx[ax] = r[ax] != 0.0 ? -norm * sum_df[ax] / r[ax] : 0.0;
+                        gr[ax] = (r[ax] != 0.0 ? -norm * sum_dft[ax] / r[ax] : 0.0) +
+                                 p * r[ax] / (norm * norm);
+                    }
+                    long iv = pix / c->n_u, iu = pix % c->n_u;
+                    double alpha = ((double)iu - 0.5 * (double)(c->n_u - 1) + c->offset_u) * c->pitch_u;
+                    double beta = ((double)iv - 0.5 * (double)(c->n_v - 1) + c->offset_v) * c->pitch_v;
+                    for (int ax = 0; ax < 3; ++ax) {
+                        double dsrc, dpix;
+                        if (c->beam == 1) {
+                            dsrc = gx[ax] - gr[ax];
+                            dpix = gr[ax];
+                        } else {
+                            dsrc = gr[ax];
+                            dpix = gx[ax];
+                        }
+                        g[ax] += wr * dsrc;
+                        g[3 + ax] += wr * dpix;
+                        g[6 + ax] += wr * alpha * dpix;
+                        g[9 + ax] += wr * beta * dpix;
+                    }
+                }
+                for (int m = 0; m < 12; ++m) out[12 * view + m] = g[m];
+            }
+        }
+        free(buf);
+    }
+    return err;
+}
