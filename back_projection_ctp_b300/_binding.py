@@ -53,7 +53,7 @@ class _PlanInfo(ctypes.Structure):
 EXPORTS = ("ctp_plan", "ctp_destroy", "ctp_plan_info_get", "ctp_forward", "ctp_backward",
            "ctp_segment_count", "ctp_forward_host", "ctp_backward_host", "ctp_status_string",
            "ctp_forward_static", "ctp_ramp_filter", "ctp_weighted_backproject",
-           "ctp_weighted_backproject_transpose", "ctp_fdk")
+           "ctp_weighted_backproject_transpose", "ctp_fdk", "ctp_geometry_vjp")
 
 RAMPS = {"ramlak": 0, "shepp_logan": 1}
 
@@ -84,6 +84,7 @@ def load_library(path: str | None = None):
         lib.ctp_weighted_backproject.argtypes = [P, P, P, P]
         lib.ctp_weighted_backproject_transpose.argtypes = [P, P, P, P]
         lib.ctp_fdk.argtypes = [P, P, P, P, P, I, P]
+        lib.ctp_geometry_vjp.argtypes = [P, P, P, P, P]
         lib.ctp_status_string.argtypes = [I]
         lib.ctp_status_string.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -353,3 +354,21 @@ def full_scan_view_weights(n_views: int):
     """View weights of a full 2 pi scan with equally spaced views: pi / n_views
     (the angular step, halved because every line is measured twice)."""
     return np.full(int(n_views), np.pi / max(int(n_views), 1), dtype=np.float32)
+
+
+# ------------------------------------------------------------ geometry gradients
+def ctp_geometry_vjp(plan: Plan, vol, weight, grad=None, stream=None):
+    """grad[s] = sum over view s's rays of weight[ray] * d (A vol)[ray] / d frame[s],
+    as a float64 CUDA tensor (n_views, 4, 3): src, det_centre, det_u, det_v."""
+    import torch
+    n_views = plan.sino_shape[0]
+    if grad is None:
+        grad = torch.empty((n_views, 4, 3), dtype=torch.float64, device=vol.device)
+    if not (isinstance(grad, torch.Tensor) and grad.is_cuda and grad.dtype == torch.float64
+            and grad.is_contiguous() and grad.numel() == 12 * n_views):
+        raise TypeError("grad must be a contiguous float64 CUDA tensor of n_views * 12 elements")
+    _check(load_library().ctp_geometry_vjp(
+        plan.handle, _device_f32(vol, plan.vol_shape, "vol"),
+        _device_f32(weight, plan.sino_shape, "weight"), grad.data_ptr(), _stream_ptr(stream)),
+        "ctp_geometry_vjp")
+    return grad

@@ -12,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libctp.so")
 SOURCES = ["ctp_api.cu"]
 DEPS = ["ctp_api.cu", "ctp_ray.cuh", "ctp_column.cuh", "ctp_plane.cuh", "ctp_fdk.cuh",
-        "ctp_internal.h"]
+        "ctp_geometry.cuh", "ctp_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

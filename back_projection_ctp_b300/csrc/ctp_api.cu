@@ -18,6 +18,7 @@
 #include "ctp.h"
 #include "ctp_column.cuh"
 #include "ctp_fdk.cuh"
+#include "ctp_geometry.cuh"
 #include "ctp_plane.cuh"
 #include "ctp_internal.h"
 #include "ctp_ray.cuh"
@@ -30,6 +31,7 @@ struct ctp_plan {
     int n[3] = {0, 0, 0};
     double spacing[3] = {0, 0, 0};
     double origin[3] = {0, 0, 0};
+    double pitch_u = 1, pitch_v = 1, offset_u = 0, offset_v = 0;
     long long n_rays = 0, n_cells = 0;
     std::vector<ctp::ViewFrame> frames;     // host copy
     ctp::ViewFrame *d_frames = nullptr;     // device copy
@@ -381,6 +383,10 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
     p->origin[0] = vol->ox;
     p->origin[1] = vol->oy;
     p->origin[2] = vol->oz;
+    p->pitch_u = geom->pitch_u;
+    p->pitch_v = geom->pitch_v;
+    p->offset_u = geom->offset_u;
+    p->offset_v = geom->offset_v;
     p->n_rays = (long long)geom->n_views * geom->n_u * geom->n_v;
     p->n_cells = (long long)vol->nx * vol->ny * vol->nz;
 
@@ -700,6 +706,24 @@ int ctp_weighted_backproject_transpose(const ctp_plan_t *plan, const float *vol_
     if (plan->n_rays == 0) return CTP_OK;
     return ctp::fdk_scatter(plan->fdk, vol_dev, sino_dev, (cudaStream_t)stream) ? CTP_E_CUDA
                                                                                 : CTP_OK;
+}
+
+int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *weight_dev,
+                     double *grad_dev, void *stream)
+{
+    if (!plan) return CTP_E_NULL;
+    if (plan->n_views > 0 && !grad_dev) return CTP_E_NULL;
+    if (plan->n_rays > 0 && (!vol_dev || !weight_dev)) return CTP_E_NULL;
+    int st = check_device(plan);
+    if (st != CTP_OK) return st;
+    if (plan->n_views == 0) return CTP_OK;
+    ctp::GeomParams Q;
+    Q.cu = (float)(0.5 * (plan->n_u - 1) - plan->offset_u);
+    Q.cv = (float)(0.5 * (plan->n_v - 1) - plan->offset_v);
+    Q.pitch_u = (float)plan->pitch_u;
+    Q.pitch_v = (float)plan->pitch_v;
+    return ctp::geometry_vjp(ray_params(plan), Q, vol_dev, weight_dev, grad_dev,
+                             (cudaStream_t)stream) ? CTP_E_CUDA : CTP_OK;
 }
 
 int ctp_fdk(const ctp_plan_t *plan, const float *sino_dev, float *work_dev, float *vol_dev,

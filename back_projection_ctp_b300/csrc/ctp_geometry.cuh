@@ -1,0 +1,246 @@
+// First-order geometry gradients of the path sums (vector-Jacobian product):
+//
+//     G[view][m] = sum over rays R of the view of w[R] * d p(R) / d theta_m,
+//     theta = (src, det_centre, det_u, det_v) of that view (12 numbers),
+//
+// the calibration gradient of the pages ("first-order source / centre / axis
+// gradients", diffct 2.4.1 -> 2.4.2, docs/video/README.md, shot "Geometry";
+// trajectory tensors that require gradients receive geometry gradients, diffct
+// 2.1.0 -> 2.2.1, README "Arbitrary trajectories").
+//
+// For the line X0 + t r (divergent: X0 = source, r = pixel - source, t in
+// [0, 1]; parallel: X0 = pixel, r = src) the path sum of the cell-constant
+// image is p = |r| sum_j (t_{j+1} - t_j) f_j.  A piece ends where the line
+// crosses a grid plane x_a = const (value outside the grid: 0) or at the ray's
+// own end point, which does not move with the planes.  A plane crossing at t_k
+// moves by dt_k = -(dX0_a + t_k dr_a) / r_a, hence
+//     dp/dX0_a = -|r| sum_{k on axis a} (f_before - f_after)_k / r_a
+//     dp/dr_a  = -|r| sum_{k on axis a} (f_before - f_after)_k t_k / r_a + p r_a / |r|^2
+// and pixel = centre + alpha u + beta v.  Configurations where two crossings
+// coincide (a ray through a cell edge) are kinks of p; the walk attributes the
+// jump to one of them.
+//
+// B300 design: the ray path's float64 set-up and exact fixed-point slab walk
+// (the same pieces as the forward), one thread per ray, crossings taken from
+// the walk's carries in order; the per-ray gradient is reduced over the block
+// (all threads of a block belong to one view) and added to the view's twelve
+// float64 sums with one atomic each.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ctp_internal.h"
+#include "ctp_ray.cuh"
+
+namespace ctp {
+
+struct GeomParams {
+    float cu, cv;            // pixel index of the detector centre: (n - 1)/2 - offset
+    float pitch_u, pitch_v;
+};
+
+// Axes, mirrored start and world direction of the ray through pixel (iu, iv):
+// the quantities slab_setup keeps implicit.
+struct RayAxes {
+    int ax[3];       // world axes of the slab walk's p, b, c (selected, not indexed)
+    double Ap, awp;  // mirrored p coordinate of X0 and |w_p| (cell units)
+    float r[3];      // world direction r (physical units)
+    float rn;        // |r|
+};
+
+__device__ __forceinline__ void ray_axes(const RayParams &P, int view, int iu, int iv, RayAxes &A)
+{
+    const ViewFrame &V = P.views[view];
+    double X0[3], w[3];
+    const double fu = (double)iu, fv = (double)iv;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        const double pix = __fma_rn(fv, V.dv[a], __fma_rn(fu, V.du[a], V.p00[a]));
+        X0[a] = P.beam == 1 ? V.a[a] : pix;
+        w[a] = P.beam == 1 ? __dsub_rn(pix, V.a[a]) : V.a[a];
+    }
+    const double aw0 = fabs(w[0]), aw1 = fabs(w[1]), aw2 = fabs(w[2]);
+    const int p = (aw0 >= aw1 && aw0 >= aw2) ? 0 : (aw1 >= aw2 ? 1 : 2);
+    A.ax[0] = p;
+    A.ax[1] = p == 0 ? 1 : 0;
+    A.ax[2] = p == 2 ? 1 : 2;
+    A.awp = p == 0 ? aw0 : (p == 1 ? aw1 : aw2);
+    A.Ap = w[p] < 0.0 ? __dsub_rn((double)P.n[p], X0[p]) : X0[p];
+    double n2 = 0.0;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        const double ra = __dmul_rn(w[a], P.spacing[a]);
+        A.r[a] = (float)ra;
+        n2 = __fma_rn(ra, ra, n2);
+    }
+    A.rn = (float)sqrt(n2);
+}
+
+// Walk of one ray collecting, per walk axis (0 = p, 1 = b, 2 = c), the sums of
+// value jumps (before - after) and of jumps times t over the plane crossings,
+// and the path sum.
+struct GradSums {
+    float df[3], dft[3];
+    float path;   // sum of slab fraction * value (times ell: the path sum)
+};
+
+// Adds jump j at parameter t to walk axis b (on_b) or c.
+__device__ __forceinline__ void grad_add_bc(GradSums &G, bool on_b, float j, float t)
+{
+    if (on_b) {
+        G.df[1] += j;
+        G.dft[1] = __fmaf_rn(j, t, G.dft[1]);
+    } else {
+        G.df[2] += j;
+        G.dft[2] = __fmaf_rn(j, t, G.dft[2]);
+    }
+}
+
+__device__ __forceinline__ void grad_walk(const SlabRay &R, const RayAxes &A,
+                                          const float *__restrict__ vol, GradSums &G)
+{
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        G.df[a] = 0.0f;
+        G.dft[a] = 0.0f;
+    }
+    G.path = 0.0f;
+    // t of the mirrored p coordinate xi: t = (xi - Ap) / |w_p|
+    const float t0 = (float)__ddiv_rn(__dsub_rn((double)R.k0, A.Ap), A.awp);
+    const float tinv = (float)__ddiv_rn(1.0, A.awp);
+    uint32_t fb = R.fb, fc = R.fc;
+    int jb = R.jb, jc = R.jc, addr = R.addr;
+    const unsigned nb = (unsigned)R.nb, nc = (unsigned)R.nc;
+    float f_prev = 0.0f;
+    for (int k = R.k0; k <= R.k1; ++k) {
+        const uint32_t gb = fb + R.bb, gc = fc + R.bc;
+        const bool cb = gb < fb, cc = gc < fc;
+        const float tb = cb ? fminf(__fmul_rn(__uint2float_rn(0u - fb), R.ib), 1.0f) : 1.0f;
+        const float tc = cc ? fminf(__fmul_rn(__uint2float_rn(0u - fc), R.ic), 1.0f) : 1.0f;
+        const float lo = k == R.k0 ? R.tlo : 0.0f;
+        const float hi = k == R.k1 ? R.thi : 1.0f;
+        const bool bfirst = tb < tc;
+        const float x1 = fminf(tb, tc), x2 = fmaxf(tb, tc);  // crossing fractions
+        const bool c1 = bfirst ? cb : cc, c2 = bfirst ? cc : cb;
+        const float e1 = fminf(fmaxf(x1, lo), hi);
+        const float e2 = fminf(fmaxf(x2, lo), hi);
+        const float d1 = __fsub_rn(e1, lo), d2 = __fsub_rn(e2, e1), d3 = __fsub_rn(hi, e2);
+        const int jb2 = jb + (bfirst ? 1 : 0), jc2 = jc + (bfirst ? 0 : 1);
+        const int jb3 = jb + (cb ? 1 : 0), jc3 = jc + (cc ? 1 : 0);
+        const int a2 = addr + (bfirst ? R.sb : R.sc);
+        const int a3 = addr + (cb ? R.sb : 0) + (cc ? R.sc : 0);
+        const float v1 = ((unsigned)jb < nb && (unsigned)jc < nc) ? __ldg(vol + addr) : 0.0f;
+        const float v2 = ((unsigned)jb2 < nb && (unsigned)jc2 < nc) ? __ldg(vol + a2) : 0.0f;
+        const float v3 = ((unsigned)jb3 < nb && (unsigned)jc3 < nc) ? __ldg(vol + a3) : 0.0f;
+        G.path = __fmaf_rn(d1, v1, __fmaf_rn(d2, v2, __fmaf_rn(d3, v3, G.path)));
+        const float tk = __fmaf_rn((float)(k - R.k0), tinv, t0);  // t at the slab start
+        // the p plane at the slab start: crossed unless the ray begins in this slab
+        if (k > R.k0 || R.tlo == 0.0f) {
+            const float j = f_prev - v1;
+            G.df[0] += j;
+            G.dft[0] = __fmaf_rn(j, tk, G.dft[0]);
+        }
+        // transverse crossings strictly inside the ray's extent in this slab
+        const bool r1 = c1 && x1 > lo && x1 < hi, r2 = c2 && x2 > lo && x2 < hi;
+        if (r1) grad_add_bc(G, bfirst, v1 - v2, __fmaf_rn(x1, tinv, tk));
+        if (r2) grad_add_bc(G, !bfirst, v2 - v3, __fmaf_rn(x2, tinv, tk));
+        // the cell at the slab's end lies past every crossing before hi, also
+        // those before the ray's own start
+        const bool h1 = c1 && x1 < hi, h2 = c2 && x2 < hi;
+        f_prev = h2 ? v3 : (h1 ? v2 : v1);
+        fb = gb;
+        fc = gc;
+        jb = jb3;
+        jc = jc3;
+        addr = a3 + R.sp;
+    }
+    // the p plane at the end of the last slab, when the ray goes on past it
+    if (R.thi == 1.0f) {
+        const float tk = __fmaf_rn((float)(R.k1 + 1 - R.k0), tinv, t0);
+        G.df[0] += f_prev;
+        G.dft[0] = __fmaf_rn(f_prev, tk, G.dft[0]);
+    }
+}
+
+template <int TU, int TV>
+__global__ void __launch_bounds__(TU *TV) geometry_vjp_kernel(RayParams P, GeomParams Q,
+                                                              const float *__restrict__ vol,
+                                                              const float *__restrict__ w,
+                                                              double *__restrict__ out)
+{
+    constexpr int kWarps = TU * TV / 32;
+    __shared__ float part[kWarps][12];
+    const int iu = blockIdx.x * TU + (int)(threadIdx.x % TU);
+    const int iv = blockIdx.z * TV + (int)(threadIdx.x / TU);
+    const int view = P.view0 + (int)blockIdx.y;
+    float g[12];
+#pragma unroll
+    for (int m = 0; m < 12; ++m) g[m] = 0.0f;
+    if (iu < P.n_u && iv < P.n_v) {
+        const long long ray = ((long long)view * P.n_v + iv) * P.n_u + iu;
+        const float wr = w[ray];
+        SlabRay R;
+        if (wr != 0.0f && slab_setup(P, view, iu, iv, R)) {
+            RayAxes A;
+            ray_axes(P, view, iu, iv, A);
+            GradSums S;
+            grad_walk(R, A, vol, S);
+            const float p = __fmul_rn(S.path, R.ell);
+            const float rn2 = __fmul_rn(A.rn, A.rn);
+            const float alpha = ((float)iu - Q.cu) * Q.pitch_u;
+            const float beta = ((float)iv - Q.cv) * Q.pitch_v;
+#pragma unroll
+            for (int a = 0; a < 3; ++a) {
+                // the walk axis that is world axis a
+                const int q = A.ax[0] == a ? 0 : (A.ax[1] == a ? 1 : 2);
+                const float df = q == 0 ? S.df[0] : (q == 1 ? S.df[1] : S.df[2]);
+                const float dft = q == 0 ? S.dft[0] : (q == 1 ? S.dft[1] : S.dft[2]);
+                const float ra = A.r[a];
+                const float gx = ra != 0.0f ? -A.rn * df / ra : 0.0f;
+                const float gr = (ra != 0.0f ? -A.rn * dft / ra : 0.0f) + p * ra / rn2;
+                const float dsrc = P.beam == 1 ? gx - gr : gr;
+                const float dpix = P.beam == 1 ? gr : gx;
+                g[a] = wr * dsrc;
+                g[3 + a] = wr * dpix;
+                g[6 + a] = wr * alpha * dpix;
+                g[9 + a] = wr * beta * dpix;
+            }
+        }
+    }
+    // block reduction (one view per block), then one float64 atomic per component
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int m = 0; m < 12; ++m) {
+        float v = g[m];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+        if (lane == 0) part[warp][m] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < 12) {
+        double s = 0.0;
+#pragma unroll
+        for (int q = 0; q < kWarps; ++q) s += (double)part[q][threadIdx.x];
+        atomicAdd(out + 12 * (long long)view + threadIdx.x, s);
+    }
+}
+
+inline int geometry_vjp(const RayParams &P, const GeomParams &Q, const float *vol, const float *w,
+                        double *out, cudaStream_t s)
+{
+    if (cudaMemsetAsync(out, 0, sizeof(double) * 12 * (size_t)(P.n_views > 0 ? P.n_views : 0), s) !=
+        cudaSuccess)
+        return 9;
+    if (P.view_count <= 0) return 0;
+    if (P.n_v == 1) {
+        dim3 grid((P.n_u + 127) / 128, P.view_count, 1);
+        geometry_vjp_kernel<128, 1><<<grid, 128, 0, s>>>(P, Q, vol, w, out);
+    } else {
+        dim3 grid((P.n_u + 31) / 32, P.view_count, (P.n_v + 3) / 4);
+        geometry_vjp_kernel<32, 4><<<grid, 128, 0, s>>>(P, Q, vol, w, out);
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+}  // namespace ctp

@@ -526,6 +526,100 @@ def run_fdk(args, w, world, rank, local):
     return 0
 
 
+# ------------------------------------------------ geometry gradients (third op)
+GEOM_METRIC = "Geometry-gradient Gseg/s (ray walk with crossing terms) on 1 B300"
+
+
+def run_geometry(args, w, world, rank, local):
+    """Time K geometry vector-Jacobian products (all views) of the workload."""
+    import torch
+    import back_projection_ctp_b300 as ctp
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    frames = ci.frames(w)
+    plan = ctp.ctp_plan(geometry_of(w, frames), volume_of(w), args.path)
+    segments = golden_segments(args.config) if args.views is None else ctp.ctp_segment_count(plan)
+    stream = torch.cuda.current_stream(dev)
+    d_vol = torch.from_numpy(ci.phantom(w)).to(dev)
+    d_y = torch.from_numpy(ci.sinogram_noise(w).reshape(plan.sino_shape)).to(dev)
+    grad = torch.empty((w.n_views, 4, 3), dtype=torch.float64, device=dev)
+    for _ in range(args.warmup):
+        ctp.ctp_geometry_vjp(plan, d_vol, d_y, grad, stream)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side), torch.cuda.graph(graph, stream=side):
+        cur = torch.cuda.current_stream(dev)
+        for _ in range(args.steps):
+            ctp.ctp_geometry_vjp(plan, d_vol, d_y, grad, cur)
+    torch.cuda.synchronize(dev)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
+    value = world * segments / (ms * 1e-3) / 1e9
+    achieved = 4.0 * segments / (ms * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            import oracle
+            scan = oracle.Scan.from_workload(w, frames)
+            cores = len(os.sched_getaffinity(0))
+            per = w.n_u * w.n_v
+            t = time.perf_counter()
+            oracle.geometry_vjp(_first_views(oracle, scan, w, 1), ci.phantom(w),
+                                np.ones(per, np.float32), threads=cores)
+            probe = time.perf_counter() - t
+            m = int(max(1, min(w.n_views, args.ref_budget // max(probe, 1e-3))))
+            sub = _first_views(oracle, scan, w, m)
+            segs = oracle.segment_count(sub, threads=cores)
+            t = time.perf_counter()
+            oracle.geometry_vjp(sub, ci.phantom(w), np.ones(m * per, np.float32), threads=cores)
+            dt = time.perf_counter() - t
+            cpu = {"value": segs / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+                   "sample": f"views 0..{m - 1} of {w.n_views}: float64 C oracle geometry "
+                             f"gradient, {segs} segments, {dt:.1f} s"}
+        line = {
+            "metric": GEOM_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "op": "geometry", "views": w.n_views,
+                       "detector_vu": [w.n_v, w.n_u], "segments_per_pass": segments,
+                       "parallelism": f"replicas{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "kernel": "geometry_vjp_kernel", "call": "geometry_vjp",
+                         "note": f"4 B per segment over the call's event time; peak {peak_src}"},
+            "cpu_baseline": cpu,
+            "gpu_launches": args.steps,
+            "timing": "one CUDA graph of K calls replayed between CUDA events on the calls' stream",
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    plan.destroy()
+    return 0
+
+
+def _first_views(oracle, scan, w, m):
+    return oracle.Scan(w.beam, *(a[:m] for a in scan.arrays), w.n_u, w.n_v, w.pitch_u,
+                       w.pitch_v, w.shape, w.spacing, w.origin, w.offset_u, w.offset_v, w.ndim)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -539,9 +633,10 @@ def main(argv=None):
     ap.add_argument("--path", default="auto", choices=["auto", "ray", "column"])
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="siddon", choices=["siddon", "fdk"],
+    ap.add_argument("--op", default="siddon", choices=["siddon", "fdk", "geometry"],
                     help="siddon: the projector pair (default); fdk: the analytical "
-                         "filtered backprojection on the same workload")
+                         "filtered backprojection on the same workload; geometry: the "
+                         "projection's geometry gradients")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -555,6 +650,8 @@ def main(argv=None):
             return run_reference(args, w, world, rank)
         if args.op == "fdk":
             return run_fdk(args, w, world, rank, local)
+        if args.op == "geometry":
+            return run_geometry(args, w, world, rank, local)
         return run_gpu(args, w, world, rank, local)
     finally:
         if world > 1:

@@ -252,6 +252,34 @@ int ctp_weighted_backproject_transpose(const ctp_plan_t *plan, const float *vol_
 int ctp_fdk(const ctp_plan_t *plan, const float *sino_dev, float *work_dev, float *vol_dev,
             const float *view_weight_dev, int ramp, void *stream);
 
+/*
+ * ctp_geometry_vjp -- first-order geometry gradients of the projection
+ * ("first-order source / centre / axis gradients", diffct release diff
+ * 2.4.1 -> 2.4.2, docs/video/README.md; trajectory tensors that require
+ * gradients receive geometry gradients, release diff 2.1.0 -> 2.2.1, README
+ * "Arbitrary trajectories"):
+ *
+ *     grad[s][0..2]  = sum over rays R of view s of w[R] * dp(R)/d src[s]
+ *     grad[s][3..5]  = ... d det_centre[s],   grad[s][6..8] = ... d det_u[s],
+ *     grad[s][9..11] = ... d det_v[s]
+ *
+ * with p = A vol the path sums of the plan's scan.  For the line X0 + t r
+ * (divergent: X0 = source, r = pixel - source, t in [0, 1]; parallel: X0 =
+ * pixel, r = src) p = |r| sum_j (t_{j+1} - t_j) f_j; every crossing of a grid
+ * plane x_a = const at t_k (value outside the grid 0; the ray's own end points
+ * are not crossings) contributes -(f_before - f_after) |r| (dX0_a + t_k dr_a) / r_a,
+ * and the length scale contributes p r.dr / |r|^2; pixel = centre + alpha u +
+ * beta v.  The gradient of the backprojection <A^T y, h> with respect to the
+ * geometry is the same call with vol = h and w = y.  Rays through a cell edge
+ * or corner are kinks of p; the jump goes to one of the coincident crossings.
+ * vol_dev: device float32 (nz, ny, nx).  weight_dev: device float32
+ * (n_views, n_v, n_u).  grad_dev: device float64 (n_views, 12), overwritten.
+ * Runs the ray path's walk whatever path the plan chose; asynchronous on
+ * `stream`.  Errors: CTP_E_NULL, CTP_E_DEVICE, CTP_E_CUDA.
+ */
+int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *weight_dev,
+                     double *grad_dev, void *stream);
+
 /* Static English text of a status code. */
 const char *ctp_status_string(int status);
 

@@ -25,6 +25,8 @@ Functions and what pins them (the tests under ``tests/test_oracle_*.py``):
 * :func:`geometry_vjp` -- first-order gradients of the path sums with respect to
   the per-view frames; pinned by central finite differences of :func:`forward`
   and by the invariance of chords under sliding a ray's end points along it.
+* :func:`kinks` -- rays through a cell edge or corner (no geometry derivative);
+  pinned on hand-built rays.
 """
 
 from __future__ import annotations
@@ -91,6 +93,7 @@ def _load():
                 "ora_supersampled": [C, P, P, L, L, P, I],
                 "ora_trace_ray": [C, L, P, P],
                 "ora_geometry_vjp": [C, P, P, P, I],
+                "ora_kinks": [C, D, P, I],
             }
             for name, args in sigs.items():
                 fn = getattr(lib, name)
@@ -280,3 +283,13 @@ def geometry_vjp(scan: Scan, vol, weights, threads=0):
     _check(_load().ora_geometry_vjp(scan.ref(), vol.ctypes.data, w.ctypes.data,
                                     out.ctypes.data, threads), "ora_geometry_vjp")
     return out
+
+
+def kinks(scan: Scan, tol=1e-6, threads=0):
+    """Boolean (n_views, n_v, n_u): rays on which two plane crossings of different
+    axes coincide within ``tol`` cells (through a cell edge or corner), or whose
+    end point inside the grid lies on a plane: the path sum has no geometry
+    derivative there."""
+    flags = np.zeros(scan.n_rays, dtype=np.uint8)
+    _check(_load().ora_kinks(scan.ref(), float(tol), flags.ctypes.data, threads), "ora_kinks")
+    return flags.reshape(scan.sino_shape).astype(bool)

@@ -797,3 +797,91 @@ int ora_geometry_vjp(const ora_ctx *c, const float *vol, const float *w, double 
     }
     return err;
 }
+
+/*
+ * Kink flags: rays on which two plane crossings of different axes coincide
+ * within `tol` cells (the ray passes through a cell edge or corner, or enters /
+ * leaves the grid there), or whose own end point inside the grid lies within
+ * `tol` cells of a plane.  The path sum is not differentiable in the geometry
+ * there: each side's derivative gives the jump to a different axis, and any
+ * finite-precision traversal may pick either.  Used to exclude such rays from
+ * gradient comparisons.
+ */
+int ora_kinks(const ora_ctx *c, double tol, unsigned char *flags, int nthreads)
+{
+    int T = ora_threads(nthreads);
+    int B = c->n[0] + c->n[1] + c->n[2] + 8;
+    long nr = ora_n_rays(c);
+    double dmin = fmin(c->d[0], fmin(c->d[1], c->d[2]));
+    int err = 0;
+#pragma omp parallel num_threads(T)
+    {
+        double *ts = (double *)malloc(sizeof(double) * B);
+        int *axs = (int *)malloc(sizeof(int) * B);
+        if (!ts || !axs) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic, 64)
+            for (long ray = 0; ray < nr; ++ray) {
+                double X0[3], r[3], tlo, thi;
+                ora_ray(c, ray, X0, r, &tlo, &thi);
+                flags[ray] = 0;
+                double amin = tlo, amax = thi;
+                int empty = 0;
+                for (int ax = 0; ax < 3; ++ax) {
+                    double p0 = c->o[ax], p1 = c->o[ax] + (double)c->n[ax] * c->d[ax];
+                    if (r[ax] == 0.0) {
+                        if (!(X0[ax] >= p0 && X0[ax] < p1)) empty = 1;
+                        continue;
+                    }
+                    double t0 = (p0 - X0[ax]) / r[ax], t1 = (p1 - X0[ax]) / r[ax];
+                    amin = fmax(amin, fmin(t0, t1));
+                    amax = fmin(amax, fmax(t0, t1));
+                }
+                if (empty || !(amin < amax)) continue;
+                /* every plane crossing within tol of [amin, amax], all axes, unsorted */
+                double scale = ora_norm(r) / dmin, eps = tol / scale;
+                int m = 0;
+                for (int ax = 0; ax < 3; ++ax) {
+                    if (r[ax] == 0.0) continue;
+                    for (int k = 0; k <= c->n[ax]; ++k) {
+                        double t = (c->o[ax] + (double)k * c->d[ax] - X0[ax]) / r[ax];
+                        if (t >= amin - eps && t <= amax + eps) {
+                            ts[m] = t;
+                            axs[m] = ax;
+                            ++m;
+                        }
+                    }
+                }
+                /* insertion sort by t (m is at most nx + ny + nz + 3) */
+                for (int q = 1; q < m; ++q) {
+                    double t = ts[q];
+                    int a = axs[q], s = q - 1;
+                    while (s >= 0 && ts[s] > t) {
+                        ts[s + 1] = ts[s];
+                        axs[s + 1] = axs[s];
+                        --s;
+                    }
+                    ts[s + 1] = t;
+                    axs[s + 1] = a;
+                }
+                for (int q = 1; q < m; ++q)
+                    if (axs[q] != axs[q - 1] && (ts[q] - ts[q - 1]) * scale <= tol) {
+                        flags[ray] = 1;
+                        break;
+                    }
+                /* an end point of the ray inside the grid that lies on a plane */
+                for (int q = 0; q < m; ++q)
+                    if ((amin == tlo && fabs(ts[q] - amin) * scale <= tol) ||
+                        (amax == thi && fabs(amax - ts[q]) * scale <= tol)) {
+                        flags[ray] = 1;
+                        break;
+                    }
+            }
+        }
+        free(ts);
+        free(axs);
+    }
+    return err;
+}

@@ -103,3 +103,31 @@ def test_uniform_volume_gradient_is_the_box_chord_gradient(oracle_mod):
             minus[part][:, ax] -= h
             fd = (chords(plus) - chords(minus)) / (2 * h)
             np.testing.assert_allclose(g[:, part, ax], fd, rtol=1e-6, atol=1e-7)
+
+
+def test_kink_flags_on_hand_built_rays(oracle_mod):
+    """Unit cells: a ray through the edge x = 1, y = 1 (the diagonal of the xy
+    plane at z = 0.5) is a kink; the same ray shifted by 0.3 in y is not; a ray
+    entering through the box edge x = 0, y = 0 is one too."""
+    def scan_of(src, cen):
+        z = np.float32
+        fr = (np.array([src], z), np.array([cen], z), np.array([[0, 0, 1]], z),
+              np.array([[1, -1, 0]], z) / np.float32(np.sqrt(2)))
+        return oracle_mod.Scan("divergent", *fr, 1, 1, 1.0, 1.0, (3, 3, 3), (1.0, 1.0, 1.0),
+                               (0.0, 0.0, 0.0))
+    assert oracle_mod.kinks(scan_of((-1.0, -1.0, 0.5), (4.0, 4.0, 0.5))).all()
+    assert not oracle_mod.kinks(scan_of((-1.0, -0.7, 0.5), (4.0, 4.3, 0.5))).any()
+    assert oracle_mod.kinks(scan_of((-1.0, -1.0, 1.5), (4.0, 4.0, 1.5))).all()
+
+
+def test_kink_flags_source_on_a_plane(oracle_mod):
+    """A divergent ray starting inside the grid exactly on a plane is a kink;
+    starting 0.25 cell off it is not."""
+    def scan_of(src):
+        z = np.float32
+        fr = (np.array([src], z), np.array([[5.0, 1.3, 1.6]], z), np.array([[0, 1, 0]], z),
+              np.array([[0, 0, 1]], z))
+        return oracle_mod.Scan("divergent", *fr, 1, 1, 1.0, 1.0, (3, 3, 3), (1.0, 1.0, 1.0),
+                               (0.0, 0.0, 0.0))
+    assert oracle_mod.kinks(scan_of((1.0, 1.4, 1.55))).all()
+    assert not oracle_mod.kinks(scan_of((1.25, 1.4, 1.55))).any()
