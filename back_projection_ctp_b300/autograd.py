@@ -14,8 +14,10 @@ from __future__ import annotations
 
 import torch
 
-from ._binding import (Geometry, Plan, Volume, ctp_backward, ctp_forward, ctp_plan,
-                       ctp_ramp_filter, ctp_weighted_backproject,
+import dataclasses
+
+from ._binding import (Geometry, Plan, Volume, ctp_backward, ctp_forward, ctp_geometry_vjp,
+                       ctp_plan, ctp_ramp_filter, ctp_weighted_backproject,
                        ctp_weighted_backproject_transpose)
 
 
@@ -148,3 +150,61 @@ class _GatherT(torch.autograd.Function):
     def backward(ctx, grad):
         g = _Gather.apply(grad, ctx.proj)
         return g.to(dtype=ctx.in_dtype, device=ctx.in_device), None
+
+
+# ------------------------------------------------------------ geometry gradients
+FRAME_NAMES = ("src", "det_centre", "det_u", "det_v")
+
+
+def project_with_geometry(vol: torch.Tensor, geometry: Geometry, volume: Volume,
+                          src: torch.Tensor, det_centre: torch.Tensor, det_u: torch.Tensor,
+                          det_v: torch.Tensor, path: str = "auto") -> torch.Tensor:
+    """A vol with the per-view frames as differentiable inputs: the gradient
+    with respect to each frame tensor (n_views, 3) is the first-order geometry
+    gradient of the pages ("first-order source / centre / axis gradients";
+    trajectory tensors that require gradients receive geometry gradients,
+    README "Arbitrary trajectories").  ``geometry`` supplies the detector size,
+    pitches and offsets; its frame arrays are replaced by the tensors' values
+    (a plan is built for them on every call).  vol: (..., D, H, W); the
+    geometry gradient sums over leading dims.  First order in the frames."""
+    return _ProjectGeometry.apply(vol, geometry, volume, path, src, det_centre, det_u, det_v)
+
+
+class _ProjectGeometry(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, vol, geometry, volume, path, *frames):
+        values = [f.detach().to(device="cpu", dtype=torch.float32).contiguous().numpy()
+                  for f in frames]
+        geo = dataclasses.replace(geometry, **dict(zip(FRAME_NAMES, values)))
+        proj = Projector(geo, volume, path)
+        ctx.proj = proj
+        ctx.frame_meta = [(f.dtype, f.device) for f in frames]
+        ctx.in_dtype, ctx.in_device = vol.dtype, vol.device
+        out = _apply(proj, vol, proj.vol_shape, proj.sino_shape, ctp_forward)
+        ctx.save_for_backward(vol.detach().to(device=proj.device, dtype=torch.float32))
+        return out
+
+    @staticmethod
+    def backward(ctx, grad):
+        (vol,) = ctx.saved_tensors
+        proj = ctx.proj
+        g_vol = None
+        if ctx.needs_input_grad[0]:
+            g_vol = _Backproject.apply(grad, proj).to(dtype=ctx.in_dtype, device=ctx.in_device)
+        g_frames = [None] * 4
+        if any(ctx.needs_input_grad[4:]):
+            grad = grad.detach().to(device=proj.device, dtype=torch.float32).contiguous()
+            _batched(grad, proj.sino_shape, "grad")
+            v = vol.reshape((-1,) + tuple(proj.vol_shape))
+            gr = grad.reshape((-1,) + tuple(proj.sino_shape))
+            total = torch.zeros((proj.sino_shape[0], 4, 3), dtype=torch.float64,
+                                device=proj.device)
+            part = torch.empty_like(total)
+            stream = torch.cuda.current_stream(proj.device)
+            for i in range(gr.shape[0]):   # leading dims of vol and grad agree
+                ctp_geometry_vjp(proj.plan, v[i].contiguous(), gr[i].contiguous(), part, stream)
+                total += part
+            for q, (dt, dev) in enumerate(ctx.frame_meta):
+                if ctx.needs_input_grad[4 + q]:
+                    g_frames[q] = total[:, q, :].to(dtype=dt, device=dev)
+        return (g_vol, None, None, None, *g_frames)

@@ -98,3 +98,29 @@ def test_fdk_batch_dims(proj):
     assert out.shape == (2,) + proj.vol_shape
     one = proj.fdk(y[1])
     assert rel_l2(out[1].cpu().numpy(), one.cpu().numpy()) == 0.0
+
+
+@pytest.mark.parametrize("beam_idx", [3, 2])
+def test_geometry_gradients_through_autograd(oracle_mod, beam_idx):
+    """loss = <A(frames) x, w>: the frames' .grad equals the oracle's geometry
+    gradient (kink and face-plane rays carry zero weight) and x.grad = A^T w."""
+    import torch
+    from back_projection_ctp_b300.autograd import project_with_geometry
+    w_ = ci.small_cases()[beam_idx]
+    f = ci.frames(w_)
+    scan = oracle_mod.Scan.from_workload(w_, f)
+    skip = oracle_mod.ambiguous(scan) | oracle_mod.kinks(scan)
+    wt = np.where(skip, 0.0, np.random.default_rng(5).standard_normal(scan.sino_shape))
+    wt = wt.astype(np.float32)
+    vol = ci.phantom(w_)
+    x = torch.from_numpy(vol).cuda().requires_grad_()
+    frames = [torch.from_numpy(f[k].astype(np.float64)).requires_grad_()
+              for k in ("src", "det_centre", "det_u", "det_v")]
+    out = project_with_geometry(x, geometry_of(w_, f), volume_of(w_), *frames)
+    (out * torch.from_numpy(wt).cuda()).sum().backward()
+    got = np.stack([fr.grad.numpy() for fr in frames], axis=1)
+    ref = oracle_mod.geometry_vjp(scan, vol, wt.ravel())
+    assert rel_l2(got, ref) <= 1e-4
+    assert frames[0].grad.dtype == torch.float64
+    back = oracle_mod.backward(scan, wt.ravel())
+    assert rel_l2(x.grad.cpu().numpy(), back) <= 1e-4
