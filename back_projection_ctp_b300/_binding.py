@@ -36,7 +36,8 @@ class _Geometry(ctypes.Structure):
                 ("src", ctypes.c_void_p), ("det_centre", ctypes.c_void_p),
                 ("det_u", ctypes.c_void_p), ("det_v", ctypes.c_void_p),
                 ("pitch_u", ctypes.c_double), ("pitch_v", ctypes.c_double),
-                ("offset_u", ctypes.c_double), ("offset_v", ctypes.c_double)]
+                ("offset_u", ctypes.c_double), ("offset_v", ctypes.c_double),
+                ("pixel_offsets", ctypes.c_void_p)]
 
 
 class _Volume(ctypes.Structure):
@@ -118,6 +119,9 @@ class Geometry:
     pitch_v: float
     offset_u: float = 0.0
     offset_v: float = 0.0
+    # curved detector: (n_v, n_u, 3) per-pixel (t, s, e) offsets from det_centre
+    # along det_u, det_v and the unit normal det_u x det_v; None = the pitch grid
+    pixel_offsets: np.ndarray | None = None
 
 
 @dataclasses.dataclass
@@ -181,12 +185,25 @@ def _c_scan(geometry: Geometry, volume: Volume):
     g.src, g.det_centre, g.det_u, g.det_v = (a.ctypes.data for a in arrays)
     g.pitch_u, g.pitch_v = float(geometry.pitch_u), float(geometry.pitch_v)
     g.offset_u, g.offset_v = float(geometry.offset_u), float(geometry.offset_v)
+    arrays.append(_pixel_offsets(geometry, g))
     D, H, W = (int(s) for s in volume.shape)
     v = _Volume()
     v.nx, v.ny, v.nz = W, H, D
     v.dz, v.dy, v.dx = (float(s) for s in volume.spacing)
     v.ox, v.oy, v.oz = (float(s) for s in volume.origin)
     return g, v, arrays
+
+
+def _pixel_offsets(geometry: Geometry, g: _Geometry):
+    """Sets g.pixel_offsets; returns the array that must outlive the call."""
+    if geometry.pixel_offsets is None:
+        g.pixel_offsets = None
+        return None
+    off = np.ascontiguousarray(geometry.pixel_offsets, dtype=np.float32)
+    if off.size != 3 * int(geometry.n_u) * int(geometry.n_v):
+        raise ValueError("pixel_offsets must hold (n_v, n_u, 3) values")
+    g.pixel_offsets = off.ctypes.data
+    return off
 
 
 def ctp_forward_static(geometry: Geometry, volume: Volume, vol, sino, stream=None):
@@ -216,6 +233,7 @@ def ctp_plan(geometry: Geometry, volume: Volume, path: str = "auto") -> Plan:
     g.src, g.det_centre, g.det_u, g.det_v = (a.ctypes.data for a in arrays)
     g.pitch_u, g.pitch_v = float(geometry.pitch_u), float(geometry.pitch_v)
     g.offset_u, g.offset_v = float(geometry.offset_u), float(geometry.offset_v)
+    offsets = _pixel_offsets(geometry, g)  # noqa: F841 (kept alive for the call)
     D, H, W = (int(s) for s in volume.shape)
     dz, dy, dx = (float(s) for s in volume.spacing)
     v = _Volume()
@@ -226,7 +244,7 @@ def ctp_plan(geometry: Geometry, volume: Volume, path: str = "auto") -> Plan:
     _check(lib.ctp_plan(ctypes.byref(g), ctypes.byref(v), PATHS[path], ctypes.byref(h)),
            "ctp_plan")
     geometry = dataclasses.replace(geometry, src=arrays[0], det_centre=arrays[1],
-                                   det_u=arrays[2], det_v=arrays[3])
+                                   det_u=arrays[2], det_v=arrays[3], pixel_offsets=offsets)
     return Plan(h.value, geometry, volume)
 
 

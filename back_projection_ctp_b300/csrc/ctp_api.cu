@@ -35,6 +35,7 @@ struct ctp_plan {
     long long n_rays = 0, n_cells = 0;
     std::vector<ctp::ViewFrame> frames;     // host copy
     ctp::ViewFrame *d_frames = nullptr;     // device copy
+    float *d_offsets = nullptr;             // curved detector: (n_v, n_u, 3) pixel offsets
     unsigned long long *d_counter = nullptr;
     // column and plane paths
     ctp::ColumnPlan col{};
@@ -93,6 +94,7 @@ ctp::RayParams ray_params(const ctp_plan_t *plan)
                                          std::fmin(plan->spacing[1], plan->spacing[2])));
     P.view0 = 0;
     P.view_count = plan->n_views;
+    P.offsets = plan->d_offsets;
     return P;
 }
 
@@ -198,6 +200,7 @@ void free_plan(ctp_plan_t *p)
     if (!p) return;
     cudaDeviceSynchronize();
     cudaFree(p->d_frames);
+    cudaFree(p->d_offsets);
     cudaFree(p->d_counter);
     cudaFree(p->d_table);
     cudaFree(p->d_work_fwd);
@@ -243,6 +246,9 @@ int validate(const ctp_geometry *g, const ctp_volume *v)
     if (g->ndim == 2 && !(sp[2] > 0.0)) return CTP_E_SPACING;
     if (smax / smin > 1e4) return CTP_E_SPACING;
     if (!(g->pitch_u > 0.0) || !(g->pitch_v > 0.0)) return CTP_E_SHAPE;
+    if (g->pixel_offsets)
+        for (long long q = 0; q < 3LL * g->n_u * g->n_v; ++q)
+            if (!std::isfinite(g->pixel_offsets[q])) return CTP_E_NONFINITE;
     if (g->n_views == 0) return CTP_OK;
     if (!g->src || !g->det_centre || !g->det_u || !g->det_v) return CTP_E_NULL;
 
@@ -289,6 +295,10 @@ int validate(const ctp_geometry *g, const ctp_volume *v)
 // ramp kernels).  A scan outside their class only records CTP_E_GEOMETRY.
 int fdk_setup(ctp_plan_t *p, const ctp_geometry *g, const ctp_volume *v)
 {
+    if (g->pixel_offsets) {
+        p->fdk_status = CTP_E_GEOMETRY;  // flat detectors only
+        return CTP_OK;
+    }
     std::vector<ctp::FdkView> views;
     const int n[3] = {v->nx, v->ny, v->nz};
     const double d[3] = {v->dx, v->dy, v->dz}, o[3] = {v->ox, v->oy, v->oz};
@@ -395,12 +405,27 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
     bool v_is_z = geom->ndim == 3;
     const double cu = 0.5 * (geom->n_u - 1) - geom->offset_u;
     const double cv = 0.5 * (geom->n_v - 1) - geom->offset_v;
+    const bool curved = geom->pixel_offsets != nullptr;
     for (int s = 0; s < geom->n_views; ++s) {
         const float *S = geom->src + 3 * s, *C = geom->det_centre + 3 * s;
         const float *U = geom->det_u + 3 * s, *V = geom->det_v + 3 * s;
         ctp::ViewFrame &F = p->frames[s];
+        // unit normal of the detector, for curved detectors' depth offsets
+        const double Ud[3] = {U[0], U[1], U[2]}, Vd[3] = {V[0], V[1], V[2]};
+        double N[3];
+        cross3(Ud, Vd, N);
+        const double nn = norm3(N);
         for (int a = 0; a < 3; ++a) {
             const double d = p->spacing[a], o = p->origin[a];
+            F.a[a] = geom->beam == CTP_DIVERGENT ? ((double)S[a] - o) / d : (double)S[a] / d;
+            if (curved) {
+                // pixel = centre + t u + s v + e n (per-pixel offsets in physical units)
+                F.p00[a] = ((double)C[a] - o) / d;
+                F.du[a] = Ud[a] / d;
+                F.dv[a] = Vd[a] / d;
+                F.dn[a] = N[a] / nn / d;
+                continue;
+            }
             const double pu = geom->pitch_u * (double)U[a];
             const double pv = geom->pitch_v * (double)V[a];
             // pixel (0, 0) = centre - cu * pitch_u * u - cv * pitch_v * v
@@ -408,14 +433,24 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
             F.p00[a] = (p00 - o) / d;
             F.du[a] = pu / d;
             F.dv[a] = pv / d;
-            F.a[a] = geom->beam == CTP_DIVERGENT ? ((double)S[a] - o) / d : (double)S[a] / d;
+            F.dn[a] = 0.0;
         }
         if (!(V[0] == 0.0f && V[1] == 0.0f && V[2] != 0.0f)) v_is_z = false;
+    }
+    if (curved) {
+        // the column and plane paths assume the pitch grid
+        if (path == CTP_PATH_COLUMN || path == CTP_PATH_PLANE) {
+            free_plan(p);
+            return CTP_E_OPTION;
+        }
+        v_is_z = false;
     }
 
     int chosen = path;
     if (chosen == CTP_PATH_AUTO)
-        chosen = geom->ndim == 2 ? CTP_PATH_PLANE : (v_is_z ? CTP_PATH_COLUMN : CTP_PATH_RAY);
+        chosen = curved ? CTP_PATH_RAY
+                        : (geom->ndim == 2 ? CTP_PATH_PLANE
+                                           : (v_is_z ? CTP_PATH_COLUMN : CTP_PATH_RAY));
     if ((chosen == CTP_PATH_COLUMN && (!v_is_z || geom->ndim != 3)) ||
         (chosen == CTP_PATH_PLANE && geom->ndim != 2)) {
         free_plan(p);
@@ -431,6 +466,16 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
         return CTP_E_CUDA;
     }
     p->device_bytes = fbytes + sizeof(unsigned long long);
+    if (curved) {
+        const size_t ob = sizeof(float) * 3 * (size_t)geom->n_u * geom->n_v;
+        if (cudaMalloc(&p->d_offsets, ob) != cudaSuccess ||
+            cudaMemcpy(p->d_offsets, geom->pixel_offsets, ob, cudaMemcpyHostToDevice) !=
+                cudaSuccess) {
+            free_plan(p);
+            return CTP_E_CUDA;
+        }
+        p->device_bytes += ob;
+    }
     if (chosen == CTP_PATH_COLUMN || chosen == CTP_PATH_PLANE) {
         if (chosen == CTP_PATH_COLUMN)
             st = ctp::column_plan_build(ray_params(p), &p->col, &p->d_table, &p->d_work_fwd,
@@ -716,6 +761,7 @@ int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *
     if (plan->n_rays > 0 && (!vol_dev || !weight_dev)) return CTP_E_NULL;
     int st = check_device(plan);
     if (st != CTP_OK) return st;
+    if (plan->d_offsets) return CTP_E_OPTION;  // the chain rule assumes the pitch grid
     if (plan->n_views == 0) return CTP_OK;
     ctp::GeomParams Q;
     Q.cu = (float)(0.5 * (plan->n_u - 1) - plan->offset_u);
@@ -750,7 +796,7 @@ int ctp_fdk(const ctp_plan_t *plan, const float *sino_dev, float *work_dev, floa
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr int kStaticMaxViews = 4096;   // 4096 frames x 96 B = 384 KiB per device
+constexpr int kStaticMaxViews = 4096;   // 4096 frames x 120 B = 480 KiB per device
 constexpr int kStaticMaxDevices = 64;
 constexpr int kStaticChunk = 32;        // frames staged per host-to-device copy
 
@@ -792,6 +838,7 @@ void static_frame(const ctp_geometry *g, const ctp_volume *v, int s, ctp::ViewFr
         F->du[a] = pu / d;
         F->dv[a] = pv / d;
         F->a[a] = g->beam == CTP_DIVERGENT ? ((double)S[a] - o) / d : (double)S[a] / d;
+        F->dn[a] = 0.0;
     }
 }
 
@@ -803,6 +850,7 @@ extern "C" int ctp_forward_static(const ctp_geometry *geom, const ctp_volume *vo
     if (!geom || !vol) return CTP_E_NULL;
     int st = validate(geom, vol);
     if (st != CTP_OK) return st;
+    if (geom->pixel_offsets) return CTP_E_OPTION;  // flat detectors only
     if (geom->n_views > kStaticMaxViews) return CTP_E_LIMIT;
     if (geom->n_views == 0) return CTP_OK;
     if (!vol_dev || !sino_dev) return CTP_E_NULL;

@@ -7,12 +7,16 @@ namespace ctp {
 
 // Per-view frame in CELL coordinates (x, y, z): world X maps to (X - o) / d.
 // Divergent: a = source.  Parallel: a = ray direction (cell units).
-// Pixel (iu, iv) = p00 + iu * du + iv * dv.  Built on the host in float64.
+// Flat detector: pixel (iu, iv) = p00 + iu * du + iv * dv.  Curved detector
+// (per-pixel offsets (t, s, e)): pixel = p00 + t du + s dv + e dn with p00 the
+// detector centre and du, dv, dn the unit axes and normal per unit length.
+// Built on the host in float64.
 struct ViewFrame {
     double a[3];
     double p00[3];
     double du[3];
     double dv[3];
+    double dn[3];
 };
 
 // Launch-time constants of the ray path.
@@ -26,6 +30,7 @@ struct RayParams {
     float min_len;        // segment counter: pieces longer than this (physical units)
     int view0;            // first view of a launch (grid row y handles view view0 + y)
     int view_count;       // views of a launch
+    const float *offsets; // curved detector: (n_v, n_u, 3) per-pixel offsets; else null
 };
 
 }  // namespace ctp

@@ -57,10 +57,18 @@ __device__ __forceinline__ bool slab_setup(const RayParams &P, int view, int iu,
 {
     const ViewFrame &V = P.views[view];
     double X0[3], w[3];
-    const double fu = (double)iu, fv = (double)iv;
+    double fu = (double)iu, fv = (double)iv, fe = 0.0;
+    if (P.offsets) {
+        // curved detector: the pixel's (t, s, e) offsets along du, dv, dn
+        const float *q = P.offsets + 3 * ((long long)iv * P.n_u + iu);
+        fu = (double)q[0];
+        fv = (double)q[1];
+        fe = (double)q[2];
+    }
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
         double pix = __fma_rn(fv, V.dv[a], __fma_rn(fu, V.du[a], V.p00[a]));
+        if (P.offsets) pix = __fma_rn(fe, V.dn[a], pix);
         if (P.beam == 1) {
             X0[a] = V.a[a];
             w[a] = __dsub_rn(pix, V.a[a]);

@@ -89,6 +89,19 @@ typedef struct ctp_geometry {
     const float *det_v;       /* HOST (n_views, 3) unit v axis (2-D: any vector not along u) */
     double pitch_u, pitch_v;  /* detector pitch (physical units) */
     double offset_u, offset_v;/* detector-centre offset in pixels */
+    const float *pixel_offsets; /* NULL: flat detector (the pitch grid above).  Else a
+                                 curved detector: HOST (n_v, n_u, 3) per-pixel (t, s, e),
+                                 shared by all views: pixel (iu, iv) of view k sits at
+                                 det_centre + t det_u + s det_v + e n, n = the unit
+                                 normal (det_u x det_v) / |det_u x det_v| (the pages'
+                                 surface composition: point = centre + tangent u +
+                                 vertical v + depth n, release diff 2.4.1 -> 2.4.2,
+                                 kernels/surface_geometry.py compose_surface); pitches
+                                 and offsets are then unused.  Such plans take the ray
+                                 path; ctp_forward_static, the analytical operators and
+                                 ctp_geometry_vjp refuse them (CTP_E_OPTION /
+                                 CTP_E_GEOMETRY).  Offsets must be finite
+                                 (CTP_E_NONFINITE). */
 } ctp_geometry;
 
 typedef struct ctp_volume {
@@ -185,7 +198,7 @@ int ctp_backward_host(ctp_plan_t *plan, const float *sino_host, float *vol_host,
  * codes).  vol_dev / sino_dev: device float32 buffers as for ctp_forward (may be
  * NULL when n_views is 0).  stream: a cudaStream_t (NULL = default stream).
  * Scratch: the per-view frame table lives in a fixed device array of
- * 4096 views (384 KiB) that every device loading the library holds until exit;
+ * 4096 views (480 KiB) that every device loading the library holds until exit;
  * n_views above 4096 returns CTP_E_LIMIT, and so does a current device ordinal
  * of 64 or more.  The first call on a device looks the array up
  * (cudaGetSymbolAddress); make that first call before any stream capture.

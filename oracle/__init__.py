@@ -71,6 +71,7 @@ class _Ctx(ctypes.Structure):
         ("offset_u", ctypes.c_double), ("offset_v", ctypes.c_double),
         ("n", ctypes.c_int * 3), ("pad_", ctypes.c_int),
         ("d", ctypes.c_double * 3), ("o", ctypes.c_double * 3),
+        ("offsets", ctypes.c_void_p),
     ]
 
 
@@ -109,7 +110,7 @@ class Scan:
     the world (x, y, z) of the min corner of voxel (0, 0, 0)."""
 
     def __init__(self, beam, src, det_centre, det_u, det_v, n_u, n_v, pitch_u, pitch_v,
-                 shape, spacing, origin, offset_u=0.0, offset_v=0.0, ndim=3):
+                 shape, spacing, origin, offset_u=0.0, offset_v=0.0, ndim=3, pixel_offsets=None):
         self.beam = beam
         self.ndim = int(ndim)
         self.pitch_u, self.pitch_v = float(pitch_u), float(pitch_v)
@@ -132,6 +133,12 @@ class Scan:
         c.n[0], c.n[1], c.n[2] = W, H, D
         c.d[0], c.d[1], c.d[2] = dx, dy, dz
         c.o[0], c.o[1], c.o[2] = self.origin
+        # curved detector: per-pixel (tangent, vertical, depth) offsets (n_v, n_u, 3)
+        self.pixel_offsets = None
+        if pixel_offsets is not None:
+            self.pixel_offsets = np.ascontiguousarray(pixel_offsets, dtype=np.float32).reshape(
+                self.n_v, self.n_u, 3)
+            c.offsets = self.pixel_offsets.ctypes.data
         self._ctx = c
 
     @classmethod

@@ -52,6 +52,7 @@ typedef struct {
     int pad_;
     double d[3];         /* spacing along x, y, z */
     double o[3];         /* world position of the min corner of cell (0, 0, 0) */
+    const float *offsets;  /* NULL (flat detector) or (n_v, n_u, 3) per-pixel offsets */
 } ora_ctx;
 
 static int ora_threads(int requested)
@@ -65,7 +66,12 @@ static int ora_threads(int requested)
 #endif
 }
 
-/* The ray of detector sample `ray` (view-major, then v, then u). */
+/* The ray of detector sample `ray` (view-major, then v, then u).  Flat
+ * detector: pixel = centre + a u + b v with a, b the pitch grid.  Curved
+ * (per-pixel offsets (t, s, e), shared by all views; the pages' surface
+ * composition, diffct 2.4.1 -> 2.4.2, kernels/surface_geometry.py
+ * `compose_surface`: point = centre + tangent u + vertical v + depth n):
+ * pixel = centre + t u + s v + e n, n = (u x v) / |u x v|. */
 static void ora_ray(const ora_ctx *c, long ray, double X0[3], double r[3],
                     double *tlo, double *thi)
 {
@@ -73,13 +79,24 @@ static void ora_ray(const ora_ctx *c, long ray, double X0[3], double r[3],
     long view = ray / per_view;
     long pix = ray % per_view;
     long iv = pix / c->n_u, iu = pix % c->n_u;
-    double a = ((double)iu - 0.5 * (double)(c->n_u - 1) + c->offset_u) * c->pitch_u;
-    double b = ((double)iv - 0.5 * (double)(c->n_v - 1) + c->offset_v) * c->pitch_v;
     const float *S = c->src + 3 * view, *C = c->det_centre + 3 * view;
     const float *U = c->det_u + 3 * view, *V = c->det_v + 3 * view;
     double P[3];
-    for (int ax = 0; ax < 3; ++ax)
-        P[ax] = (double)C[ax] + a * (double)U[ax] + b * (double)V[ax];
+    if (c->offsets) {
+        const float *q = c->offsets + 3 * pix;
+        double u[3] = {U[0], U[1], U[2]}, v[3] = {V[0], V[1], V[2]};
+        double n[3] = {u[1] * v[2] - u[2] * v[1], u[2] * v[0] - u[0] * v[2],
+                       u[0] * v[1] - u[1] * v[0]};
+        double nn = sqrt(n[0] * n[0] + n[1] * n[1] + n[2] * n[2]);
+        for (int ax = 0; ax < 3; ++ax)
+            P[ax] = (double)C[ax] + (double)q[0] * u[ax] + (double)q[1] * v[ax] +
+                    (double)q[2] * (n[ax] / nn);
+    } else {
+        double a = ((double)iu - 0.5 * (double)(c->n_u - 1) + c->offset_u) * c->pitch_u;
+        double b = ((double)iv - 0.5 * (double)(c->n_v - 1) + c->offset_v) * c->pitch_v;
+        for (int ax = 0; ax < 3; ++ax)
+            P[ax] = (double)C[ax] + a * (double)U[ax] + b * (double)V[ax];
+    }
     if (c->beam == 1) {
         for (int ax = 0; ax < 3; ++ax) {
             X0[ax] = (double)S[ax];
@@ -455,6 +472,7 @@ static int ora_solve3(const double m0[3], const double m1[3], const double m2[3]
 int ora_backward_voxels(const ora_ctx *c, const float *sino, const long *voxels, long count,
                         double *out, int nthreads)
 {
+    if (c->offsets) return 2;  /* the candidate-ray solve assumes a flat detector */
     int T = ora_threads(nthreads);
 #pragma omp parallel for num_threads(T) schedule(dynamic, 1)
     for (long q = 0; q < count; ++q) {
@@ -647,6 +665,7 @@ int ora_trace_ray(const ora_ctx *c, long ray, long *cells, double *lens)
 int ora_geometry_vjp(const ora_ctx *c, const float *vol, const float *w, double *out,
                      int nthreads)
 {
+    if (c->offsets) return 2;  /* flat detectors only */
     int T = ora_threads(nthreads);
     int B = ora_buf_len(c);
     long per_view = (long)c->n_u * c->n_v;
