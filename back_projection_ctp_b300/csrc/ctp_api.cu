@@ -36,6 +36,7 @@ struct ctp_plan {
     std::vector<ctp::ViewFrame> frames;     // host copy
     ctp::ViewFrame *d_frames = nullptr;     // device copy
     float *d_offsets = nullptr;             // curved detector: (n_v, n_u, 3) pixel offsets
+    double4 *d_columns = nullptr;           // curved detector, column path: (t, e, s0, ds)
     unsigned long long *d_counter = nullptr;
     // column and plane paths
     ctp::ColumnPlan col{};
@@ -95,6 +96,7 @@ ctp::RayParams ray_params(const ctp_plan_t *plan)
     P.view0 = 0;
     P.view_count = plan->n_views;
     P.offsets = plan->d_offsets;
+    P.columns = plan->d_columns;
     return P;
 }
 
@@ -201,6 +203,7 @@ void free_plan(ctp_plan_t *p)
     cudaDeviceSynchronize();
     cudaFree(p->d_frames);
     cudaFree(p->d_offsets);
+    cudaFree(p->d_columns);
     cudaFree(p->d_counter);
     cudaFree(p->d_table);
     cudaFree(p->d_work_fwd);
@@ -437,18 +440,39 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
         }
         if (!(V[0] == 0.0f && V[1] == 0.0f && V[2] != 0.0f)) v_is_z = false;
     }
+    // A curved detector runs on the column path when its columns are straight
+    // vertical lines of evenly spaced pixels (tangent and depth offsets the same
+    // in every row, vertical offsets affine in the row to 1e-6 of the column's
+    // span): circular / helical scans with cylindrical detectors.  Other curved
+    // detectors run on the ray path; the plane path assumes the pitch grid.
+    std::vector<double4> colq;
     if (curved) {
-        // the column and plane paths assume the pitch grid
-        if (path == CTP_PATH_COLUMN || path == CTP_PATH_PLANE) {
+        bool columnar = geom->ndim == 3 && geom->n_v >= 2;
+        for (int iu = 0; iu < geom->n_u && columnar; ++iu) {
+            const float *q0 = geom->pixel_offsets + 3 * (long long)iu;
+            const float *q1 = q0 + 3LL * geom->n_u;
+            const double s0 = q0[1], ds = (double)q1[1] - (double)q0[1];
+            const double span = std::fabs(ds) * (geom->n_v - 1);
+            for (int iv = 1; iv < geom->n_v && columnar; ++iv) {
+                const float *q = q0 + 3LL * geom->n_u * iv;
+                columnar = q[0] == q0[0] && q[2] == q0[2] &&
+                           std::fabs((double)q[1] - (s0 + ds * iv)) <= 1e-6 * span;
+            }
+            colq.push_back(make_double4(q0[0], q0[2], s0, ds));
+        }
+        if (!columnar) {
+            colq.clear();
+            v_is_z = false;
+        }
+        if ((path == CTP_PATH_COLUMN && !v_is_z) || path == CTP_PATH_PLANE) {
             free_plan(p);
             return CTP_E_OPTION;
         }
-        v_is_z = false;
     }
 
     int chosen = path;
     if (chosen == CTP_PATH_AUTO)
-        chosen = curved ? CTP_PATH_RAY
+        chosen = curved ? (v_is_z ? CTP_PATH_COLUMN : CTP_PATH_RAY)
                         : (geom->ndim == 2 ? CTP_PATH_PLANE
                                            : (v_is_z ? CTP_PATH_COLUMN : CTP_PATH_RAY));
     if ((chosen == CTP_PATH_COLUMN && (!v_is_z || geom->ndim != 3)) ||
@@ -475,6 +499,16 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
             return CTP_E_CUDA;
         }
         p->device_bytes += ob;
+        if (chosen == CTP_PATH_COLUMN) {
+            const size_t cb = sizeof(double4) * colq.size();
+            if (cudaMalloc(&p->d_columns, cb) != cudaSuccess ||
+                cudaMemcpy(p->d_columns, colq.data(), cb, cudaMemcpyHostToDevice) !=
+                    cudaSuccess) {
+                free_plan(p);
+                return CTP_E_CUDA;
+            }
+            p->device_bytes += cb;
+        }
     }
     if (chosen == CTP_PATH_COLUMN || chosen == CTP_PATH_PLANE) {
         if (chosen == CTP_PATH_COLUMN)
@@ -489,10 +523,13 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
             cudaFree(p->d_table);
             cudaFree(p->d_work_fwd);
             cudaFree(p->d_work_bwd);
+            cudaFree(p->d_columns);
             p->d_table = nullptr;
             p->d_work_fwd = nullptr;
             p->d_work_bwd = nullptr;
-            p->device_bytes = fbytes + sizeof(unsigned long long);
+            p->d_columns = nullptr;
+            p->device_bytes = fbytes + sizeof(unsigned long long) +
+                              (curved ? sizeof(float) * 3 * (size_t)geom->n_u * geom->n_v : 0);
             p->path = CTP_PATH_RAY;
             st = CTP_OK;
         }

@@ -80,9 +80,19 @@ __global__ void column_setup_kernel(RayParams P, ColumnTrace *__restrict__ T,
     C.pad_ = 0;
     C.Z0 = C.ZD = C.B0 = C.BD = 0;
 
-    double P0[3];
+    // pixel of row 0 and the z step per row: the pitch grid, or a curved
+    // detector's column (t, e fixed, s = s0 + iv ds; frames hold unit axes)
+    double P0[3], dvz = V.dv[2];
+    if (P.columns) {
+        const double4 q = P.columns[iu];
 #pragma unroll
-    for (int a = 0; a < 3; ++a) P0[a] = __fma_rn((double)iu, V.du[a], V.p00[a]);
+        for (int a = 0; a < 3; ++a)
+            P0[a] = __fma_rn(q.y, V.dn[a], __fma_rn(q.z, V.dv[a], __fma_rn(q.x, V.du[a], V.p00[a])));
+        dvz = __dmul_rn(q.w, V.dv[2]);
+    } else {
+#pragma unroll
+        for (int a = 0; a < 3; ++a) P0[a] = __fma_rn((double)iu, V.du[a], V.p00[a]);
+    }
     double X0[2], w[2];
     if (P.beam == 1) {
         for (int a = 0; a < 2; ++a) {
@@ -170,12 +180,12 @@ __global__ void column_setup_kernel(RayParams P, ColumnTrace *__restrict__ T,
     if (P.beam == 1) {
         const double wz0 = __dsub_rn(P0[2], V.a[2]);
         zc = __fma_rn(lam, wz0, V.a[2]);
-        zd = __dmul_rn(lam, V.dv[2]);
+        zd = __dmul_rn(lam, dvz);
         bc = __dmul_rn(wz0, inv);
-        bd = __dmul_rn(V.dv[2], inv);
+        bd = __dmul_rn(dvz, inv);
     } else {
         zc = __fma_rn(lam, V.a[2], P0[2]);
-        zd = V.dv[2];
+        zd = dvz;
         bc = __dmul_rn(V.a[2], inv);
         bd = 0.0;
     }

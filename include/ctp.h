@@ -97,11 +97,15 @@ typedef struct ctp_geometry {
                                  surface composition: point = centre + tangent u +
                                  vertical v + depth n, release diff 2.4.1 -> 2.4.2,
                                  kernels/surface_geometry.py compose_surface); pitches
-                                 and offsets are then unused.  Such plans take the ray
-                                 path; ctp_forward_static, the analytical operators and
-                                 ctp_geometry_vjp refuse them (CTP_E_OPTION /
-                                 CTP_E_GEOMETRY).  Offsets must be finite
-                                 (CTP_E_NONFINITE). */
+                                 and offsets are then unused.  3-D scans whose every
+                                 view has det_v = +-z and whose columns are straight
+                                 (t and e the same in every row, s affine in the row
+                                 to 1e-6 of the column's span: cylindrical detectors)
+                                 may take the column path; others take the ray path;
+                                 the plane path is refused.  ctp_forward_static, the
+                                 analytical operators and ctp_geometry_vjp refuse
+                                 curved detectors (CTP_E_OPTION / CTP_E_GEOMETRY).
+                                 Offsets must be finite (CTP_E_NONFINITE). */
 } ctp_geometry;
 
 typedef struct ctp_volume {

@@ -45,15 +45,42 @@ def _pair(torch, ctp, plan, vol, y):
     return d_s.cpu().numpy(), d_g.cpu().numpy()
 
 
-def test_cylindrical_detector_matches_oracle(torch, ctp, oracle_mod):
+@pytest.mark.parametrize("path", ["auto", "ray"])
+def test_cylindrical_detector_matches_oracle(torch, ctp, oracle_mod, path):
+    """A cylindrical detector (columns straight and vertical, rows evenly spaced)
+    takes the column path under AUTO; both paths match the oracle."""
     off = _cylinder_offsets(53, 41, 1000.0, 0.0094, 9.4)
     w, scan, g, v = _cone_scan(oracle_mod, ctp, off, 53, 41)
+    plan = ctp.ctp_plan(g, v, path)
+    assert plan.path == ("column" if path == "auto" else "ray")
+    vol = ci.phantom(w)
+    amb = oracle_mod.ambiguous(scan)
+    y = np.where(amb, np.float32(0),
+                 np.random.default_rng(7).standard_normal(scan.sino_shape).astype(np.float32))
+    p, gg = _pair(torch, ctp, plan, vol, y)
+    p_ref = oracle_mod.forward(scan, vol).reshape(scan.sino_shape)
+    assert rel_l2(p[~amb], p_ref[~amb]) <= TOL_FORWARD
+    assert rel_l2(gg, oracle_mod.backward(scan, y.ravel())) <= TOL_BACKWARD
+    assert abs(ctp.ctp_segment_count(plan) - oracle_mod.segment_count(scan)) <= \
+        1e-6 * oracle_mod.segment_count(scan)
+
+
+def test_irregular_curved_detector_takes_the_ray_path(torch, ctp, oracle_mod):
+    """Tangent offsets that vary down a column: no column structure, so AUTO takes
+    the ray path and an explicit column request is refused; the ray path matches
+    the oracle."""
+    off = _cylinder_offsets(31, 25, 1000.0, 0.015, 12.0)
+    off[:, :, 0] += np.linspace(-3.0, 3.0, 25, dtype=np.float32)[:, None]
+    w, scan, g, v = _cone_scan(oracle_mod, ctp, off, 31, 25)
+    with pytest.raises(ctp.CtpError) as e:
+        ctp.ctp_plan(g, v, "column")
+    assert e.value.status == 11
     plan = ctp.ctp_plan(g, v)
     assert plan.path == "ray"
     vol = ci.phantom(w)
     amb = oracle_mod.ambiguous(scan)
     y = np.where(amb, np.float32(0),
-                 np.random.default_rng(7).standard_normal(scan.sino_shape).astype(np.float32))
+                 np.random.default_rng(9).standard_normal(scan.sino_shape).astype(np.float32))
     p, gg = _pair(torch, ctp, plan, vol, y)
     p_ref = oracle_mod.forward(scan, vol).reshape(scan.sino_shape)
     assert rel_l2(p[~amb], p_ref[~amb]) <= TOL_FORWARD
@@ -77,10 +104,9 @@ def test_flat_offsets_equal_the_flat_plan(torch, ctp, oracle_mod):
 def test_calls_that_refuse_curved_detectors(torch, ctp, oracle_mod):
     off = _cylinder_offsets(9, 7, 1000.0, 0.0094, 9.4)
     w, scan, g, v = _cone_scan(oracle_mod, ctp, off, 9, 7, K=3)
-    for path in ("column", "plane"):
-        with pytest.raises(ctp.CtpError) as e:
-            ctp.ctp_plan(g, v, path)
-        assert e.value.status == 11
+    with pytest.raises(ctp.CtpError) as e:
+        ctp.ctp_plan(g, v, "plane")
+    assert e.value.status == 11
     plan = ctp.ctp_plan(g, v)
     vol = torch.zeros(plan.vol_shape, device="cuda")
     sino = torch.zeros(plan.sino_shape, device="cuda")
