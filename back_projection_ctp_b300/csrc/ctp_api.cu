@@ -36,7 +36,7 @@ struct ctp_plan {
     std::vector<ctp::ViewFrame> frames;     // host copy
     ctp::ViewFrame *d_frames = nullptr;     // device copy
     float *d_offsets = nullptr;             // curved detector: (n_v, n_u, 3) pixel offsets
-    double4 *d_columns = nullptr;           // curved detector, column path: (t, e, s0, ds)
+    ctp::ColumnOffsets *d_columns = nullptr;  // curved detector, column path: per column
     unsigned long long *d_counter = nullptr;
     // column and plane paths
     ctp::ColumnPlan col{};
@@ -333,6 +333,14 @@ int fdk_setup(ctp_plan_t *p, const ctp_geometry *g, const ctp_volume *v)
     return CTP_OK;
 }
 
+// CTP_GEOMETRY_RAY = 1 runs the geometry gradients on the ray walk for every
+// plan (a cross-check of the column walk).
+bool column_gvjp_disabled()
+{
+    const char *env = getenv("CTP_GEOMETRY_RAY");
+    return env && env[0] == '1';
+}
+
 int fdk_check(const ctp_plan_t *plan)
 {
     const int st = check_device(plan);
@@ -445,7 +453,7 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
     // in every row, vertical offsets affine in the row to 1e-6 of the column's
     // span): circular / helical scans with cylindrical detectors.  Other curved
     // detectors run on the ray path; the plane path assumes the pitch grid.
-    std::vector<double4> colq;
+    std::vector<ctp::ColumnOffsets> colq;
     if (curved) {
         bool columnar = geom->ndim == 3 && geom->n_v >= 2;
         for (int iu = 0; iu < geom->n_u && columnar; ++iu) {
@@ -458,7 +466,7 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
                 columnar = q[0] == q0[0] && q[2] == q0[2] &&
                            std::fabs((double)q[1] - (s0 + ds * iv)) <= 1e-6 * span;
             }
-            colq.push_back(make_double4(q0[0], q0[2], s0, ds));
+            colq.push_back(ctp::ColumnOffsets{q0[0], q0[2], s0, ds});
         }
         if (!columnar) {
             colq.clear();
@@ -500,7 +508,7 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
         }
         p->device_bytes += ob;
         if (chosen == CTP_PATH_COLUMN) {
-            const size_t cb = sizeof(double4) * colq.size();
+            const size_t cb = sizeof(ctp::ColumnOffsets) * colq.size();
             if (cudaMalloc(&p->d_columns, cb) != cudaSuccess ||
                 cudaMemcpy(p->d_columns, colq.data(), cb, cudaMemcpyHostToDevice) !=
                     cudaSuccess) {
@@ -805,8 +813,16 @@ int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *
     Q.cv = (float)(0.5 * (plan->n_v - 1) - plan->offset_v);
     Q.pitch_u = (float)plan->pitch_u;
     Q.pitch_v = (float)plan->pitch_v;
-    return ctp::geometry_vjp(ray_params(plan), Q, vol_dev, weight_dev, grad_dev,
-                             (cudaStream_t)stream) ? CTP_E_CUDA : CTP_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (plan->path == CTP_PATH_COLUMN && !column_gvjp_disabled()) {
+        // the column walk reads the plan's padded z-fastest working copy
+        if ((st = forward_in(plan, vol_dev, s)) != CTP_OK) return st;
+        return ctp::column_geometry_vjp(ray_params(plan), Q, (const ctp::ColumnTrace *)plan->d_table,
+                                        plan->d_work_fwd, weight_dev, grad_dev, s)
+                   ? CTP_E_CUDA : CTP_OK;
+    }
+    return ctp::geometry_vjp(ray_params(plan), Q, vol_dev, weight_dev, grad_dev, s) ? CTP_E_CUDA
+                                                                                   : CTP_OK;
 }
 
 int ctp_fdk(const ctp_plan_t *plan, const float *sino_dev, float *work_dev, float *vol_dev,

@@ -30,6 +30,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "ctp_column.cuh"
 #include "ctp_internal.h"
 #include "ctp_ray.cuh"
 
@@ -224,6 +225,181 @@ __global__ void __launch_bounds__(TU *TV) geometry_vjp_kernel(RayParams P, GeomP
         for (int q = 0; q < kWarps; ++q) s += (double)part[q][threadIdx.x];
         atomicAdd(out + 12 * (long long)view + threadIdx.x, s);
     }
+}
+
+// Column path (3-D scans whose v axis is +-z): the same crossing sums for the R
+// rows a thread owns, over the column's shared xy walk (the b crossing is
+// uniform across the warp) and each row's own z crossings, on the padded
+// z-fastest working copy of the volume (zero halo in x and y; z validity per
+// access).  t of the p coordinate is shared by the column's rows.
+template <int R>
+__global__ void __launch_bounds__(256) column_gvjp_kernel(RayParams P, GeomParams Q,
+                                                          const ColumnTrace *__restrict__ T,
+                                                          const float *__restrict__ zvol,
+                                                          const float *__restrict__ wsino,
+                                                          double *__restrict__ out)
+{
+    __shared__ float part[kColumnsPerBlock][12];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int iu = blockIdx.x * kColumnsPerBlock + warp;
+    const int view = P.view0 + (int)blockIdx.y;
+    float g[12];
+#pragma unroll
+    for (int m = 0; m < 12; ++m) g[m] = 0.0f;
+    const ColumnTrace C = iu < P.n_u ? T[(long long)view * P.n_u + iu] : ColumnTrace{};
+    if (iu < P.n_u && C.k0 <= C.k1) {
+        // column constants in float64: axes, the t map of the p coordinate, r
+        const ViewFrame &V = P.views[view];
+        double P0[3];
+#pragma unroll
+        for (int a = 0; a < 3; ++a) P0[a] = __fma_rn((double)iu, V.du[a], V.p00[a]);
+        double X0[2], w[2];
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+            X0[a] = P.beam == 1 ? V.a[a] : P0[a];
+            w[a] = P.beam == 1 ? __dsub_rn(P0[a], V.a[a]) : V.a[a];
+        }
+        const int p = fabs(w[0]) >= fabs(w[1]) ? 0 : 1;
+        const double awp = fabs(w[p]);
+        const double Ap = w[p] < 0.0 ? __dsub_rn((double)P.n[p], X0[p]) : X0[p];
+        const float tinv = (float)__ddiv_rn(1.0, awp);
+        const float t0 = (float)__ddiv_rn(__dsub_rn((double)C.k0, Ap), awp);
+        const float rx = (float)__dmul_rn(w[0], P.spacing[0]);
+        const float ry = (float)__dmul_rn(w[1], P.spacing[1]);
+        const double z0 = P.beam == 1 ? __dsub_rn(P0[2], V.a[2]) : V.a[2];
+        const double zstep = P.beam == 1 ? V.dv[2] : 0.0;
+        const float alpha = ((float)iu - Q.cu) * Q.pitch_u;
+
+        const int row0 = blockIdx.z * 32 * R + lane;
+        RowZ Z[R];
+        float wr[R], acc[R], fprev[R], dfp[R], dfb[R], dfz[R], dtp[R], dtb[R], dtz[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int iv = row0 + 32 * r;
+            wr[r] = iv < P.n_v ? wsino[((long long)view * P.n_v + iv) * P.n_u + iu] : 0.0f;
+            Z[r] = wr[r] != 0.0f ? column_row_setup(P, C, iv) : column_row_idle();
+            acc[r] = fprev[r] = dfp[r] = dfb[r] = dfz[r] = dtp[r] = dtb[r] = dtz[r] = 0.0f;
+        }
+        bool any = false;
+#pragma unroll
+        for (int r = 0; r < R; ++r) any |= wr[r] != 0.0f;
+        any = __any_sync(0xffffffffu, any);  // the warp shares the column
+        const unsigned nz = (unsigned)P.n[2];
+        uint32_t fb = C.fb;
+        int xy = C.addr_xy;
+        for (int k = C.k0; any && k <= C.k1; ++k) {
+            const float lo = k == C.k0 ? C.tlo : 0.0f;
+            const float hi = k == C.k1 ? C.thi : 1.0f;
+            const uint32_t gb = fb + C.bb;
+            const bool cb = gb < fb;
+            const float tb = cb ? fmaxf(__fmaf_rn(-__uint2float_rn(gb), C.ib, 1.0f), 0.0f) : 2.0f;
+            const float tk = __fmaf_rn((float)(k - C.k0), tinv, t0);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t gz = Z[r].fz + Z[r].bz;
+                const bool cz = gz < Z[r].fz;
+                const float tz =
+                    cz ? fmaxf(__fmaf_rn(-__uint2float_rn(gz), Z[r].ibz, 1.0f), 0.0f) : 2.0f;
+                const int za = Z[r].zoff, z1 = za + Z[r].sz;
+                const bool bfirst = tb < tz;
+                const float x1 = fminf(tb, tz), x2 = fmaxf(tb, tz);
+                // cells: A before both crossings, B after the first, C after both
+                const int zb = bfirst ? za : (cz ? z1 : za), xyb = bfirst ? xy + C.sb : xy;
+                const int zc = cz ? z1 : za, xyc = cb ? xy + C.sb : xy;
+                const float vA = (unsigned)za < nz ? __ldg(zvol + xy + za) : 0.0f;
+                const float vB = (unsigned)zb < nz ? __ldg(zvol + xyb + zb) : 0.0f;
+                const float vC = (unsigned)zc < nz ? __ldg(zvol + xyc + zc) : 0.0f;
+                const float e1 = fminf(fmaxf(x1, lo), hi), e2 = fminf(fmaxf(x2, lo), hi);
+                acc[r] = __fmaf_rn(__fsub_rn(e1, lo), vA,
+                                   __fmaf_rn(__fsub_rn(e2, e1), vB,
+                                             __fmaf_rn(__fsub_rn(hi, e2), vC, acc[r])));
+                if (k > C.k0 || C.tlo == 0.0f) {
+                    const float j = fprev[r] - vA;
+                    dfp[r] += j;
+                    dtp[r] = __fmaf_rn(j, tk, dtp[r]);
+                }
+                if (x1 > lo && x1 < hi) {
+                    const float j = vA - vB, t = __fmaf_rn(x1, tinv, tk);
+                    if (bfirst) {
+                        dfb[r] += j;
+                        dtb[r] = __fmaf_rn(j, t, dtb[r]);
+                    } else {
+                        dfz[r] += j;
+                        dtz[r] = __fmaf_rn(j, t, dtz[r]);
+                    }
+                }
+                if (x2 > lo && x2 < hi) {
+                    const float j = vB - vC, t = __fmaf_rn(x2, tinv, tk);
+                    if (bfirst) {
+                        dfz[r] += j;
+                        dtz[r] = __fmaf_rn(j, t, dtz[r]);
+                    } else {
+                        dfb[r] += j;
+                        dtb[r] = __fmaf_rn(j, t, dtb[r]);
+                    }
+                }
+                fprev[r] = x2 < hi ? vC : (x1 < hi ? vB : vA);
+                Z[r].fz = gz;
+                if (cz) Z[r].zoff = z1;
+            }
+            xy += cb ? C.sp + C.sb : C.sp;
+            fb = gb;
+        }
+        const float tend = __fmaf_rn((float)(C.k1 + 1 - C.k0), tinv, t0);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (wr[r] == 0.0f) continue;
+            if (C.thi == 1.0f) {
+                dfp[r] += fprev[r];
+                dtp[r] = __fmaf_rn(fprev[r], tend, dtp[r]);
+            }
+            const int iv = row0 + 32 * r;
+            const float rz = (float)(__fma_rn((double)iv, zstep, z0) * P.spacing[2]);
+            const float rv[3] = {rx, ry, rz};
+            const float rn2 = rx * rx + ry * ry + rz * rz, rn = sqrtf(rn2);
+            const float pval = acc[r] * column_row_ell(P, C, Z[r].bz);
+            const float beta = ((float)iv - Q.cv) * Q.pitch_v;
+#pragma unroll
+            for (int a = 0; a < 3; ++a) {
+                const float df = a == 2 ? dfz[r] : (a == p ? dfp[r] : dfb[r]);
+                const float dt = a == 2 ? dtz[r] : (a == p ? dtp[r] : dtb[r]);
+                const float ra = rv[a];
+                const float gx = ra != 0.0f ? -rn * df / ra : 0.0f;
+                const float gr = (ra != 0.0f ? -rn * dt / ra : 0.0f) + pval * ra / rn2;
+                const float dsrc = P.beam == 1 ? gx - gr : gr;
+                const float dpix = P.beam == 1 ? gr : gx;
+                g[a] += wr[r] * dsrc;
+                g[3 + a] += wr[r] * dpix;
+                g[6 + a] += wr[r] * alpha * dpix;
+                g[9 + a] += wr[r] * beta * dpix;
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < 12; ++m) {
+        float v = g[m];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+        if (lane == 0) part[warp][m] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < 12) {
+        double sum = 0.0;
+#pragma unroll
+        for (int q = 0; q < kColumnsPerBlock; ++q) sum += (double)part[q][threadIdx.x];
+        atomicAdd(out + 12 * (long long)view + threadIdx.x, sum);
+    }
+}
+
+inline int column_geometry_vjp(const RayParams &P, const GeomParams &Q, const ColumnTrace *T,
+                               const float *zvol, const float *w, double *out, cudaStream_t s)
+{
+    if (cudaMemsetAsync(out, 0, sizeof(double) * 12 * (size_t)(P.n_views > 0 ? P.n_views : 0), s) !=
+        cudaSuccess)
+        return 9;
+    if (P.view_count <= 0) return 0;
+    column_gvjp_kernel<2><<<column_grid(P, 2), 256, 0, s>>>(P, Q, T, zvol, w, out);
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 
 inline int geometry_vjp(const RayParams &P, const GeomParams &Q, const float *vol, const float *w,

@@ -3,8 +3,6 @@
 
 #include <cstdint>
 
-#include <vector_types.h>
-
 namespace ctp {
 
 // Per-view frame in CELL coordinates (x, y, z): world X maps to (X - o) / d.
@@ -21,6 +19,12 @@ struct ViewFrame {
     double dn[3];
 };
 
+// Curved detector with column structure: column iu's tangent and depth offsets
+// (the same in every row), the vertical offset of row 0 and the step per row.
+struct ColumnOffsets {
+    double t, e, s0, ds;
+};
+
 // Launch-time constants of the ray path.
 struct RayParams {
     const ViewFrame *views;
@@ -33,10 +37,7 @@ struct RayParams {
     int view0;            // first view of a launch (grid row y handles view view0 + y)
     int view_count;       // views of a launch
     const float *offsets; // curved detector: (n_v, n_u, 3) per-pixel offsets; else null
-    // curved detector with column structure (column path): per column iu the
-    // tangent and depth offsets t, e (the same in every row), the vertical offset
-    // s0 of row 0 and the step ds per row; else null
-    const double4 *columns;
+    const ColumnOffsets *columns;  // curved detector on the column path: per column; else null
 };
 
 }  // namespace ctp

@@ -41,7 +41,12 @@ def _weights(oracle_mod, scan, seed):
 
 
 @pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
-def test_small_cases_match_oracle(torch, ctp, oracle_mod, idx):
+@pytest.mark.parametrize("walk", ["auto", "ray"])
+def test_small_cases_match_oracle(torch, ctp, oracle_mod, monkeypatch, idx, walk):
+    """AUTO runs the column walk on the 3-D circular / helical scans and the ray
+    walk elsewhere; CTP_GEOMETRY_RAY=1 forces the ray walk."""
+    if walk == "ray":
+        monkeypatch.setenv("CTP_GEOMETRY_RAY", "1")
     w = SMALL[idx]
     f = ci.frames(w)
     scan = oracle_mod.Scan.from_workload(w, f)
