@@ -68,10 +68,12 @@ typedef enum ctp_beam { CTP_PARALLEL = 0, CTP_DIVERGENT = 1 } ctp_beam;
 
 /* Traversal path.  AUTO picks PLANE for 2-D scans (rays in the slice plane),
  * COLUMN for 3-D scans whose detector v axis is exactly +-z in every view (then
- * all rays of a detector column share one xy trace), else RAY; it falls back to
- * RAY when a scan does not meet PLANE's or COLUMN's conditions (rays leaving the
- * slice; rows crossing more than one z plane per slab).  All paths compute the
- * same operator; they differ in work layout only. */
+ * all rays of a detector column share one xy trace; curved detectors qualify
+ * when their columns are straight, see pixel_offsets), else RAY; it falls back
+ * to RAY when a scan does not meet PLANE's or COLUMN's conditions (rays leaving
+ * the slice; rows crossing more than one z plane per slab).  An explicit PLANE
+ * or COLUMN request for a scan outside its class returns CTP_E_OPTION.  All
+ * paths compute the same operator; they differ in work layout only. */
 typedef enum ctp_path {
     CTP_PATH_AUTO = 0,
     CTP_PATH_RAY = 1,
