@@ -415,8 +415,9 @@ struct ColumnCount {
 
 constexpr int kColumnsPerBlock = 8;  // 8 warps: 8 columns, each 32 * R rows
 
-// Rows a thread owns: iv = band * 32R + 32 r + lane, r < R (each load or atomic
-// instruction then covers 32 adjacent rows).
+// Rows a forward thread owns: iv = band * 32R + 32 r + lane, r < R (each load
+// instruction then covers 32 adjacent rows; the backward interleaves its rows,
+// see column_row_slot).
 template <int R>
 __global__ void __launch_bounds__(256, 5) column_forward_kernel(RayParams P,
                                                              const ColumnTrace *__restrict__ T,
