@@ -40,7 +40,8 @@ detector, written in physical detector units):
   with tau = pitch_u, cw = SDD_k / |P_pix - a_k| the cosine of the ray to the
   normal (parallel: 1), w_k caller-given view weights (full 2 pi scans: pi / K,
   i.e. half the angular step), and h the ramp kernel with frequency response
-  |omega| in radians per unit length (Ram-Lak) or |omega| |sinc| (Shepp-Logan).
+  |omega| in radians per unit length times a window (none: Ram-Lak; sinc:
+  Shepp-Logan; cosine, Hamming, Hann).
 
 With these, g = gather(filter(p)) is the textbook FBP / FDK estimate of the
 image whose line integrals are p.  What pins it (``tests/test_oracle_fdk_pins.py``):
@@ -57,7 +58,7 @@ import math
 
 import numpy as np
 
-RAMLAK, SHEPP_LOGAN = 0, 1
+RAMLAK, SHEPP_LOGAN, COSINE, HAMMING, HANN = 0, 1, 2, 3, 4
 
 
 def _frames(scan):
@@ -188,18 +189,43 @@ def weighted_backproject_transpose(scan, vol):
     return out
 
 
+def _band_limited_ramp(x, tau):
+    """g(x) = (1 / 2 pi) * integral over |omega| <= pi / tau of |omega| exp(i omega x tau),
+    the band-limited ramp at a (possibly fractional) sample offset x."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.empty_like(x)
+    zero = x == 0
+    xs = np.where(zero, 1.0, x)
+    out[:] = (math.pi * np.sin(math.pi * xs) / xs + (np.cos(math.pi * xs) - 1.0) / xs ** 2) / (
+        math.pi * tau * tau)
+    out[zero] = math.pi / (2.0 * tau * tau)
+    return out
+
+
 def ramp_kernel(n_u, tau, kind=RAMLAK):
     """Spatial ramp kernel h[m], m = -(n_u-1) .. n_u-1 (index m + n_u - 1), in the
-    convention where tau * sum_m h[m] exp(-i omega m tau) -> |omega| (Ram-Lak) or
-    (2 / tau) |sin(omega tau / 2)| (Shepp-Logan) for |omega| <= pi / tau."""
+    convention where tau * sum_m h[m] exp(-i omega m tau) -> H(omega) for
+    |omega| <= pi / tau, with H = |omega| times a window (the pages name Ram-Lak,
+    Shepp-Logan, cosine, Hamming and Hann):
+        Ram-Lak      |omega|
+        Shepp-Logan  (2 / tau) |sin(omega tau / 2)|  = |omega| sinc
+        cosine       |omega| cos(omega tau / 2)
+        Hamming      |omega| (0.54 + 0.46 cos(omega tau))
+        Hann         |omega| (1 + cos(omega tau)) / 2
+    Each is the inverse transform of H: the band-limited ramp g at the sample
+    offsets, or its half-sample / one-sample shifts for the cosine windows."""
     m = np.arange(-(n_u - 1), n_u, dtype=np.float64)
+    g = lambda x: _band_limited_ramp(x, tau)  # noqa: E731
     if kind == RAMLAK:
-        h = np.zeros_like(m)
-        h[m == 0] = math.pi / (2.0 * tau * tau)
-        odd = (np.abs(m) % 2) == 1
-        h[odd] = -2.0 / (math.pi * m[odd] ** 2 * tau * tau)
+        h = g(m)
     elif kind == SHEPP_LOGAN:
         h = -4.0 / (math.pi * tau * tau * (4.0 * m * m - 1.0))
+    elif kind == COSINE:
+        h = 0.5 * (g(m - 0.5) + g(m + 0.5))
+    elif kind == HAMMING:
+        h = 0.54 * g(m) + 0.23 * (g(m - 1.0) + g(m + 1.0))
+    elif kind == HANN:
+        h = 0.5 * g(m) + 0.25 * (g(m - 1.0) + g(m + 1.0))
     else:
         raise ValueError(f"unknown filter {kind}")
     return h
@@ -246,6 +272,62 @@ def filter_sinogram_transpose(scan, q, view_weight=None, kind=RAMLAK):
     w = np.ones(scan.n_views) if view_weight is None else np.asarray(view_weight, np.float64)
     T = _toeplitz(scan, kind)
     return cosine_weights(scan) * (scan.pitch_u * ((q * w[:, None, None]) @ T))
+
+
+def parker(beta, gamma, big_gamma):
+    """Parker's short-scan weight of the ray with scan angle beta in [0, pi + 2 Gamma]
+    and signed fan angle gamma (counter-clockwise from the central ray, the scan
+    turning counter-clockwise), half fan angle Gamma (Parker 1982, as the pages'
+    "Parker weights"): the weights of a ray and of its conjugate
+    (beta + pi + 2 gamma, -gamma) sum to one."""
+    beta = np.asarray(beta, np.float64)
+    gamma = np.asarray(gamma, np.float64)
+    g = big_gamma
+    w = np.ones(np.broadcast(beta, gamma).shape)
+    lo = beta < 2 * (g - gamma)
+    hi = beta > math.pi - 2 * gamma
+    with np.errstate(divide="ignore", invalid="ignore"):
+        w = np.where(lo, np.sin(0.25 * math.pi * beta / (g - gamma)) ** 2, w)
+        w = np.where(hi, np.sin(0.25 * math.pi * (math.pi + 2 * g - beta) / (g + gamma)) ** 2, w)
+    w = np.where((beta < 0) | (beta > math.pi + 2 * g), 0.0, w)
+    return w
+
+
+def scan_angles(scan):
+    """Per view the scan angle beta (source azimuth about the vertical axis through
+    the volume centre, from view 0 in the direction the scan turns), per view and
+    detector column the signed fan angle gamma in the xy plane (from the central
+    ray -- source to axis -- to the column's ray, counter-clockwise in the
+    turning sense), and the half fan angle Gamma (largest |gamma| of view 0)."""
+    a, c, u, v = _frames(scan)
+    iso = volume_centre(scan)
+    rel = a[:, :2] - iso[None, :2]
+    az = np.unwrap(np.arctan2(rel[:, 1], rel[:, 0]))
+    sense = 1.0 if scan.n_views < 2 or az[1] >= az[0] else -1.0
+    beta = sense * (az - az[0])
+    iu = (np.arange(scan.n_u) - 0.5 * (scan.n_u - 1) + scan.offset_u) * scan.pitch_u
+    P = c[:, None, :] + iu[None, :, None] * u[:, None, :]
+    d = (P - a[:, None, :])[:, :, :2]
+    ctr = -rel[:, None, :] / np.linalg.norm(rel, axis=1)[:, None, None]
+    cross = ctr[..., 0] * d[..., 1] - ctr[..., 1] * d[..., 0]
+    dot = (ctr * d).sum(-1)
+    gamma = sense * np.arctan2(cross, dot)
+    return beta, gamma, float(np.abs(gamma[0]).max())
+
+
+def parker_weights(scan):
+    """(n_views, n_u) Parker weights of a circular short scan (see :func:`parker`)."""
+    beta, gamma, big = scan_angles(scan)
+    return parker(beta[:, None], gamma, big)
+
+
+def filter_sinogram_pw(scan, p, view_weight=None, pixel_weight=None, kind=RAMLAK):
+    """:func:`filter_sinogram` with per-(view, column) weights applied before the
+    convolution (Parker weights, or any learned weights)."""
+    p = np.asarray(p, np.float64).reshape(scan.n_views, scan.n_v, scan.n_u)
+    if pixel_weight is not None:
+        p = p * np.asarray(pixel_weight, np.float64)[:, None, :]
+    return filter_sinogram(scan, p, view_weight, kind)
 
 
 def fdk(scan, p, view_weight=None, kind=RAMLAK):
