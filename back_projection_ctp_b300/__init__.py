@@ -6,20 +6,20 @@ The entry points carry the C names: :func:`ctp_plan`, :func:`ctp_forward`,
 :func:`ctp_backward_host`, :func:`ctp_destroy`, :func:`ctp_status_string`, the
 allocation-free :func:`ctp_forward_static`, and the analytical FBP / FDK operators
 :func:`ctp_ramp_filter`, :func:`ctp_weighted_backproject`,
-:func:`ctp_weighted_backproject_transpose` and :func:`ctp_fdk`, and the geometry
-gradients :func:`ctp_geometry_vjp`.
+:func:`ctp_weighted_backproject_transpose`, :func:`ctp_fdk` and
+:func:`ctp_parker_weights`, and the geometry gradients :func:`ctp_geometry_vjp`.
 """
 
 from ._binding import (EXPORTS, CtpError, Geometry, Plan, Volume, ctp_backward,
                        ctp_backward_host, ctp_destroy, ctp_fdk, ctp_forward, ctp_forward_host,
-                       ctp_forward_static, ctp_geometry_vjp, ctp_plan, ctp_ramp_filter,
-                       ctp_segment_count,
+                       ctp_forward_static, ctp_geometry_vjp, ctp_parker_weights, ctp_plan,
+                       ctp_ramp_filter, ctp_segment_count,
                        ctp_status_string, ctp_weighted_backproject,
                        ctp_weighted_backproject_transpose, full_scan_view_weights, load_library)
 
 __all__ = ["EXPORTS", "CtpError", "Geometry", "Plan", "Volume", "ctp_backward",
            "ctp_backward_host", "ctp_destroy", "ctp_fdk", "ctp_forward", "ctp_forward_host",
-           "ctp_forward_static", "ctp_geometry_vjp", "ctp_plan", "ctp_ramp_filter",
-           "ctp_segment_count",
+           "ctp_forward_static", "ctp_geometry_vjp", "ctp_parker_weights", "ctp_plan",
+           "ctp_ramp_filter", "ctp_segment_count",
            "ctp_status_string", "ctp_weighted_backproject", "ctp_weighted_backproject_transpose",
            "full_scan_view_weights", "load_library"]

@@ -54,9 +54,10 @@ class _PlanInfo(ctypes.Structure):
 EXPORTS = ("ctp_plan", "ctp_destroy", "ctp_plan_info_get", "ctp_forward", "ctp_backward",
            "ctp_segment_count", "ctp_forward_host", "ctp_backward_host", "ctp_status_string",
            "ctp_forward_static", "ctp_ramp_filter", "ctp_weighted_backproject",
-           "ctp_weighted_backproject_transpose", "ctp_fdk", "ctp_geometry_vjp")
+           "ctp_weighted_backproject_transpose", "ctp_fdk", "ctp_geometry_vjp",
+           "ctp_parker_weights")
 
-RAMPS = {"ramlak": 0, "shepp_logan": 1}
+RAMPS = {"ramlak": 0, "shepp_logan": 1, "cosine": 2, "hamming": 3, "hann": 4}
 
 
 def load_library(path: str | None = None):
@@ -81,10 +82,11 @@ def load_library(path: str | None = None):
         lib.ctp_segment_count.argtypes = [P, ctypes.POINTER(ctypes.c_ulonglong), P]
         lib.ctp_forward_static.argtypes = [ctypes.POINTER(_Geometry), ctypes.POINTER(_Volume),
                                            P, P, P]
-        lib.ctp_ramp_filter.argtypes = [P, P, P, P, I, I, P]
+        lib.ctp_ramp_filter.argtypes = [P, P, P, P, P, I, I, P]
         lib.ctp_weighted_backproject.argtypes = [P, P, P, P]
         lib.ctp_weighted_backproject_transpose.argtypes = [P, P, P, P]
-        lib.ctp_fdk.argtypes = [P, P, P, P, P, I, P]
+        lib.ctp_fdk.argtypes = [P, P, P, P, P, P, I, P]
+        lib.ctp_parker_weights.argtypes = [P, P, P]
         lib.ctp_geometry_vjp.argtypes = [P, P, P, P, P]
         lib.ctp_status_string.argtypes = [I]
         lib.ctp_status_string.restype = ctypes.c_char_p
@@ -329,14 +331,22 @@ def _view_weight(plan: Plan, view_weight):
     return _device_f32(view_weight, (plan.sino_shape[0],), "view_weight")
 
 
+def _pixel_weight(plan: Plan, pixel_weight):
+    if pixel_weight is None:
+        return None
+    return _device_f32(pixel_weight, (plan.sino_shape[0], plan.sino_shape[2]), "pixel_weight")
+
+
 def ctp_ramp_filter(plan: Plan, sino, out, view_weight=None, ramp: str = "ramlak",
-                    transpose: bool = False, stream=None):
-    """out <- ramp filter along u of the cosine-weighted sino, times the view
-    weights (transpose: the transposed operator).  ``out`` may be ``sino``."""
+                    transpose: bool = False, stream=None, pixel_weight=None):
+    """out <- ramp filter along u of the cosine- (and pixel-) weighted sino, times
+    the view weights (transpose: the transposed operator).  ``out`` may be
+    ``sino``.  pixel_weight: (n_views, n_u), e.g. :func:`ctp_parker_weights`."""
     _check(load_library().ctp_ramp_filter(
         plan.handle, _device_f32(sino, plan.sino_shape, "sino"),
         _device_f32(out, plan.sino_shape, "out"), _view_weight(plan, view_weight),
-        RAMPS[ramp], int(bool(transpose)), _stream_ptr(stream)), "ctp_ramp_filter")
+        _pixel_weight(plan, pixel_weight), RAMPS[ramp], int(bool(transpose)),
+        _stream_ptr(stream)), "ctp_ramp_filter")
     return out
 
 
@@ -358,14 +368,28 @@ def ctp_weighted_backproject_transpose(plan: Plan, vol, sino, stream=None):
     return sino
 
 
-def ctp_fdk(plan: Plan, sino, work, vol, view_weight=None, ramp: str = "ramlak", stream=None):
+def ctp_fdk(plan: Plan, sino, work, vol, view_weight=None, ramp: str = "ramlak", stream=None,
+            pixel_weight=None):
     """vol <- FBP / FDK of sino: ramp filter into ``work`` (may be ``sino``), then the
     weighted gather."""
     _check(load_library().ctp_fdk(
         plan.handle, _device_f32(sino, plan.sino_shape, "sino"),
         _device_f32(work, plan.sino_shape, "work"), _device_f32(vol, plan.vol_shape, "vol"),
-        _view_weight(plan, view_weight), RAMPS[ramp], _stream_ptr(stream)), "ctp_fdk")
+        _view_weight(plan, view_weight), _pixel_weight(plan, pixel_weight), RAMPS[ramp],
+        _stream_ptr(stream)), "ctp_fdk")
     return vol
+
+
+def ctp_parker_weights(plan: Plan, out=None, stream=None):
+    """Parker short-scan weights (n_views, n_u) as a float32 CUDA tensor; use with
+    view weights equal to the angular step."""
+    import torch
+    shape = (plan.sino_shape[0], plan.sino_shape[2])
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32, device=torch.device("cuda", plan.device))
+    _check(load_library().ctp_parker_weights(plan.handle, _device_f32(out, shape, "out"),
+                                             _stream_ptr(stream)), "ctp_parker_weights")
+    return out
 
 
 def full_scan_view_weights(n_views: int):

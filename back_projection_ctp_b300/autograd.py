@@ -48,16 +48,18 @@ class Projector:
         return _Backproject.apply(sino, self)
 
     def fdk(self, sino: torch.Tensor, view_weight: torch.Tensor | None = None,
-            ramp: str = "ramlak") -> torch.Tensor:
+            ramp: str = "ramlak", pixel_weight: torch.Tensor | None = None) -> torch.Tensor:
         """Differentiable FBP / FDK: ramp filter (cosine and view weights) then the
         weighted gather; the gradient is the transposed filter of the gather's
         transpose (diffct README "Differentiable FBP and FDK": sinogram gradients
         through the transposed interpolation stencil).  ``view_weight``: (n_views,)
         tensor, e.g. ``full_scan_view_weights``; no gradient flows to it."""
-        vw = None
+        vw = pw = None
         if view_weight is not None:
             vw = view_weight.detach().to(device=self.device, dtype=torch.float32).contiguous()
-        return _Gather.apply(_Filter.apply(sino, self, vw, ramp), self)
+        if pixel_weight is not None:
+            pw = pixel_weight.detach().to(device=self.device, dtype=torch.float32).contiguous()
+        return _Gather.apply(_Filter.apply(sino, self, vw, ramp, False, pw), self)
 
     __call__ = project
 
@@ -105,24 +107,24 @@ class _Backproject(torch.autograd.Function):
         return g.to(dtype=ctx.in_dtype, device=ctx.in_device), None
 
 
-def _filter_fn(vw, ramp, transpose):
+def _filter_fn(vw, ramp, transpose, pw):
     def fn(plan, x, out, stream):
-        ctp_ramp_filter(plan, x, out, vw, ramp, transpose, stream)
+        ctp_ramp_filter(plan, x, out, vw, ramp, transpose, stream, pw)
     return fn
 
 
 class _Filter(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, sino, proj, vw, ramp, transpose=False):
-        ctx.proj, ctx.vw, ctx.ramp, ctx.transpose = proj, vw, ramp, transpose
+    def forward(ctx, sino, proj, vw, ramp, transpose=False, pw=None):
+        ctx.proj, ctx.vw, ctx.ramp, ctx.transpose, ctx.pw = proj, vw, ramp, transpose, pw
         ctx.in_dtype, ctx.in_device = sino.dtype, sino.device
         return _apply(proj, sino, proj.sino_shape, proj.sino_shape,
-                      _filter_fn(vw, ramp, transpose))
+                      _filter_fn(vw, ramp, transpose, pw))
 
     @staticmethod
     def backward(ctx, grad):
-        g = _Filter.apply(grad, ctx.proj, ctx.vw, ctx.ramp, not ctx.transpose)
-        return g.to(dtype=ctx.in_dtype, device=ctx.in_device), None, None, None, None
+        g = _Filter.apply(grad, ctx.proj, ctx.vw, ctx.ramp, not ctx.transpose, ctx.pw)
+        return g.to(dtype=ctx.in_dtype, device=ctx.in_device), None, None, None, None, None
 
 
 class _Gather(torch.autograd.Function):

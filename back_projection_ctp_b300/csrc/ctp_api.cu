@@ -34,6 +34,7 @@ struct ctp_plan {
     double pitch_u = 1, pitch_v = 1, offset_u = 0, offset_v = 0;
     long long n_rays = 0, n_cells = 0;
     std::vector<ctp::ViewFrame> frames;     // host copy
+    std::vector<float> raw;                 // the caller's frames: src, centre, u, v (n_views x 12)
     ctp::ViewFrame *d_frames = nullptr;     // device copy
     float *d_offsets = nullptr;             // curved detector: (n_v, n_u, 3) pixel offsets
     ctp::ColumnOffsets *d_columns = nullptr;  // curved detector, column path: per column
@@ -52,7 +53,7 @@ struct ctp_plan {
     int fdk_status = CTP_E_GEOMETRY;
     ctp::FdkParams fdk{};
     ctp::FdkView *d_fdk = nullptr;
-    float *d_ramp[2] = {nullptr, nullptr};  // Ram-Lak, Shepp-Logan kernels (2 n_u - 1)
+    float *d_ramp[ctp::kRampKinds] = {};    // ramp kernels (2 n_u - 1) by ctp_ramp value
     unsigned long long device_bytes = 0;
 };
 
@@ -211,8 +212,7 @@ void free_plan(ctp_plan_t *p)
     cudaFree(p->d_stage_vol);
     cudaFree(p->d_stage_sino);
     cudaFree(p->d_fdk);
-    cudaFree(p->d_ramp[0]);
-    cudaFree(p->d_ramp[1]);
+    for (float *h : p->d_ramp) cudaFree(h);
     if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
     if (p->ev_start) cudaEventDestroy(p->ev_start);
     for (cudaEvent_t e : p->ev_chunk)
@@ -319,7 +319,7 @@ int fdk_setup(ctp_plan_t *p, const ctp_geometry *g, const ctp_volume *v)
     p->device_bytes += vbytes;
     p->fdk.views = p->d_fdk;
     if (g->n_u <= ctp::kFilterMaxU) {
-        for (int kind = 0; kind < 2; ++kind) {
+        for (int kind = 0; kind < ctp::kRampKinds; ++kind) {
             std::vector<float> h;
             ctp::fdk_ramp_kernel(g->n_u, g->pitch_u, kind, h);
             const size_t hb = sizeof(float) * h.size();
@@ -409,6 +409,14 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
     p->offset_u = geom->offset_u;
     p->offset_v = geom->offset_v;
     p->n_rays = (long long)geom->n_views * geom->n_u * geom->n_v;
+    p->raw.assign(12 * (size_t)geom->n_views, 0.0f);
+    for (int s = 0; s < geom->n_views; ++s)
+        for (int a = 0; a < 3; ++a) {
+            p->raw[12 * (size_t)s + a] = geom->src[3 * s + a];
+            p->raw[12 * (size_t)s + 3 + a] = geom->det_centre[3 * s + a];
+            p->raw[12 * (size_t)s + 6 + a] = geom->det_u[3 * s + a];
+            p->raw[12 * (size_t)s + 9 + a] = geom->det_v[3 * s + a];
+        }
     p->n_cells = (long long)vol->nx * vol->ny * vol->nz;
 
     // Per-view frames in cell coordinates, float64.
@@ -760,17 +768,47 @@ int ctp_backward_host(ctp_plan_t *plan, const float *sino_host, float *vol_host,
     return CTP_OK;
 }
 
+int ctp_parker_weights(const ctp_plan_t *plan, float *weight_dev, void *stream)
+{
+    if (!plan) return CTP_E_NULL;
+    if (plan->n_views > 0 && !weight_dev) return CTP_E_NULL;
+    int st = check_device(plan);
+    if (st != CTP_OK) return st;
+    if (plan->beam != CTP_DIVERGENT || plan->d_offsets) return CTP_E_GEOMETRY;
+    if (plan->n_views == 0) return CTP_OK;
+    std::vector<float> src(3 * (size_t)plan->n_views), cen(src.size()), u(src.size());
+    for (int k = 0; k < plan->n_views; ++k)
+        for (int a = 0; a < 3; ++a) {
+            src[3 * k + a] = plan->raw[12 * (size_t)k + a];
+            cen[3 * k + a] = plan->raw[12 * (size_t)k + 3 + a];
+            u[3 * k + a] = plan->raw[12 * (size_t)k + 6 + a];
+        }
+    const double iso[2] = {plan->origin[0] + 0.5 * plan->n[0] * plan->spacing[0],
+                           plan->origin[1] + 0.5 * plan->n[1] * plan->spacing[1]};
+    std::vector<float> w;
+    ctp::fdk_parker(plan->n_views, plan->n_u, src.data(), cen.data(), u.data(), plan->pitch_u,
+                    plan->offset_u, iso, w);
+    cudaStream_t s = (cudaStream_t)stream;
+    // the host vector dies with this call: copy, then wait for the copy
+    if (cudaMemcpyAsync(weight_dev, w.data(), sizeof(float) * w.size(), cudaMemcpyHostToDevice,
+                        s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return CTP_E_CUDA;
+    return CTP_OK;
+}
+
 int ctp_ramp_filter(const ctp_plan_t *plan, const float *sino_dev, float *out_dev,
-                    const float *view_weight_dev, int ramp, int transpose, void *stream)
+                    const float *view_weight_dev, const float *pixel_weight_dev, int ramp,
+                    int transpose, void *stream)
 {
     if (!plan) return CTP_E_NULL;
     if (plan->n_rays > 0 && (!sino_dev || !out_dev)) return CTP_E_NULL;
-    if (ramp != CTP_RAMLAK && ramp != CTP_SHEPP_LOGAN) return CTP_E_OPTION;
+    if (ramp < CTP_RAMLAK || ramp > CTP_HANN) return CTP_E_OPTION;
     int st = fdk_check(plan);
     if (st != CTP_OK) return st;
     if (!plan->d_ramp[ramp]) return CTP_E_LIMIT;
     return ctp::fdk_filter(plan->fdk, plan->d_ramp[ramp], sino_dev, out_dev, view_weight_dev,
-                           transpose ? 1 : 0, (cudaStream_t)stream)
+                           pixel_weight_dev, transpose ? 1 : 0, (cudaStream_t)stream)
                ? CTP_E_CUDA : CTP_OK;
 }
 
@@ -826,10 +864,11 @@ int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *
 }
 
 int ctp_fdk(const ctp_plan_t *plan, const float *sino_dev, float *work_dev, float *vol_dev,
-            const float *view_weight_dev, int ramp, void *stream)
+            const float *view_weight_dev, const float *pixel_weight_dev, int ramp, void *stream)
 {
     if (!plan || !vol_dev || (plan->n_rays > 0 && (!sino_dev || !work_dev))) return CTP_E_NULL;
-    int st = ctp_ramp_filter(plan, sino_dev, work_dev, view_weight_dev, ramp, 0, stream);
+    int st = ctp_ramp_filter(plan, sino_dev, work_dev, view_weight_dev, pixel_weight_dev, ramp, 0,
+                             stream);
     if (st != CTP_OK) return st;
     return ctp_weighted_backproject(plan, work_dev, vol_dev, stream);
 }

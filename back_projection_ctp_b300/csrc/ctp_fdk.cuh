@@ -327,7 +327,8 @@ __device__ __forceinline__ float fdk_cosine(const FdkParams &F, const FdkView &V
 template <int RB>
 __global__ void ramp_filter_kernel(FdkParams F, const float *__restrict__ h,
                                    const float *__restrict__ x, float *__restrict__ out,
-                                   const float *__restrict__ view_weight, int transpose,
+                                   const float *__restrict__ view_weight,
+                                   const float *__restrict__ pixel_weight, int transpose,
                                    long long n_rows)
 {
     extern __shared__ float sm[];
@@ -342,8 +343,13 @@ __global__ void ramp_filter_kernel(FdkParams F, const float *__restrict__ h,
         float val = 0.0f;
         if (row < n_rows) {
             const int view = (int)(row / F.n_v), iv = (int)(row - (long long)view * F.n_v);
-            const float pre = transpose ? (view_weight ? view_weight[view] : 1.0f)
-                                        : fdk_cosine(F, F.views[view], jj, iv);
+            float pre;
+            if (transpose) {
+                pre = view_weight ? view_weight[view] : 1.0f;
+            } else {
+                pre = fdk_cosine(F, F.views[view], jj, iv);
+                if (pixel_weight) pre *= pixel_weight[(long long)view * nu + jj];
+            }
             val = x[row * nu + jj] * pre;
         }
         xs[t] = val;
@@ -379,8 +385,13 @@ __global__ void ramp_filter_kernel(FdkParams F, const float *__restrict__ h,
             for (int m = 0; m < 4; ++m) {
                 const int i = i0 + m * T;
                 if (i >= nu) continue;
-                const float post = transpose ? fdk_cosine(F, F.views[view], i, iv)
-                                             : (view_weight ? view_weight[view] : 1.0f);
+                float post;
+                if (transpose) {
+                    post = fdk_cosine(F, F.views[view], i, iv);
+                    if (pixel_weight) post *= pixel_weight[(long long)view * nu + i];
+                } else {
+                    post = view_weight ? view_weight[view] : 1.0f;
+                }
                 out[row * nu + i] = __fmul_rn(__fmul_rn(acc[r][m], F.pitch_u), post);
             }
         }
@@ -542,21 +553,44 @@ inline int fdk_build(int ndim, int beam, int n_views, int n_u, int n_v, const fl
     return 0;
 }
 
-// Ramp kernels h[m], m = -(n-1) .. n-1, with frequency response |omega|
-// (radians per unit length; Ram-Lak) or (2/tau)|sin(omega tau / 2)| (Shepp-Logan).
+// Ramp kernels h[m], m = -(n-1) .. n-1: the inverse transforms of H(omega) =
+// |omega| (radians per unit length) times a window, for |omega| <= pi / tau:
+// none (Ram-Lak), (2/(tau |omega|)) |sin(omega tau / 2)| (Shepp-Logan),
+// cos(omega tau / 2) (cosine), 0.54 + 0.46 cos(omega tau) (Hamming) and
+// (1 + cos(omega tau)) / 2 (Hann).  The cosine windows shift the band-limited
+// ramp r(x) = (pi sin(pi x) / x + (cos(pi x) - 1) / x^2) / (pi tau^2) by half or
+// whole samples.
+constexpr int kRampKinds = 5;
+
+inline double fdk_band_ramp(double x, double tau)
+{
+    const double kPi = 3.14159265358979323846;
+    if (x == 0.0) return kPi / (2.0 * tau * tau);
+    const long long m = (long long)x;
+    if ((double)m == x)  // whole samples: 0 (even) or -2 / (pi m^2 tau^2) (odd)
+        return (m % 2 == 0) ? 0.0 : -2.0 / (kPi * x * x * tau * tau);
+    return (kPi * std::sin(kPi * x) / x + (std::cos(kPi * x) - 1.0) / (x * x)) / (kPi * tau * tau);
+}
+
 inline void fdk_ramp_kernel(int n, double tau, int kind, std::vector<float> &h)
 {
     const double kPi = 3.14159265358979323846;
     h.assign(2 * n - 1, 0.0f);
     for (int t = 0; t < 2 * n - 1; ++t) {
-        const long long m = t - (n - 1);
+        const double m = (double)(t - (n - 1));
         double v;
-        if (kind == 0) {
-            if (m == 0) v = kPi / (2.0 * tau * tau);
-            else if (m % 2 != 0) v = -2.0 / (kPi * (double)m * (double)m * tau * tau);
-            else v = 0.0;
-        } else {
-            v = -4.0 / (kPi * tau * tau * (4.0 * (double)m * (double)m - 1.0));
+        switch (kind) {
+        case 0: v = fdk_band_ramp(m, tau); break;
+        case 1: v = -4.0 / (kPi * tau * tau * (4.0 * m * m - 1.0)); break;
+        case 2: v = 0.5 * (fdk_band_ramp(m - 0.5, tau) + fdk_band_ramp(m + 0.5, tau)); break;
+        case 3:
+            v = 0.54 * fdk_band_ramp(m, tau) +
+                0.23 * (fdk_band_ramp(m - 1.0, tau) + fdk_band_ramp(m + 1.0, tau));
+            break;
+        default:
+            v = 0.5 * fdk_band_ramp(m, tau) +
+                0.25 * (fdk_band_ramp(m - 1.0, tau) + fdk_band_ramp(m + 1.0, tau));
+            break;
         }
         h[t] = (float)v;
     }
@@ -612,7 +646,8 @@ constexpr int kFilterMaxU = 16384;
 
 template <int RB>
 inline int ramp_launch(const FdkParams &F, const float *h, const float *x, float *out,
-                       const float *view_weight, int transpose, cudaStream_t s)
+                       const float *view_weight, const float *pixel_weight, int transpose,
+                       cudaStream_t s)
 {
     const long long rows = (long long)F.n_views * F.n_v;
     const size_t smem = sizeof(float) * ((size_t)RB * F.n_u + 2 * (size_t)F.n_u);
@@ -625,21 +660,82 @@ inline int ramp_launch(const FdkParams &F, const float *h, const float *x, float
     threads = threads < 32 ? 32 : (threads > 256 ? 256 : threads);
     const long long blocks = (rows + RB - 1) / RB;
     ramp_filter_kernel<RB><<<(unsigned)blocks, threads, smem, s>>>(F, h, x, out, view_weight,
-                                                                   transpose, rows);
+                                                                   pixel_weight, transpose, rows);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 
 inline int fdk_filter(const FdkParams &F, const float *h, const float *x, float *out,
-                      const float *view_weight, int transpose, cudaStream_t s)
+                      const float *view_weight, const float *pixel_weight, int transpose,
+                      cudaStream_t s)
 {
     if ((long long)F.n_views * F.n_v == 0) return 0;
     // rows per block: as many as fit 48 KB of shared memory, at most 8
     const size_t per_row = sizeof(float) * (size_t)F.n_u;
     const size_t hbytes = 2 * per_row;
-    if (hbytes + 8 * per_row <= 48 * 1024) return ramp_launch<8>(F, h, x, out, view_weight, transpose, s);
-    if (hbytes + 4 * per_row <= 48 * 1024) return ramp_launch<4>(F, h, x, out, view_weight, transpose, s);
-    if (hbytes + 2 * per_row <= 48 * 1024) return ramp_launch<2>(F, h, x, out, view_weight, transpose, s);
-    return ramp_launch<1>(F, h, x, out, view_weight, transpose, s);
+    const float *vw = view_weight, *pw = pixel_weight;
+    if (hbytes + 8 * per_row <= 48 * 1024) return ramp_launch<8>(F, h, x, out, vw, pw, transpose, s);
+    if (hbytes + 4 * per_row <= 48 * 1024) return ramp_launch<4>(F, h, x, out, vw, pw, transpose, s);
+    if (hbytes + 2 * per_row <= 48 * 1024) return ramp_launch<2>(F, h, x, out, vw, pw, transpose, s);
+    return ramp_launch<1>(F, h, x, out, vw, pw, transpose, s);
+}
+
+// Parker's short-scan weights (Parker 1982) of a circular divergent scan about
+// the vertical axis through the volume centre: per view the scan angle beta
+// (source azimuth from view 0, in the turning sense), per view and column the
+// signed fan angle gamma in the xy plane (central ray to the column's ray, in
+// the turning sense), Gamma the largest |gamma| of view 0;
+//   w = sin^2(pi/4 beta / (Gamma - gamma))              for beta < 2 (Gamma - gamma)
+//     = sin^2(pi/4 (pi + 2 Gamma - beta) / (Gamma + gamma))  for beta > pi - 2 gamma
+//     = 1 between, 0 outside [0, pi + 2 Gamma],
+// so that the weights of a ray and its conjugate (beta + pi + 2 gamma, -gamma)
+// sum to one.  Host float64 (n_views x n_u values, set-up work).
+inline void fdk_parker(int n_views, int n_u, const float *src, const float *centre,
+                       const float *det_u, double pitch_u, double offset_u, const double iso[2],
+                       std::vector<float> &out)
+{
+    const double kPi = 3.14159265358979323846;
+    out.assign((size_t)n_views * n_u, 0.0f);
+    if (n_views == 0) return;
+    std::vector<double> az(n_views), gam((size_t)n_views * n_u);
+    for (int k = 0; k < n_views; ++k) {
+        az[k] = std::atan2((double)src[3 * k + 1] - iso[1], (double)src[3 * k] - iso[0]);
+        if (k > 0) {  // unwrap
+            while (az[k] - az[k - 1] > kPi) az[k] -= 2 * kPi;
+            while (az[k] - az[k - 1] < -kPi) az[k] += 2 * kPi;
+        }
+    }
+    const double sense = (n_views < 2 || az[1] >= az[0]) ? 1.0 : -1.0;
+    double big = 0.0;
+    for (int k = 0; k < n_views; ++k) {
+        const double ax = src[3 * k], ay = src[3 * k + 1];
+        const double rx = ax - iso[0], ry = ay - iso[1], rn = std::sqrt(rx * rx + ry * ry);
+        const double cx = -rx / rn, cy = -ry / rn;  // central ray direction
+        for (int i = 0; i < n_u; ++i) {
+            const double off = ((double)i - 0.5 * (n_u - 1) + offset_u) * pitch_u;
+            const double dx = centre[3 * k] + off * det_u[3 * k] - ax;
+            const double dy = centre[3 * k + 1] + off * det_u[3 * k + 1] - ay;
+            const double g = sense * std::atan2(cx * dy - cy * dx, cx * dx + cy * dy);
+            gam[(size_t)k * n_u + i] = g;
+            if (k == 0) big = std::fmax(big, std::fabs(g));
+        }
+    }
+    for (int k = 0; k < n_views; ++k) {
+        const double beta = sense * (az[k] - az[0]);
+        for (int i = 0; i < n_u; ++i) {
+            const double g = gam[(size_t)k * n_u + i];
+            double w = 1.0;
+            if (beta < 0.0 || beta > kPi + 2 * big) {
+                w = 0.0;
+            } else if (beta < 2 * (big - g)) {
+                const double t = std::sin(0.25 * kPi * beta / (big - g));
+                w = t * t;
+            } else if (beta > kPi - 2 * g) {
+                const double t = std::sin(0.25 * kPi * (kPi + 2 * big - beta) / (big + g));
+                w = t * t;
+            }
+            out[(size_t)k * n_u + i] = (float)w;
+        }
+    }
 }
 
 }  // namespace ctp

@@ -227,8 +227,9 @@ int ctp_forward_static(const ctp_geometry *geom, const ctp_volume *vol, const fl
  *              from the source (parallel: along the rays); SDD_s = (c_s - a_s).n_s,
  *              SID_s = (iso - a_s).n_s, a_s = src[s], c_s = det_centre[s].
  *   ramp       q[s,iv,i] = post * pitch_u * sum_j h[i-j] * pre * p[s,iv,j] along u,
- *              h the Ram-Lak kernel (frequency response |omega|, radians per unit
- *              length) or Shepp-Logan ((2/tau)|sin(omega tau/2)|), tau = pitch_u.
+ *              h the inverse transform of |omega| (radians per unit length) times
+ *              a window (ctp_ramp: none = Ram-Lak, sinc = Shepp-Logan, cosine,
+ *              Hamming, Hann; the pages' list of ramp filters), tau = pitch_u.
  *              Forward: pre = SDD_s / |pixel - a_s| (cosine weight; parallel 1),
  *              post = view_weight[s].  Transpose: pre and post swapped.
  *   gather     g(x) = sum_s k_s (SID_s / U_s(x))^2 I(q_s; u_s(x), v_s(x)): x the
@@ -251,7 +252,9 @@ int ctp_forward_static(const ctp_geometry *geom, const ctp_volume *vol, const fl
  * the projector pair).  ctp_ramp_filter needs n_u <= 16384 (else CTP_E_LIMIT).
  *
  * Buffers: device float32, layouts as above; view_weight_dev: device float32
- * (n_views), or NULL for all ones.  ramp: CTP_RAMLAK or CTP_SHEPP_LOGAN.
+ * (n_views), or NULL for all ones; pixel_weight_dev: device float32 (n_views,
+ * n_u), or NULL for all ones, multiplied into the forward filter's pre-weight
+ * (and the transpose's post-weight) -- e.g. ctp_parker_weights.  ramp: a ctp_ramp.
  * transpose: 0 or 1.  ctp_ramp_filter may run in place (out_dev == sino_dev).
  * ctp_weighted_backproject overwrites vol_dev; ctp_weighted_backproject_transpose
  * overwrites sino_dev (zeroed, then accumulated with float atomics).  ctp_fdk =
@@ -260,16 +263,40 @@ int ctp_forward_static(const ctp_geometry *geom, const ctp_volume *vol, const fl
  * Errors: CTP_E_NULL, CTP_E_DEVICE, CTP_E_OPTION (unknown ramp), CTP_E_GEOMETRY,
  * CTP_E_LIMIT, CTP_E_CUDA.  All are asynchronous on `stream`.
  */
-typedef enum ctp_ramp { CTP_RAMLAK = 0, CTP_SHEPP_LOGAN = 1 } ctp_ramp;
+typedef enum ctp_ramp {
+    CTP_RAMLAK = 0,       /* |omega| */
+    CTP_SHEPP_LOGAN = 1,  /* (2 / tau) |sin(omega tau / 2)| */
+    CTP_COSINE = 2,       /* |omega| cos(omega tau / 2) */
+    CTP_HAMMING = 3,      /* |omega| (0.54 + 0.46 cos(omega tau)) */
+    CTP_HANN = 4          /* |omega| (1 + cos(omega tau)) / 2 */
+} ctp_ramp;
 
 int ctp_ramp_filter(const ctp_plan_t *plan, const float *sino_dev, float *out_dev,
-                    const float *view_weight_dev, int ramp, int transpose, void *stream);
+                    const float *view_weight_dev, const float *pixel_weight_dev, int ramp,
+                    int transpose, void *stream);
 int ctp_weighted_backproject(const ctp_plan_t *plan, const float *sino_dev, float *vol_dev,
                              void *stream);
 int ctp_weighted_backproject_transpose(const ctp_plan_t *plan, const float *vol_dev,
                                        float *sino_dev, void *stream);
 int ctp_fdk(const ctp_plan_t *plan, const float *sino_dev, float *work_dev, float *vol_dev,
-            const float *view_weight_dev, int ramp, void *stream);
+            const float *view_weight_dev, const float *pixel_weight_dev, int ramp, void *stream);
+
+/*
+ * ctp_parker_weights -- Parker's short-scan weights (the pages' analytical
+ * helpers list Parker weights) of a circular divergent scan about the vertical
+ * axis through the volume centre, for pixel_weight_dev of the calls above:
+ * weight_dev[k][i] (device float32, n_views x n_u) = sin^2(pi/4 beta / (G - g))
+ * for beta < 2 (G - g), sin^2(pi/4 (pi + 2 G - beta) / (G + g)) for
+ * beta > pi - 2 g, 1 between and 0 outside [0, pi + 2 G]: beta = view k's source
+ * azimuth from view 0 in the scan's turning sense, g = the signed fan angle of
+ * column i (xy plane, central ray to the column's ray, in the turning sense),
+ * G = the largest |g| of view 0.  A ray's and its conjugate's weights sum to
+ * one; with them, view weights equal to the angular step (not half of it)
+ * reconstruct a scan of pi + 2 G.  Computed on the host in float64 and copied;
+ * the call waits for the copy.  Errors: CTP_E_NULL, CTP_E_DEVICE,
+ * CTP_E_GEOMETRY (parallel beam or curved detector), CTP_E_CUDA.
+ */
+int ctp_parker_weights(const ctp_plan_t *plan, float *weight_dev, void *stream);
 
 /*
  * ctp_geometry_vjp -- first-order geometry gradients of the projection
