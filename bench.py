@@ -40,12 +40,26 @@ CSRC = os.path.join(ROOT, "back_projection_ctp_b300", "csrc")
 
 
 # ----------------------------------------------------------------- helpers
-def source_hash() -> str:
+# Sources that compile into each profiled kernel (its code, its launch set-up
+# and its parameter structs).
+KERNEL_SOURCES = {
+    "column_forward_kernel": ("ctp_column.cuh", "ctp_ray.cuh", "ctp_internal.h"),
+    "column_backward_kernel": ("ctp_column.cuh", "ctp_ray.cuh", "ctp_internal.h"),
+}
+
+
+def source_hash(kernel: str) -> str:
+    """Hash of a kernel's sources with comments and blank space removed, so that a
+    stored ncu capture stays attached to unchanged code only."""
+    import re
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
-        with open(os.path.join(CSRC, name), "rb") as fh:
-            h.update(name.encode())
-            h.update(fh.read())
+    for name in KERNEL_SOURCES.get(kernel, sorted(os.listdir(CSRC))):
+        with open(os.path.join(CSRC, name)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(name.encode())
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
@@ -74,7 +88,7 @@ def stored_traffic(kernel: str, workload: str):
     except (OSError, ValueError):
         return None
     entry = rec.get(kernel, {}).get(workload)
-    if not entry or entry.get("source_hash") != source_hash():
+    if not entry or entry.get("source_hash") != source_hash(kernel):
         return None
     return entry.get("dram_bytes_per_launch")
 
