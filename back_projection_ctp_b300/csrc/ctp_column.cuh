@@ -292,8 +292,10 @@ __device__ __forceinline__ RowZ column_row_setup(const RayParams &P, const Colum
 // t = (beta - g) / beta = 1 - g / beta.  CLAMP restricts the slab to [lo, hi]
 // (first / last slab of rays that start or end inside).  op(r, addr, length,
 // on, jb) sees every piece of row r; `on` = inside the grid in z (x and y are
-// covered by the zero halo), jb lets the counter test x / y.
-template <int R, bool CLAMP, bool CHECK, class Op>
+// covered by the zero halo), jb lets the counter test x / y.  SZ = +-1: the
+// z step of every row that crosses z planes (then a row's next z cell is a
+// fixed address offset from its current one); 0: each row's own.
+template <int R, bool CLAMP, bool CHECK, int SZ, class Op>
 __device__ __forceinline__ void column_slab(uint32_t &fb, uint32_t bb, float ib, int &jb, int sb,
                                             int &xy, int sp, RowZ (&Z)[R], unsigned nz, float lo,
                                             float hi, Op &op)
@@ -309,9 +311,11 @@ __device__ __forceinline__ void column_slab(uint32_t &fb, uint32_t bb, float ib,
             if (CLAMP) e = fminf(fmaxf(e, lo), hi);
             const float d0 = CLAMP ? __fsub_rn(e, lo) : e;
             const float d1 = __fsub_rn(CLAMP ? hi : 1.0f, e);
-            const int z1 = Z[r].zoff + Z[r].sz;
-            op(r, xy + Z[r].zoff, d0, !CHECK || (unsigned)Z[r].zoff < nz, jb);
-            op(r, xy + z1, d1, cz && (!CHECK || (unsigned)z1 < nz), jb);
+            const int sz = SZ ? SZ : Z[r].sz;
+            const int z1 = Z[r].zoff + sz;
+            const int a0 = xy + Z[r].zoff;
+            op(r, a0, d0, !CHECK || (unsigned)Z[r].zoff < nz, jb);
+            op(r, a0 + sz, d1, cz && (!CHECK || (unsigned)z1 < nz), jb);
             Z[r].fz = gz;
             if (cz) Z[r].zoff = z1;
         }
@@ -333,11 +337,13 @@ __device__ __forceinline__ void column_slab(uint32_t &fb, uint32_t bb, float ib,
             const float d1 = CLAMP ? __fsub_rn(e1, lo) : e1;
             const float d2 = __fsub_rn(e2, e1);
             const float d3 = __fsub_rn(CLAMP ? hi : 1.0f, e2);
-            const int z0 = Z[r].zoff, z1 = z0 + Z[r].sz;
+            const int sz = SZ ? SZ : Z[r].sz;
+            const int z0 = Z[r].zoff, z1 = z0 + sz;
             const bool v0 = !CHECK || (unsigned)z0 < nz, v1 = !CHECK || (unsigned)z1 < nz;
-            op(r, xy + z0, d1, v0, jb);
-            op(r, bfirst ? xy + sb + z0 : xy + z1, d2, bfirst ? v0 : v1, bfirst ? jb + 1 : jb);
-            op(r, xy + sb + z1, d3, cz && v1, jb + 1);
+            const int a0 = xy + z0;
+            op(r, a0, d1, v0, jb);
+            op(r, a0 + (bfirst ? sb : sz), d2, bfirst ? v0 : v1, bfirst ? jb + 1 : jb);
+            op(r, a0 + sb + sz, d3, cz && v1, jb + 1);
             Z[r].fz = gz;
             if (cz) Z[r].zoff = z1;
         }
@@ -350,9 +356,9 @@ __device__ __forceinline__ void column_slab(uint32_t &fb, uint32_t bb, float ib,
 // Walk all slabs of a column for R rows: partial first / last slab peeled off;
 // between them the slabs where every row of the warp is inside the grid in z
 // (ka..kb) run without validity tests, the others with them.
-template <int R, class Op>
-__device__ __forceinline__ void column_walk(const ColumnTrace &C, RowZ (&Z)[R], unsigned nz,
-                                            Op &op)
+template <int R, int SZ, class Op>
+__device__ __forceinline__ void column_walk_sz(const ColumnTrace &C, RowZ (&Z)[R], unsigned nz,
+                                               Op &op)
 {
     uint32_t fb = C.fb;
     int jb = C.jb, xy = C.addr_xy;
@@ -367,19 +373,36 @@ __device__ __forceinline__ void column_walk(const ColumnTrace &C, RowZ (&Z)[R], 
     }
     const int ka = max(__reduce_max_sync(0xffffffffu, kin), C.k0 + 1);
     const int kb = min(__reduce_min_sync(0xffffffffu, kout), C.k1 - 1);
-    column_slab<R, true, true>(fb, bb, ib, jb, sb, xy, sp, Z, nz, C.tlo,
+    column_slab<R, true, true, SZ>(fb, bb, ib, jb, sb, xy, sp, Z, nz, C.tlo,
                                C.k0 == C.k1 ? C.thi : 1.0f, op);
     int k = C.k0 + 1;
     if (ka <= kb) {
         for (; k < ka; ++k)
-            column_slab<R, false, true>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
+            column_slab<R, false, true, SZ>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
         for (; k <= kb; ++k)
-            column_slab<R, false, false>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
+            column_slab<R, false, false, SZ>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
     }
     for (; k < C.k1; ++k)
-        column_slab<R, false, true>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
+        column_slab<R, false, true, SZ>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
     if (C.k1 > C.k0)
-        column_slab<R, true, true>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, C.thi, op);
+        column_slab<R, true, true, SZ>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, C.thi, op);
+}
+
+// The walk with the z step fixed at compile time when every row of the warp
+// that crosses z planes steps the same way (all warps but those whose rows
+// straddle the source's z), else per row.
+template <int R, class Op>
+__device__ __forceinline__ void column_walk(const ColumnTrace &C, RowZ (&Z)[R], unsigned nz,
+                                            Op &op)
+{
+    unsigned dir = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        if (Z[r].bz) dir |= Z[r].sz > 0 ? 1u : 2u;
+    dir = __reduce_or_sync(0xffffffffu, dir);
+    if (dir == 2u) column_walk_sz<R, -1>(C, Z, nz, op);
+    else if (dir == 3u) column_walk_sz<R, 0>(C, Z, nz, op);
+    else column_walk_sz<R, 1>(C, Z, nz, op);
 }
 
 template <int R>
