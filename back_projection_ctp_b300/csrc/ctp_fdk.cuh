@@ -160,6 +160,14 @@ __device__ __forceinline__ void fdk_column_of(int tx, int &i, int &j)
     j = blockIdx.y * 8 + (warp / wx) * (32 / tx) + lane / tx;
 }
 
+// True when no stencil row of the K steps is on the detector: the rows of step
+// t lie in [iv + t dvi, iv + t (dvi + 1) + 1].
+template <int K>
+__device__ __forceinline__ bool fdk_rows_miss(const FdkParams &F, const ColumnView &C)
+{
+    return C.iv + (K - 1) * max(C.dvi + 1, 0) + 1 < 0 || C.iv + (K - 1) * min(C.dvi, 0) >= F.n_v;
+}
+
 // The K updates of one column in one view, stencil values read straight from
 // the filtered sinogram.  Rows of step t lie in [iv + t dvi, iv + t (dvi + 1)];
 // when the stencils of all K steps are on the detector the loop runs without
@@ -249,13 +257,20 @@ __global__ void __launch_bounds__(256) wbp_gather_kernel(FdkParams F, const floa
             acc[0] = __fmaf_rn(C.w, __fmaf_rn(C.fu, a1 - a0, a0), acc[0]);
             continue;
         }
+        if (fdk_rows_miss<K>(F, C)) continue;
         gather_column<K>(F, C, base, acc);
     }
     store_column<K>(F, i, j, k0, acc, vol);
 }
 
-// Transpose: the same stencil, each voxel's s_k W_k g scattered with float atomics
-// into a zeroed sinogram.
+// Transpose: the same stencil, each voxel's s_k W_k g reduced with float
+// atomics into a zeroed sinogram.  In 3-D the taps of consecutive z steps on a
+// shared detector row are first summed in registers: the stencil rows of step
+// t are (iv, iv + 1) and iv moves monotonically by floor(dv) or floor(dv) + 1
+// per step, so a row pair overlaps the previous one in at most one row (or
+// both, for steps under a pixel).  The pending pair (pa at row P, pb at row
+// P + 1) takes the new step's taps where rows coincide and is reduced into the
+// sinogram only when a row is left (C4 transpose 370 -> 288 ms on B300).
 template <int K>
 __global__ void __launch_bounds__(256) wbp_scatter_kernel(FdkParams F,
                                                           const float *__restrict__ vol,
@@ -275,8 +290,8 @@ __global__ void __launch_bounds__(256) wbp_scatter_kernel(FdkParams F,
     for (int s = 0; s < F.n_views; ++s) {
         ColumnView C;
         if (!fdk_column_view(F, F.views[s], i, j, k0, C)) continue;
-        float *base = q + s * plane;
         if (F.ndim == 2) {
+            float *base = q + s * plane;
             const float val = C.w * g[0];
             if (val != 0.0f) {
                 if (C.c0) atomicAdd(base + C.iu, val * (1.0f - C.fu));
@@ -284,28 +299,42 @@ __global__ void __launch_bounds__(256) wbp_scatter_kernel(FdkParams F,
             }
             continue;
         }
-        int iv = C.iv;
-        float fv = C.fv;
-#pragma unroll
-        for (int t = 0; t < K; ++t) {
-            const bool r0 = (unsigned)iv < (unsigned)F.n_v;
-            const bool r1 = (unsigned)(iv + 1) < (unsigned)F.n_v;
-            const float val = C.w * g[t];
-            if ((r0 || r1) && val != 0.0f) {
-                float *row = base + (long long)iv * F.n_u + C.iu;
-                const float va = val * (1.0f - fv), vb = val * fv;
-                if (r0 && C.c0) atomicAdd(row, va * (1.0f - C.fu));
-                if (r0 && C.c1) atomicAdd(row + 1, va * C.fu);
-                if (r1 && C.c0) atomicAdd(row + F.n_u, vb * (1.0f - C.fu));
-                if (r1 && C.c1) atomicAdd(row + F.n_u + 1, vb * C.fu);
+        if (fdk_rows_miss<K>(F, C)) continue;
+        float *col = q + s * plane + C.iu;
+        const float wu0 = C.c0 ? 1.0f - C.fu : 0.0f, wu1 = C.c1 ? C.fu : 0.0f;
+        // reduce row r's value x into the sinogram (both columns)
+        auto flush = [&](int r, float x) {
+            if ((unsigned)r < (unsigned)F.n_v && x != 0.0f) {
+                float *px = col + (long long)r * F.n_u;
+                if (C.c0) atomicAdd(px, x * wu0);
+                if (C.c1) atomicAdd(px + 1, x * wu1);
             }
+        };
+        int P = C.iv;
+        float fv = C.fv;
+        float pa = C.w * g[0] * (1.0f - fv), pb = C.w * g[0] * fv;
+#pragma unroll
+        for (int t = 1; t < K; ++t) {
+            // the step from the previous row P, as in the gather
             fv += C.dvf;
-            iv += C.dvi;
+            int iv = P + C.dvi;
             if (fv >= 1.0f) {
                 fv -= 1.0f;
                 iv += 1;
             }
+            const float val = C.w * g[t];
+            const float va = val * (1.0f - fv), vb = val * fv;
+            const int d = iv - P;
+            if (d != 0 && d != -1) flush(P, pa);
+            if (d != 0 && d != 1) flush(P + 1, pb);
+            const float na = d == 0 ? pa + va : (d == 1 ? pb + va : va);
+            const float nb = d == 0 ? pb + vb : (d == -1 ? pa + vb : vb);
+            pa = na;
+            pb = nb;
+            P = iv;
         }
+        flush(P, pa);
+        flush(P + 1, pb);
     }
 }
 
