@@ -288,12 +288,42 @@ __global__ void __launch_bounds__(256) column_gvjp_kernel(RayParams P, GeomParam
         uint32_t fb = C.fb;
         int xy = C.addr_xy;
         for (int k = C.k0; any && k <= C.k1; ++k) {
-            const float lo = k == C.k0 ? C.tlo : 0.0f;
-            const float hi = k == C.k1 ? C.thi : 1.0f;
             const uint32_t gb = fb + C.bb;
             const bool cb = gb < fb;
-            const float tb = cb ? fmaxf(__fmaf_rn(-__uint2float_rn(gb), C.ib, 1.0f), 0.0f) : 2.0f;
             const float tk = __fmaf_rn((float)(k - C.k0), tinv, t0);
+            if (!cb && k != C.k0 && k != C.k1) {
+                // interior slab without a b crossing (uniform across the warp):
+                // the general body below with lo = 0, hi = 1 and tb = 2, where the
+                // cells after the first and after both crossings coincide
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t gz = Z[r].fz + Z[r].bz;
+                    const bool cz = gz < Z[r].fz;
+                    const float tz = fmaxf(__fmaf_rn(-__uint2float_rn(gz), Z[r].ibz, 1.0f), 0.0f);
+                    const int za = Z[r].zoff, z1 = za + Z[r].sz;
+                    const float vA = (unsigned)za < nz ? __ldg(zvol + xy + za) : 0.0f;
+                    const float vB = cz ? ((unsigned)z1 < nz ? __ldg(zvol + xy + z1) : 0.0f) : vA;
+                    const float e1 = cz ? tz : 1.0f;
+                    acc[r] = __fmaf_rn(e1, vA, __fmaf_rn(__fsub_rn(1.0f, e1), vB, acc[r]));
+                    const float j = fprev[r] - vA;
+                    dfp[r] += j;
+                    dtp[r] = __fmaf_rn(j, tk, dtp[r]);
+                    if (cz && tz > 0.0f && tz < 1.0f) {
+                        const float jz = vA - vB, t = __fmaf_rn(tz, tinv, tk);
+                        dfz[r] += jz;
+                        dtz[r] = __fmaf_rn(jz, t, dtz[r]);
+                    }
+                    fprev[r] = cz && tz < 1.0f ? vB : vA;
+                    Z[r].fz = gz;
+                    if (cz) Z[r].zoff = z1;
+                }
+                xy += C.sp;
+                fb = gb;
+                continue;
+            }
+            const float lo = k == C.k0 ? C.tlo : 0.0f;
+            const float hi = k == C.k1 ? C.thi : 1.0f;
+            const float tb = cb ? fmaxf(__fmaf_rn(-__uint2float_rn(gb), C.ib, 1.0f), 0.0f) : 2.0f;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t gz = Z[r].fz + Z[r].bz;
