@@ -442,7 +442,7 @@ constexpr int kColumnsPerBlock = 8;  // 8 warps: 8 columns, each 32 * R rows
 // instruction then covers 32 adjacent rows; the backward interleaves its rows,
 // see column_row_slot).
 template <int R>
-__global__ void __launch_bounds__(256, 4) column_forward_kernel(RayParams P,
+__global__ void __launch_bounds__(256, R >= 4 ? 4 : 5) column_forward_kernel(RayParams P,
                                                              const ColumnTrace *__restrict__ T,
                                                              const float *__restrict__ zvol,
                                                              float *__restrict__ sino)
