@@ -236,7 +236,7 @@ __device__ __forceinline__ void store_column(const FdkParams &F, int i, int j, i
 // One thread per (x, y) column and K consecutive z; blocks of 32 x 8 columns;
 // stencil values straight from global memory (2-D scans, and a tuning override).
 template <int K>
-__global__ void __launch_bounds__(256, 5) wbp_gather_kernel(FdkParams F, const float *__restrict__ q,
+__global__ void __launch_bounds__(256, K > 1 ? 5 : 8) wbp_gather_kernel(FdkParams F, const float *__restrict__ q,
                                                          float *__restrict__ vol)
 {
     int i, j;
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(256, 5) wbp_gather_kernel(FdkParams F, const f
 // P + 1) takes the new step's taps where rows coincide and is reduced into the
 // sinogram only when a row is left (C4 transpose 370 -> 288 ms on B300).
 template <int K>
-__global__ void __launch_bounds__(256, 4) wbp_scatter_kernel(FdkParams F,
+__global__ void __launch_bounds__(256, K > 1 ? 4 : 8) wbp_scatter_kernel(FdkParams F,
                                                           const float *__restrict__ vol,
                                                           float *__restrict__ q)
 {

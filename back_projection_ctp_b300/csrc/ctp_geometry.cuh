@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(TU *TV) geometry_vjp_kernel(RayParams P, GeomP
 // z-fastest working copy of the volume (zero halo in x and y; z validity per
 // access).  t of the p coordinate is shared by the column's rows.
 template <int R>
-__global__ void __launch_bounds__(256) column_gvjp_kernel(RayParams P, GeomParams Q,
+__global__ void __launch_bounds__(256, 4) column_gvjp_kernel(RayParams P, GeomParams Q,
                                                           const ColumnTrace *__restrict__ T,
                                                           const float *__restrict__ zvol,
                                                           const float *__restrict__ wsino,
