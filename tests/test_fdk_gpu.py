@@ -236,6 +236,50 @@ def test_source_inside_the_volume_and_truncated_detector(torch, ctp, oracle_mod,
     assert rel_l2(vol.cpu().numpy(), ofdk.weighted_backproject(scan, q)) <= TOL_GATHER
 
 
+@pytest.mark.parametrize("pitch_v", [8.0, 1.2, 0.4])
+@pytest.mark.parametrize("v_sign", [1.0, -1.0])
+def test_row_steps_of_every_size_and_a_flipped_v_axis(torch, ctp, oracle_mod, ofdk, pitch_v,
+                                                      v_sign):
+    """Along a voxel column the stencil rows advance by dv = magnification x dz /
+    pitch_v per z step: under one row (consecutive steps share both rows), between
+    one and two (they share one), over two (none), and with the v axis along -z
+    (rows decrease).  The transpose's register row sums and the gather's and
+    transpose's skip of off-detector columns must match the oracle in each case;
+    40 z voxels make two whole 16-voxel chunks and a ragged one."""
+    K = 10
+    b = np.arange(K) * 2 * math.pi / K + 0.1
+    c, s, zero, one = np.cos(b), np.sin(b), np.zeros(K), np.ones(K)
+    frames = {"src": np.stack([40 * c, 40 * s, zero], 1),
+              "det_centre": np.stack([-30 * c, -30 * s, zero], 1),
+              "det_u": np.stack([-s, c, zero], 1), "det_v": np.stack([zero, zero, v_sign * one], 1)}
+    frames = {k: v.astype(np.float32) for k, v in frames.items()}
+    shape, spacing = (40, 12, 12), (1.0, 1.0, 1.0)
+    origin = (-6.0, -6.0, -20.0)
+    n_u, n_v, pu = 26, 24, 1.5
+    scan = oracle_mod.Scan("divergent", frames["src"], frames["det_centre"], frames["det_u"],
+                           frames["det_v"], n_u, n_v, pu, pitch_v, shape, spacing, origin, 0.2,
+                           0.3, 3)
+    g = ctp.Geometry(ndim=3, beam="divergent", n_u=n_u, n_v=n_v, pitch_u=pu, pitch_v=pitch_v,
+                     offset_u=0.2, offset_v=0.3, **frames)
+    plan = ctp.ctp_plan(g, ctp.Volume(shape, spacing, origin))
+    rng = np.random.default_rng(int(10 * pitch_v) + (v_sign > 0))
+    q = rng.standard_normal(plan.sino_shape).astype(np.float32)
+    x = rng.standard_normal(plan.vol_shape).astype(np.float32)
+    d_q, d_x = _dev(torch, q), _dev(torch, x)
+    vol = torch.full(plan.vol_shape, float("nan"), device="cuda")
+    t = torch.full(plan.sino_shape, float("nan"), device="cuda")
+    ctp.ctp_weighted_backproject(plan, d_q, vol)
+    ctp.ctp_weighted_backproject_transpose(plan, d_x, t)
+    torch.cuda.synchronize()
+    got_b, got_t = vol.cpu().numpy(), t.cpu().numpy()
+    assert rel_l2(got_b, ofdk.weighted_backproject(scan, q)) <= TOL_GATHER
+    ref_t = ofdk.weighted_backproject_transpose(scan, x)
+    assert np.abs(ref_t).max() > 0.0
+    assert rel_l2(got_t, ref_t) <= TOL_SCATTER
+    cs, _ = adjoint_mismatch(got_b, x, q, got_t)
+    assert cs <= TOL_ADJOINT
+
+
 @pytest.mark.parametrize("n_u", [5000, 16385])
 def test_wide_detector_rows(torch, ctp, oracle_mod, ofdk, n_u):
     """Rows wider than 4096 pixels take the one-row-per-block filter with more than
