@@ -151,7 +151,10 @@ int ctp_plan_info_get(const ctp_plan_t *plan, ctp_plan_info *info);
  * sino_dev: device float32 (n_views, n_v, n_u), fully overwritten (rays that
  * miss the volume get 0).  stream: a cudaStream_t (NULL = default stream).
  * The two buffers must not overlap.  For a plan without rays both pointers may
- * be NULL (nothing is done).  Errors: CTP_E_NULL, CTP_E_DEVICE, CTP_E_CUDA.
+ * be NULL (nothing is done).  The column and plane paths walk padded working
+ * copies of the volume that the plan owns, so device calls on one plan must be
+ * ordered (one stream, or events between streams); different plans are
+ * independent.  Errors: CTP_E_NULL, CTP_E_DEVICE, CTP_E_CUDA.
  */
 int ctp_forward(const ctp_plan_t *plan, const float *vol_dev, float *sino_dev, void *stream);
 
@@ -320,8 +323,12 @@ int ctp_parker_weights(const ctp_plan_t *plan, float *weight_dev, void *stream);
  * or corner are kinks of p; the jump goes to one of the coincident crossings.
  * vol_dev: device float32 (nz, ny, nx).  weight_dev: device float32
  * (n_views, n_v, n_u).  grad_dev: device float64 (n_views, 12), overwritten.
- * Runs the ray path's walk whatever path the plan chose; asynchronous on
- * `stream`.  Errors: CTP_E_NULL, CTP_E_DEVICE, CTP_E_CUDA.
+ * Column-path plans run the sums over the column walk on the plan's working
+ * copy of vol_dev (ordered with the plan's other calls, as ctp_forward); other
+ * plans run the ray path's walk (the environment variable CTP_GEOMETRY_RAY=1
+ * forces it for column plans too).  Asynchronous on `stream`.  Errors:
+ * CTP_E_NULL, CTP_E_DEVICE, CTP_E_OPTION (curved detectors: the chain rule
+ * above assumes the pitch grid), CTP_E_CUDA.
  */
 int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *weight_dev,
                      double *grad_dev, void *stream);
