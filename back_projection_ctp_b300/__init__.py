@@ -11,15 +11,16 @@ allocation-free :func:`ctp_forward_static`, and the analytical FBP / FDK operato
 """
 
 from ._binding import (EXPORTS, CtpError, Geometry, Plan, Volume, ctp_backward,
-                       ctp_backward_host, ctp_destroy, ctp_fdk, ctp_forward, ctp_forward_host,
-                       ctp_forward_static, ctp_geometry_vjp, ctp_parker_weights, ctp_plan,
-                       ctp_ramp_filter, ctp_segment_count,
+                       ctp_backward_host, ctp_check_violations, ctp_destroy, ctp_fdk,
+                       ctp_forward, ctp_forward_host, ctp_forward_static, ctp_geometry_vjp,
+                       ctp_parker_weights, ctp_plan, ctp_ramp_filter, ctp_segment_count,
                        ctp_status_string, ctp_weighted_backproject,
-                       ctp_weighted_backproject_transpose, full_scan_view_weights, load_library)
+                       ctp_weighted_backproject_transpose, full_scan_view_weights,
+                       load_library)
 
 __all__ = ["EXPORTS", "CtpError", "Geometry", "Plan", "Volume", "ctp_backward",
-           "ctp_backward_host", "ctp_destroy", "ctp_fdk", "ctp_forward", "ctp_forward_host",
-           "ctp_forward_static", "ctp_geometry_vjp", "ctp_parker_weights", "ctp_plan",
-           "ctp_ramp_filter", "ctp_segment_count",
-           "ctp_status_string", "ctp_weighted_backproject", "ctp_weighted_backproject_transpose",
-           "full_scan_view_weights", "load_library"]
+           "ctp_backward_host", "ctp_check_violations", "ctp_destroy", "ctp_fdk",
+           "ctp_forward", "ctp_forward_host", "ctp_forward_static", "ctp_geometry_vjp",
+           "ctp_parker_weights", "ctp_plan", "ctp_ramp_filter", "ctp_segment_count",
+           "ctp_status_string", "ctp_weighted_backproject",
+           "ctp_weighted_backproject_transpose", "full_scan_view_weights", "load_library"]

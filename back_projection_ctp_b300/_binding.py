@@ -16,6 +16,8 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libctp.so")
+# CTP_LIBRARY_VARIANT=check loads the bounds-checked debug build instead
+_CHECK_LIB_PATH = os.path.join(_HERE, "libctp_check.so")
 _lib = None
 _lock = threading.Lock()
 
@@ -55,21 +57,23 @@ EXPORTS = ("ctp_plan", "ctp_destroy", "ctp_plan_info_get", "ctp_forward", "ctp_b
            "ctp_segment_count", "ctp_forward_host", "ctp_backward_host", "ctp_status_string",
            "ctp_forward_static", "ctp_ramp_filter", "ctp_weighted_backproject",
            "ctp_weighted_backproject_transpose", "ctp_fdk", "ctp_geometry_vjp",
-           "ctp_parker_weights")
+           "ctp_parker_weights", "ctp_check_violations")
 
 RAMPS = {"ramlak": 0, "shepp_logan": 1, "cosine": 2, "hamming": 3, "hann": 4}
 
 
 def load_library(path: str | None = None):
-    """Load ``libctp.so`` (building it first when it is absent and nvcc exists)."""
+    """Load ``libctp.so`` (building it first when it is absent and nvcc exists);
+    with CTP_LIBRARY_VARIANT=check, the bounds-checked ``libctp_check.so``."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        lib_path = path or _LIB_PATH
+        check = os.environ.get("CTP_LIBRARY_VARIANT") == "check"
+        lib_path = path or (_CHECK_LIB_PATH if check else _LIB_PATH)
         if not os.path.exists(lib_path):
             from . import build as _build
-            _build.build()
+            _build.build(check=check)
         lib = ctypes.CDLL(lib_path)
         P, I = ctypes.c_void_p, ctypes.c_int
         lib.ctp_plan.argtypes = [ctypes.POINTER(_Geometry), ctypes.POINTER(_Volume), I,
@@ -88,6 +92,10 @@ def load_library(path: str | None = None):
         lib.ctp_fdk.argtypes = [P, P, P, P, P, P, I, P]
         lib.ctp_parker_weights.argtypes = [P, P, P]
         lib.ctp_geometry_vjp.argtypes = [P, P, P, P, P]
+        lib.ctp_check_violations.argtypes = [ctypes.POINTER(ctypes.c_ulonglong),
+                                             ctypes.POINTER(ctypes.c_longlong),
+                                             ctypes.POINTER(ctypes.c_longlong),
+                                             ctypes.POINTER(ctypes.c_int)]
         lib.ctp_status_string.argtypes = [I]
         lib.ctp_status_string.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -291,6 +299,16 @@ def ctp_segment_count(plan: Plan, stream=None) -> int:
     _check(load_library().ctp_segment_count(plan.handle, ctypes.byref(out), _stream_ptr(stream)),
            "ctp_segment_count")
     return int(out.value)
+
+
+def ctp_check_violations() -> tuple[int, int, int, int]:
+    """(count, first index, its buffer's extent, access site) of the out-of-range
+    accesses since the previous call, in the bounds-checked build; resets them.
+    Raises CtpError (CTP_E_OPTION) in normal builds."""
+    c, i, e, site = ctypes.c_ulonglong(0), ctypes.c_longlong(0), ctypes.c_longlong(0), ctypes.c_int(0)
+    _check(load_library().ctp_check_violations(ctypes.byref(c), ctypes.byref(i), ctypes.byref(e),
+                                               ctypes.byref(site)), "ctp_check_violations")
+    return int(c.value), int(i.value), int(e.value), int(site.value)
 
 
 def _host_f32(a, shape, name, writable=False):

@@ -10,6 +10,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libctp.so")
+# bounds-checked debug build (-DCTP_CHECK): every walk access tested and counted
+CHECK_LIB = os.path.join(HERE, "libctp_check.so")
 SOURCES = ["ctp_api.cu"]
 DEPS = ["ctp_api.cu", "ctp_ray.cuh", "ctp_column.cuh", "ctp_plane.cuh", "ctp_fdk.cuh",
         "ctp_geometry.cuh", "ctp_internal.h"]
@@ -22,20 +24,25 @@ def _newest_input():
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
-        return LIB
+def build(force: bool = False, verbose: bool = False, check: bool = False) -> str:
+    """Build ``libctp.so`` (``check``: the bounds-checked ``libctp_check.so``)."""
+    lib = CHECK_LIB if check else LIB
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input():
+        return lib
     nvcc = os.environ.get("NVCC", "nvcc")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
            "-I", os.path.join(ROOT, "include"), "-o", tmp]
+    if check:
+        cmd += ["-DCTP_CHECK"]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     cmd += [os.path.join(CSRC, s) for s in SOURCES]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                check="--check" in sys.argv))

@@ -373,6 +373,30 @@ const char *ctp_status_string(int status)
     }
 }
 
+int ctp_check_violations(unsigned long long *count, long long *index, long long *extent,
+                         int *site)
+{
+    if (!count || !index || !extent || !site) return CTP_E_NULL;
+#ifdef CTP_CHECK
+    ctp::CheckState h{};
+    const ctp::CheckState zero{};
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(&h, ctp::ctp_check_state, sizeof h) != cudaSuccess ||
+        cudaMemcpyToSymbol(ctp::ctp_check_state, &zero, sizeof zero) != cudaSuccess)
+        return CTP_E_CUDA;
+    *count = h.count;
+    *index = h.index;
+    *extent = h.extent;
+    *site = h.site;
+    return CTP_OK;
+#else
+    *count = 0;
+    *index = *extent = 0;
+    *site = 0;
+    return CTP_E_OPTION;
+#endif
+}
+
 int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan_t **out)
 {
     if (!out) return CTP_E_NULL;

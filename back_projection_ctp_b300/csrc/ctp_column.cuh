@@ -57,6 +57,12 @@ struct ColumnPlan {
 // never copied out -- no xy bounds tests in the walk.
 constexpr int kHalo = 2;
 
+// Cells of a padded z-fastest working copy.
+__host__ __device__ __forceinline__ size_t column_padded_cells(const RayParams &P)
+{
+    return ((size_t)P.n[0] + 2 * kHalo) * ((size_t)P.n[1] + 2 * kHalo) * (size_t)P.n[2];
+}
+
 // Float64 set-up of the shared xy trace of every detector column.
 __global__ void column_setup_kernel(RayParams P, ColumnTrace *__restrict__ T,
                                     int *__restrict__ flag)
@@ -409,9 +415,10 @@ template <int R>
 struct ColumnGather {
     const float *__restrict__ vol;
     float acc[R];
+    long long lim;  // cells of the padded working copy (bounds-checked builds)
     __device__ __forceinline__ void operator()(int r, int a, float d, bool on, int)
     {
-        if (on) acc[r] = __fmaf_rn(d, __ldg(vol + a), acc[r]);
+        if (on && ctp_in(a, lim, kSiteColumnGather)) acc[r] = __fmaf_rn(d, __ldg(vol + a), acc[r]);
     }
 };
 
@@ -419,9 +426,11 @@ template <int R>
 struct ColumnScatter {
     float *__restrict__ vol;
     float w[R];  // ell * y of each row
+    long long lim;
     __device__ __forceinline__ void operator()(int r, int a, float d, bool on, int)
     {
-        if (on && d > 0.0f && w[r] != 0.0f) atomicAdd(vol + a, __fmul_rn(d, w[r]));
+        if (on && d > 0.0f && w[r] != 0.0f && ctp_in(a, lim, kSiteColumnScatter))
+            atomicAdd(vol + a, __fmul_rn(d, w[r]));
     }
 };
 
@@ -461,6 +470,7 @@ __global__ void __launch_bounds__(256, R >= 4 ? 4 : 5) column_forward_kernel(Ray
             RowZ Z[R];
             ColumnGather<R> op;
             op.vol = zvol;
+            op.lim = (long long)column_padded_cells(P);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int iv = row0 + 32 * r;
@@ -479,8 +489,9 @@ __global__ void __launch_bounds__(256, R >= 4 ? 4 : 5) column_forward_kernel(Ray
     for (int e = threadIdx.x; e < 32 * R * kColumnsPerBlock; e += 256) {
         const int rr = e / kColumnsPerBlock, c = e % kColumnsPerBlock;
         const int ivw = blockIdx.z * 32 * R + rr, iuw = blockIdx.x * kColumnsPerBlock + c;
-        if (ivw < P.n_v && iuw < P.n_u)
-            sino[((long long)view * P.n_v + ivw) * P.n_u + iuw] = tile[rr][c];
+        const long long ray = ((long long)view * P.n_v + ivw) * P.n_u + iuw;
+        if (ivw < P.n_v && iuw < P.n_u && ctp_in(ray, sino_cells(P), kSiteColumnSinoStore))
+            sino[ray] = tile[rr][c];
     }
 }
 
@@ -506,8 +517,9 @@ __global__ void __launch_bounds__(256, 4) column_backward_kernel(RayParams P,
     for (int e = threadIdx.x; e < 32 * R * kColumnsPerBlock; e += 256) {
         const int rr = e / kColumnsPerBlock, c = e % kColumnsPerBlock;
         const int ivr = blockIdx.z * 32 * R + rr, iur = blockIdx.x * kColumnsPerBlock + c;
-        tile[rr][c] = (ivr < P.n_v && iur < P.n_u)
-                          ? sino[((long long)view * P.n_v + ivr) * P.n_u + iur]
+        const long long ray = ((long long)view * P.n_v + ivr) * P.n_u + iur;
+        tile[rr][c] = (ivr < P.n_v && iur < P.n_u && ctp_in(ray, sino_cells(P), kSiteColumnSinoLoad))
+                          ? sino[ray]
                           : 0.0f;
     }
     __syncthreads();
@@ -519,6 +531,7 @@ __global__ void __launch_bounds__(256, 4) column_backward_kernel(RayParams P,
     RowZ Z[R];
     ColumnScatter<R> op;
     op.vol = zvol;
+    op.lim = (long long)column_padded_cells(P);
     bool any = false;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -583,7 +596,10 @@ __global__ void __launch_bounds__(256) xfast_to_zfast_kernel(const float *__rest
     __syncthreads();
     for (int j = ty; j < 32; j += 8) {
         const int x = x0 + j, z = z0 + tx;
-        if (x < nx && z < nz) out[((x + kHalo) * pny + (y + kHalo)) * nz + z] = tile[tx][j];
+        const long long o = ((long long)(x + kHalo) * pny + (y + kHalo)) * nz + z;
+        if (x < nx && z < nz &&
+            ctp_in(o, ((long long)nx + 2 * kHalo) * (long long)pny * nz, kSiteColumnLayoutIn))
+            out[o] = tile[tx][j];
     }
 }
 
@@ -598,7 +614,10 @@ __global__ void __launch_bounds__(256) zfast_to_xfast_kernel(const float *__rest
     const size_t pny = (size_t)ny + 2 * kHalo;
     for (int j = ty; j < 32; j += 8) {
         const int x = x0 + j, z = z0 + tx;
-        if (x < nx && z < nz) tile[j][tx] = in[((x + kHalo) * pny + (y + kHalo)) * nz + z];
+        const long long o = ((long long)(x + kHalo) * pny + (y + kHalo)) * nz + z;
+        if (x < nx && z < nz &&
+            ctp_in(o, ((long long)nx + 2 * kHalo) * (long long)pny * nz, kSiteColumnLayoutOut))
+            tile[j][tx] = in[o];
     }
     __syncthreads();
     for (int j = ty; j < 32; j += 8) {
@@ -607,17 +626,12 @@ __global__ void __launch_bounds__(256) zfast_to_xfast_kernel(const float *__rest
     }
 }
 
-inline size_t column_padded_cells(const RayParams &P)
-{
-    return ((size_t)P.n[0] + 2 * kHalo) * ((size_t)P.n[1] + 2 * kHalo) * (size_t)P.n[2];
-}
 
 // Rows per thread.  The shared xy walk is paid once per R rows, at the cost of
-// registers.  The forward gather waits on L2 and wants occupancy: it runs 5
-// blocks of 256 threads per SM (<= 48 registers, a few spilled) with 4 rows.
-// The backward is bound by its atomics' L1/L2 throughput and runs 2 rows
-// without a register cap.  CTP_COLUMN_ROWS_FWD / CTP_COLUMN_ROWS_BWD = 1, 2, 3 or 4
-// override the choice.
+// registers.  The forward gather runs 4 rows (4 blocks of 256 threads per SM,
+// 64 registers; 2 rows at 5 blocks on short detectors); the backward, bound by
+// its atomics' L1/L2 throughput, runs 2 rows at 4 blocks per SM.
+// CTP_COLUMN_ROWS_FWD / CTP_COLUMN_ROWS_BWD = 1, 2, 3 or 4 override the choice.
 inline int column_rows(const RayParams &P, const char *env_name, int preferred)
 {
     const char *env = getenv(env_name);

@@ -40,4 +40,47 @@ struct RayParams {
     const ColumnOffsets *columns;  // curved detector on the column path: per column; else null
 };
 
+// Bounds-checked debug build (compiled with -DCTP_CHECK): the projector walks
+// test the index of every global load, store and reduction -- and the tiled
+// backward of every shared-memory reduction -- against its buffer's extent
+// before the access.  An index outside is counted in ctp_check_state (with the
+// first offending index, its buffer's extent and the access site) and the
+// access is skipped, so a wrong index shows up as a count, never as a fault.
+// In normal builds ctp_in is the constant true and the tests vanish.
+enum CheckSite {
+    kSiteRayGather = 1, kSiteRayScatter, kSiteRaySinoStore, kSiteRaySinoLoad,
+    kSiteColumnGather = 10, kSiteColumnScatter, kSiteColumnSinoStore, kSiteColumnSinoLoad,
+    kSiteColumnLayoutIn, kSiteColumnLayoutOut,
+    kSitePlaneGather = 20, kSitePlaneScatter, kSitePlaneSinoStore, kSitePlaneSinoLoad,
+    kSitePlaneTile, kSitePlaneTileOut
+};
+
+#ifdef CTP_CHECK
+struct CheckState {
+    unsigned long long count;
+    long long index, extent;
+    int site, pad_;
+};
+__device__ CheckState ctp_check_state;
+
+__device__ __forceinline__ bool ctp_in(long long i, long long n, int site)
+{
+    if (i >= 0 && i < n) return true;
+    if (atomicAdd(&ctp_check_state.count, 1ull) == 0ull) {
+        ctp_check_state.index = i;
+        ctp_check_state.extent = n;
+        ctp_check_state.site = site;
+    }
+    return false;
+}
+#else
+__device__ __forceinline__ constexpr bool ctp_in(long long, long long, int) { return true; }
+#endif
+
+// Elements of the sinogram buffer (n_views, n_v, n_u).
+__host__ __device__ __forceinline__ long long sino_cells(const RayParams &P)
+{
+    return (long long)P.n_views * P.n_v * P.n_u;
+}
+
 }  // namespace ctp

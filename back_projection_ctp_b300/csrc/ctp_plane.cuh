@@ -224,20 +224,28 @@ __device__ __forceinline__ void plane_walk_range(const PlaneRay &R, int ka, int 
 struct PlaneGather {
     const float *__restrict__ img;
     float acc;
+    long long lim;  // cells of the padded copies (bounds-checked builds)
     __device__ __forceinline__ void operator()(int a, float d, bool on, int)
     {
-        if (on) acc = __fmaf_rn(d, __ldg(img + a), acc);
+        if (on && ctp_in(a, lim, kSitePlaneGather)) acc = __fmaf_rn(d, __ldg(img + a), acc);
     }
 };
 
 struct PlaneScatter {
     float *__restrict__ img;
     float w;
+    long long lim;
     __device__ __forceinline__ void operator()(int a, float d, bool on, int)
     {
-        if (on && d > 0.0f) atomicAdd(img + a, __fmul_rn(d, w));
+        if (on && d > 0.0f && ctp_in(a, lim, kSitePlaneScatter)) atomicAdd(img + a, __fmul_rn(d, w));
     }
 };
+
+// Cells of the two padded copies (x-fastest, then y-fastest) of one accumulator.
+__host__ __device__ __forceinline__ long long plane_cells(const RayParams &P)
+{
+    return 2LL * (P.n[0] + 2 * kPlaneHalo) * (P.n[1] + 2 * kPlaneHalo);
+}
 
 struct PlaneCount {
     unsigned n;
@@ -275,7 +283,7 @@ __global__ void __launch_bounds__(32 * CH) plane_forward_kernel(RayParams P,
             const int ka = R.k0 + chunk * len;
             const int kb = min(ka + len - 1, R.k1);
             if (ka <= kb) {
-                PlaneGather op{img, 0.0f};
+                PlaneGather op{img, 0.0f, plane_cells(P)};
                 plane_walk_range(R, ka, kb, op);
                 acc = op.acc;
             }
@@ -287,7 +295,7 @@ __global__ void __launch_bounds__(32 * CH) plane_forward_kernel(RayParams P,
         float sum = 0.0f;
 #pragma unroll
         for (int c = 0; c < CH; ++c) sum = __fadd_rn(sum, part[c][lane]);
-        sino[ray] = __fmul_rn(sum, R.ell);
+        if (ctp_in(ray, sino_cells(P), kSitePlaneSinoStore)) sino[ray] = __fmul_rn(sum, R.ell);
     }
 }
 
@@ -306,6 +314,7 @@ __global__ void __launch_bounds__(32 * CH) plane_backward_kernel(RayParams P,
     if (iu >= P.n_u) return;
     const int view = P.view0 + (int)blockIdx.y;
     const long long ray = (long long)view * P.n_u + iu;
+    if (!ctp_in(ray, sino_cells(P), kSitePlaneSinoLoad)) return;
     const float y = sino[ray];
     if (y == 0.0f) return;
     const PlaneRay R = T[ray];
@@ -314,7 +323,8 @@ __global__ void __launch_bounds__(32 * CH) plane_backward_kernel(RayParams P,
     const int ka = R.k0 + chunk * len;
     const int kb = min(ka + len - 1, R.k1);
     if (ka > kb) return;
-    PlaneScatter op{img + (long long)(view % copies) * copy_cells, __fmul_rn(R.ell, y)};
+    PlaneScatter op{img + (long long)(view % copies) * copy_cells, __fmul_rn(R.ell, y),
+                    plane_cells(P)};
     plane_walk_range(R, ka, kb, op);
 }
 
@@ -411,7 +421,9 @@ struct TileScatter {
     unsigned tb;      // tile extent along the transverse axis
     __device__ __forceinline__ void operator()(int a, float d, bool on, int jb)
     {
-        if (on && d > 0.0f && (unsigned)(jb - jlo) < tb) atomicAdd(tile + a, __fmul_rn(d, w));
+        if (on && d > 0.0f && (unsigned)(jb - jlo) < tb &&
+            ctp_in(a, kTile * (kTile + 1), kSitePlaneTile))
+            atomicAdd(tile + a, __fmul_rn(d, w));
     }
 };
 
@@ -482,6 +494,7 @@ __global__ void __launch_bounds__(256) plane_backward_tiled_kernel(RayParams P,
         }
         for (int iu = u0 + lane; iu <= u1; iu += 32) {
             const long long ray = (long long)s * P.n_u + iu;
+            if (!ctp_in(ray, sino_cells(P), kSitePlaneSinoLoad)) continue;
             const float y = sino[ray];
             if (y == 0.0f) continue;
             const PlaneRay R = T[ray];
@@ -516,7 +529,9 @@ __global__ void __launch_bounds__(256) plane_backward_tiled_kernel(RayParams P,
         const int ly = i / kTile, lx = i % kTile;
         if (lx < tnx && ly < tny) {
             const float v = tile[ly * (kTile + 1) + lx];
-            if (v != 0.0f) atomicAdd(out + (size_t)(ty0 + ly) * P.n[0] + tx0 + lx, v);
+            const long long o = (long long)(ty0 + ly) * P.n[0] + tx0 + lx;
+            if (v != 0.0f && ctp_in(o, (long long)P.n[0] * P.n[1], kSitePlaneTileOut))
+                atomicAdd(out + o, v);
         }
     }
 }

@@ -202,20 +202,28 @@ __device__ __forceinline__ void slab_walk(const SlabRay &R, Op &op)
 struct GatherOp {
     const float *__restrict__ vol;
     float acc;
+    long long lim;  // cells of vol (bounds-checked builds)
     __device__ __forceinline__ void operator()(int a, float d, bool on)
     {
-        if (on) acc = __fmaf_rn(d, __ldg(vol + a), acc);
+        if (on && ctp_in(a, lim, kSiteRayGather)) acc = __fmaf_rn(d, __ldg(vol + a), acc);
     }
 };
 
 struct ScatterOp {
     float *__restrict__ vol;
     float w;  // ell * y
+    long long lim;
     __device__ __forceinline__ void operator()(int a, float d, bool on)
     {
-        if (on) atomicAdd(vol + a, __fmul_rn(d, w));
+        if (on && ctp_in(a, lim, kSiteRayScatter)) atomicAdd(vol + a, __fmul_rn(d, w));
     }
 };
+
+// Cells of the (nz, ny, nx) volume the ray path addresses.
+__host__ __device__ __forceinline__ long long volume_cells(const RayParams &P)
+{
+    return (long long)P.n[0] * P.n[1] * P.n[2];
+}
 
 // Counts the pieces longer than thr slab units (the counting threshold over
 // the ray's length per slab).
@@ -240,11 +248,12 @@ __global__ void __launch_bounds__(TU *TV) ray_forward_kernel(RayParams P,
     float out = 0.0f;
     SlabRay R;
     if (slab_setup(P, view, iu, iv, R)) {
-        GatherOp op{vol, 0.0f};
+        GatherOp op{vol, 0.0f, volume_cells(P)};
         slab_walk(R, op);
         out = __fmul_rn(op.acc, R.ell);
     }
-    sino[((long long)view * P.n_v + iv) * P.n_u + iu] = out;
+    const long long ray = ((long long)view * P.n_v + iv) * P.n_u + iu;
+    if (ctp_in(ray, sino_cells(P), kSiteRaySinoStore)) sino[ray] = out;
 }
 
 template <int TU, int TV>
@@ -256,11 +265,13 @@ __global__ void __launch_bounds__(TU *TV) ray_backward_kernel(RayParams P,
     const int iv = blockIdx.z * TV + (int)(threadIdx.x / TU);
     const int view = P.view0 + (int)blockIdx.y;
     if (iu >= P.n_u || iv >= P.n_v) return;
-    const float y = sino[((long long)view * P.n_v + iv) * P.n_u + iu];
+    const long long ray = ((long long)view * P.n_v + iv) * P.n_u + iu;
+    if (!ctp_in(ray, sino_cells(P), kSiteRaySinoLoad)) return;
+    const float y = sino[ray];
     if (y == 0.0f) return;
     SlabRay R;
     if (slab_setup(P, view, iu, iv, R)) {
-        ScatterOp op{vol, __fmul_rn(R.ell, y)};
+        ScatterOp op{vol, __fmul_rn(R.ell, y), volume_cells(P)};
         slab_walk(R, op);
     }
 }

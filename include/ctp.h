@@ -333,6 +333,22 @@ int ctp_parker_weights(const ctp_plan_t *plan, float *weight_dev, void *stream);
 int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *weight_dev,
                      double *grad_dev, void *stream);
 
+/*
+ * ctp_check_violations -- the bounds-checked debug build (the library compiled
+ * with -DCTP_CHECK, libctp_check.so) tests, before each access, the index of
+ * every global load, store and reduction of the projector walks (ray, column
+ * and plane paths, their sinogram reads and writes, the column path's layout
+ * transposes) and every shared-memory reduction of the tiled 2-D backward
+ * against its buffer's extent; an access outside is skipped and counted.  This
+ * call waits for the device, returns the count since the previous call, the
+ * first offending index, its buffer's extent and the access site (the CheckSite
+ * values of the library's sources), and resets them.  All four pointers are
+ * host outputs.  Errors: CTP_E_NULL; CTP_E_OPTION in normal builds (outputs
+ * zeroed); CTP_E_CUDA.
+ */
+int ctp_check_violations(unsigned long long *count, long long *index, long long *extent,
+                         int *site);
+
 /* Static English text of a status code. */
 const char *ctp_status_string(int status);
 

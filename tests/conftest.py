@@ -18,3 +18,17 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(autouse=True)
+def _no_out_of_range_access():
+    """Under the bounds-checked library (CTP_LIBRARY_VARIANT=check) every test
+    must end with no walk access outside its buffer."""
+    yield
+    if os.environ.get("CTP_LIBRARY_VARIANT") != "check":
+        return
+    import back_projection_ctp_b300._binding as b
+    if b._lib is None:
+        return
+    count, index, extent, site = b.ctp_check_violations()
+    assert count == 0, f"{count} out-of-range accesses (first: index {index} of {extent}, site {site})"

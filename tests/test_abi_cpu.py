@@ -131,3 +131,17 @@ def test_parallel_direction_along_detector_is_rejected():
     f = _cone()
     f["src"] = f["det_u"].copy()  # ray direction lying in the detector plane
     assert _plan_status(f, beam="parallel") == 4
+
+
+def test_normal_build_has_no_access_counters():
+    """ctp_check_violations answers CTP_E_OPTION (outputs zeroed) unless the
+    library was compiled with CTP_CHECK; no device is needed for the answer."""
+    if os.environ.get("CTP_LIBRARY_VARIANT") == "check":
+        pytest.skip("running against the checked library")
+    lib = B.load_library()
+    c, i, e, s = ctypes.c_ulonglong(7), ctypes.c_longlong(7), ctypes.c_longlong(7), ctypes.c_int(7)
+    st = lib.ctp_check_violations(ctypes.byref(c), ctypes.byref(i), ctypes.byref(e), ctypes.byref(s))
+    assert st == 11 and (c.value, i.value, e.value, s.value) == (0, 0, 0, 0)
+    assert lib.ctp_check_violations(None, ctypes.byref(i), ctypes.byref(e), ctypes.byref(s)) == 1
+    with pytest.raises(ctp.CtpError):
+        ctp.ctp_check_violations()
