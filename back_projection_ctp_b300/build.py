@@ -14,7 +14,7 @@ LIB = os.path.join(HERE, "libctp.so")
 CHECK_LIB = os.path.join(HERE, "libctp_check.so")
 SOURCES = ["ctp_api.cu"]
 DEPS = ["ctp_api.cu", "ctp_ray.cuh", "ctp_column.cuh", "ctp_plane.cuh", "ctp_fdk.cuh",
-        "ctp_geometry.cuh", "ctp_internal.h"]
+        "ctp_geometry.cuh", "ctp_internal.h", "ctp_check.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

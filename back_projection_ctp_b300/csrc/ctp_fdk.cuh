@@ -39,6 +39,14 @@
 
 #include <cuda_runtime.h>
 
+#include "ctp_check.h"
+
+// Operands of the bounds-check hooks (they appear only inside CTP_AND_IN and
+// CTP_CHECKED_LDG, which drop them in normal builds): the element of row iv,
+// column C.iu of a view's detector plane, and the plane's size.
+#define CTP_FDK_ELEM ((long long)iv * F.n_u + C.iu)
+#define CTP_FDK_PLANE ((long long)F.n_u * F.n_v)
+
 namespace ctp {
 
 constexpr double kFixOne = 1099511627776.0;  // 2^40
@@ -185,8 +193,11 @@ __device__ __forceinline__ void gather_column(const FdkParams &F, const ColumnVi
 #pragma unroll
         for (int t = 0; t < K; ++t) {
             const float *row = col + (long long)iv * F.n_u;
-            const float a0 = __ldg(row), a1 = __ldg(row + 1);
-            const float b0 = __ldg(row + F.n_u), b1 = __ldg(row + F.n_u + 1);
+            const float a0 = CTP_CHECKED_LDG(row, CTP_FDK_ELEM, CTP_FDK_PLANE, kSiteFdkGather),
+                        a1 = CTP_CHECKED_LDG(row + 1, CTP_FDK_ELEM + 1, CTP_FDK_PLANE, kSiteFdkGather);
+            const float b0 = CTP_CHECKED_LDG(row + F.n_u, CTP_FDK_ELEM + F.n_u, CTP_FDK_PLANE, kSiteFdkGather),
+                        b1 = CTP_CHECKED_LDG(row + F.n_u + 1, CTP_FDK_ELEM + F.n_u + 1, CTP_FDK_PLANE,
+                                             kSiteFdkGather);
             const float a = __fmaf_rn(C.fu, a1 - a0, a0);
             const float b = __fmaf_rn(C.fu, b1 - b0, b0);
             acc[t] = __fmaf_rn(C.w, __fmaf_rn(fv, b - a, a), acc[t]);
@@ -205,10 +216,14 @@ __device__ __forceinline__ void gather_column(const FdkParams &F, const ColumnVi
         const bool r1 = (unsigned)(iv + 1) < (unsigned)F.n_v;
         if (r0 || r1) {
             const float *row = base + (long long)iv * F.n_u + C.iu;
-            const float a0 = (r0 && C.c0) ? __ldg(row) : 0.0f;
-            const float a1 = (r0 && C.c1) ? __ldg(row + 1) : 0.0f;
-            const float b0 = (r1 && C.c0) ? __ldg(row + F.n_u) : 0.0f;
-            const float b1 = (r1 && C.c1) ? __ldg(row + F.n_u + 1) : 0.0f;
+            const float a0 = (r0 && C.c0 CTP_AND_IN(CTP_FDK_ELEM, CTP_FDK_PLANE, kSiteFdkGather)) ? __ldg(row)
+                                                                                     : 0.0f;
+            const float a1 = (r0 && C.c1 CTP_AND_IN(CTP_FDK_ELEM + 1, CTP_FDK_PLANE, kSiteFdkGather))
+                                 ? __ldg(row + 1) : 0.0f;
+            const float b0 = (r1 && C.c0 CTP_AND_IN(CTP_FDK_ELEM + F.n_u, CTP_FDK_PLANE, kSiteFdkGather))
+                                 ? __ldg(row + F.n_u) : 0.0f;
+            const float b1 = (r1 && C.c1 CTP_AND_IN(CTP_FDK_ELEM + F.n_u + 1, CTP_FDK_PLANE, kSiteFdkGather))
+                                 ? __ldg(row + F.n_u + 1) : 0.0f;
             const float a = __fmaf_rn(C.fu, a1 - a0, a0);
             const float b = __fmaf_rn(C.fu, b1 - b0, b0);
             acc[t] = __fmaf_rn(C.w, __fmaf_rn(fv, b - a, a), acc[t]);
@@ -229,7 +244,9 @@ __device__ __forceinline__ void store_column(const FdkParams &F, int i, int j, i
     const int kn = F.ndim == 2 ? 1 : K;
 #pragma unroll
     for (int t = 0; t < K; ++t)
-        if (t < kn && k0 + t < F.n[2])
+        if (t < kn && k0 + t < F.n[2] CTP_AND_IN(((long long)(k0 + t) * F.n[1] + j) * F.n[0] + i,
+                                                 (long long)F.n[0] * F.n[1] * F.n[2],
+                                                 kSiteFdkStore))
             vol[((long long)(k0 + t) * F.n[1] + j) * F.n[0] + i] = acc[t];
 }
 
@@ -252,8 +269,10 @@ __global__ void __launch_bounds__(256, K > 1 ? 5 : 8) wbp_gather_kernel(FdkParam
         if (!fdk_column_view(F, F.views[s], i, j, k0, C)) continue;
         const float *base = q + s * plane;
         if (F.ndim == 2) {
-            const float a0 = C.c0 ? __ldg(base + C.iu) : 0.0f;
-            const float a1 = C.c1 ? __ldg(base + C.iu + 1) : 0.0f;
+            const float a0 = C.c0 CTP_AND_IN(C.iu, CTP_FDK_PLANE, kSiteFdkGather) ? __ldg(base + C.iu)
+                                                                          : 0.0f;
+            const float a1 = C.c1 CTP_AND_IN(C.iu + 1, CTP_FDK_PLANE, kSiteFdkGather)
+                                 ? __ldg(base + C.iu + 1) : 0.0f;
             acc[0] = __fmaf_rn(C.w, __fmaf_rn(C.fu, a1 - a0, a0), acc[0]);
             continue;
         }
@@ -284,7 +303,9 @@ __global__ void __launch_bounds__(256, K > 1 ? 4 : 8) wbp_scatter_kernel(FdkPara
     float g[K];
 #pragma unroll
     for (int t = 0; t < K; ++t)
-        g[t] = (t < kn && k0 + t < F.n[2])
+        g[t] = (t < kn && k0 + t < F.n[2] CTP_AND_IN(((long long)(k0 + t) * F.n[1] + j) * F.n[0] + i,
+                                                     (long long)F.n[0] * F.n[1] * F.n[2],
+                                                     kSiteFdkScatterLoad))
                    ? vol[((long long)(k0 + t) * F.n[1] + j) * F.n[0] + i] : 0.0f;
     const long long plane = (long long)F.n_u * F.n_v;
     for (int s = 0; s < F.n_views; ++s) {
@@ -294,8 +315,10 @@ __global__ void __launch_bounds__(256, K > 1 ? 4 : 8) wbp_scatter_kernel(FdkPara
             float *base = q + s * plane;
             const float val = C.w * g[0];
             if (val != 0.0f) {
-                if (C.c0) atomicAdd(base + C.iu, val * (1.0f - C.fu));
-                if (C.c1) atomicAdd(base + C.iu + 1, val * C.fu);
+                if (C.c0 CTP_AND_IN(C.iu, CTP_FDK_PLANE, kSiteFdkScatter))
+                    atomicAdd(base + C.iu, val * (1.0f - C.fu));
+                if (C.c1 CTP_AND_IN(C.iu + 1, CTP_FDK_PLANE, kSiteFdkScatter))
+                    atomicAdd(base + C.iu + 1, val * C.fu);
             }
             continue;
         }
@@ -306,8 +329,10 @@ __global__ void __launch_bounds__(256, K > 1 ? 4 : 8) wbp_scatter_kernel(FdkPara
         auto flush = [&](int r, float x) {
             if ((unsigned)r < (unsigned)F.n_v && x != 0.0f) {
                 float *px = col + (long long)r * F.n_u;
-                if (C.c0) atomicAdd(px, x * wu0);
-                if (C.c1) atomicAdd(px + 1, x * wu1);
+                if (C.c0 CTP_AND_IN((long long)r * F.n_u + C.iu, CTP_FDK_PLANE, kSiteFdkScatter))
+                    atomicAdd(px, x * wu0);
+                if (C.c1 CTP_AND_IN((long long)r * F.n_u + C.iu + 1, CTP_FDK_PLANE, kSiteFdkScatter))
+                    atomicAdd(px + 1, x * wu1);
             }
         };
         int P = C.iv;

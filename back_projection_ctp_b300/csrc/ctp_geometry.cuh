@@ -30,9 +30,14 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "ctp_check.h"
 #include "ctp_column.cuh"
 #include "ctp_internal.h"
 #include "ctp_ray.cuh"
+
+// Operand of the bounds-check hooks (dropped in normal builds): cells of the
+// padded z-fastest working copy the column walk reads.
+#define CTP_GEOM_CELLS ((long long)column_padded_cells(P))
 
 namespace ctp {
 
@@ -98,8 +103,10 @@ __device__ __forceinline__ void grad_add_bc(GradSums &G, bool on_b, float j, flo
     }
 }
 
+// nvol: cells of vol, read by the bounds-check hooks only.
 __device__ __forceinline__ void grad_walk(const SlabRay &R, const RayAxes &A,
-                                          const float *__restrict__ vol, GradSums &G)
+                                          const float *__restrict__ vol, long long nvol,
+                                          GradSums &G)
 {
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
@@ -131,9 +138,12 @@ __device__ __forceinline__ void grad_walk(const SlabRay &R, const RayAxes &A,
         const int jb3 = jb + (cb ? 1 : 0), jc3 = jc + (cc ? 1 : 0);
         const int a2 = addr + (bfirst ? R.sb : R.sc);
         const int a3 = addr + (cb ? R.sb : 0) + (cc ? R.sc : 0);
-        const float v1 = ((unsigned)jb < nb && (unsigned)jc < nc) ? __ldg(vol + addr) : 0.0f;
-        const float v2 = ((unsigned)jb2 < nb && (unsigned)jc2 < nc) ? __ldg(vol + a2) : 0.0f;
-        const float v3 = ((unsigned)jb3 < nb && (unsigned)jc3 < nc) ? __ldg(vol + a3) : 0.0f;
+        const float v1 = ((unsigned)jb < nb && (unsigned)jc < nc
+                              CTP_AND_IN(addr, nvol, kSiteGeomRayLoad)) ? __ldg(vol + addr) : 0.0f;
+        const float v2 = ((unsigned)jb2 < nb && (unsigned)jc2 < nc
+                              CTP_AND_IN(a2, nvol, kSiteGeomRayLoad)) ? __ldg(vol + a2) : 0.0f;
+        const float v3 = ((unsigned)jb3 < nb && (unsigned)jc3 < nc
+                              CTP_AND_IN(a3, nvol, kSiteGeomRayLoad)) ? __ldg(vol + a3) : 0.0f;
         G.path = __fmaf_rn(d1, v1, __fmaf_rn(d2, v2, __fmaf_rn(d3, v3, G.path)));
         const float tk = __fmaf_rn((float)(k - R.k0), tinv, t0);  // t at the slab start
         // the p plane at the slab start: crossed unless the ray begins in this slab
@@ -186,7 +196,7 @@ __global__ void __launch_bounds__(TU *TV) geometry_vjp_kernel(RayParams P, GeomP
             RayAxes A;
             ray_axes(P, view, iu, iv, A);
             GradSums S;
-            grad_walk(R, A, vol, S);
+            grad_walk(R, A, vol, volume_cells(P), S);
             const float p = __fmul_rn(S.path, R.ell);
             const float rn2 = __fmul_rn(A.rn, A.rn);
             const float alpha = ((float)iu - Q.cu) * Q.pitch_u;
@@ -223,7 +233,8 @@ __global__ void __launch_bounds__(TU *TV) geometry_vjp_kernel(RayParams P, GeomP
         double s = 0.0;
 #pragma unroll
         for (int q = 0; q < kWarps; ++q) s += (double)part[q][threadIdx.x];
-        atomicAdd(out + 12 * (long long)view + threadIdx.x, s);
+        if (true CTP_AND_IN(12 * (long long)view + threadIdx.x, 12LL * P.n_views, kSiteGeomOut))
+            atomicAdd(out + 12 * (long long)view + threadIdx.x, s);
     }
 }
 
@@ -276,7 +287,9 @@ __global__ void __launch_bounds__(256, 4) column_gvjp_kernel(RayParams P, GeomPa
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int iv = row0 + 32 * r;
-            wr[r] = iv < P.n_v ? wsino[((long long)view * P.n_v + iv) * P.n_u + iu] : 0.0f;
+            wr[r] = iv < P.n_v CTP_AND_IN(((long long)view * P.n_v + iv) * P.n_u + iu, sino_cells(P),
+                                          kSiteGeomSinoLoad)
+                        ? wsino[((long long)view * P.n_v + iv) * P.n_u + iu] : 0.0f;
             Z[r] = wr[r] != 0.0f ? column_row_setup(P, C, iv) : column_row_idle();
             acc[r] = fprev[r] = dfp[r] = dfb[r] = dfz[r] = dtp[r] = dtb[r] = dtz[r] = 0.0f;
         }
@@ -301,8 +314,13 @@ __global__ void __launch_bounds__(256, 4) column_gvjp_kernel(RayParams P, GeomPa
                     const bool cz = gz < Z[r].fz;
                     const float tz = fmaxf(__fmaf_rn(-__uint2float_rn(gz), Z[r].ibz, 1.0f), 0.0f);
                     const int za = Z[r].zoff, z1 = za + Z[r].sz;
-                    const float vA = (unsigned)za < nz ? __ldg(zvol + xy + za) : 0.0f;
-                    const float vB = cz ? ((unsigned)z1 < nz ? __ldg(zvol + xy + z1) : 0.0f) : vA;
+                    const float vA = (unsigned)za < nz CTP_AND_IN(xy + za, CTP_GEOM_CELLS,
+                                                                  kSiteGeomColumnLoad)
+                                         ? __ldg(zvol + xy + za) : 0.0f;
+                    const float vB = cz ? ((unsigned)z1 < nz CTP_AND_IN(xy + z1, CTP_GEOM_CELLS,
+                                                                        kSiteGeomColumnLoad)
+                                               ? __ldg(zvol + xy + z1) : 0.0f)
+                                        : vA;
                     const float e1 = cz ? tz : 1.0f;
                     acc[r] = __fmaf_rn(e1, vA, __fmaf_rn(__fsub_rn(1.0f, e1), vB, acc[r]));
                     const float j = fprev[r] - vA;
@@ -336,9 +354,15 @@ __global__ void __launch_bounds__(256, 4) column_gvjp_kernel(RayParams P, GeomPa
                 // cells: A before both crossings, B after the first, C after both
                 const int zb = bfirst ? za : (cz ? z1 : za), xyb = bfirst ? xy + C.sb : xy;
                 const int zc = cz ? z1 : za, xyc = cb ? xy + C.sb : xy;
-                const float vA = (unsigned)za < nz ? __ldg(zvol + xy + za) : 0.0f;
-                const float vB = (unsigned)zb < nz ? __ldg(zvol + xyb + zb) : 0.0f;
-                const float vC = (unsigned)zc < nz ? __ldg(zvol + xyc + zc) : 0.0f;
+                const float vA = (unsigned)za < nz CTP_AND_IN(xy + za, CTP_GEOM_CELLS,
+                                                              kSiteGeomColumnLoad)
+                                     ? __ldg(zvol + xy + za) : 0.0f;
+                const float vB = (unsigned)zb < nz CTP_AND_IN(xyb + zb, CTP_GEOM_CELLS,
+                                                              kSiteGeomColumnLoad)
+                                     ? __ldg(zvol + xyb + zb) : 0.0f;
+                const float vC = (unsigned)zc < nz CTP_AND_IN(xyc + zc, CTP_GEOM_CELLS,
+                                                              kSiteGeomColumnLoad)
+                                     ? __ldg(zvol + xyc + zc) : 0.0f;
                 const float e1 = fminf(fmaxf(x1, lo), hi), e2 = fminf(fmaxf(x2, lo), hi);
                 acc[r] = __fmaf_rn(__fsub_rn(e1, lo), vA,
                                    __fmaf_rn(__fsub_rn(e2, e1), vB,
@@ -417,7 +441,8 @@ __global__ void __launch_bounds__(256, 4) column_gvjp_kernel(RayParams P, GeomPa
         double sum = 0.0;
 #pragma unroll
         for (int q = 0; q < kColumnsPerBlock; ++q) sum += (double)part[q][threadIdx.x];
-        atomicAdd(out + 12 * (long long)view + threadIdx.x, sum);
+        if (true CTP_AND_IN(12 * (long long)view + threadIdx.x, 12LL * P.n_views, kSiteGeomOut))
+            atomicAdd(out + 12 * (long long)view + threadIdx.x, sum);
     }
 }
 

@@ -338,8 +338,10 @@ int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *
  * with -DCTP_CHECK, libctp_check.so) tests, before each access, the index of
  * every global load, store and reduction of the projector walks (ray, column
  * and plane paths, their sinogram reads and writes, the column path's layout
- * transposes) and every shared-memory reduction of the tiled 2-D backward
- * against its buffer's extent; an access outside is skipped and counted.  This
+ * transposes), every shared-memory reduction of the tiled 2-D backward, the
+ * weighted backprojection's and its transpose's loads, stores and reductions
+ * and the geometry-gradient walks' loads and outputs against the buffer's
+ * extent; an access outside is skipped and counted.  This
  * call waits for the device, returns the count since the previous call, the
  * first offending index, its buffer's extent and the access site (the CheckSite
  * values of the library's sources), and resets them.  All four pointers are
