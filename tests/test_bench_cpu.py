@@ -76,3 +76,30 @@ def test_reference_arm_under_two_ranks_prints_once():
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1 and json.loads(lines[0])["impl"] == "reference"
+
+
+def test_stored_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
+    """roofline.traffic comes from profiles/traffic.json only while the profiled
+    kernel's own sources (comments and blank space aside) match the capture."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for kernel in ("column_forward_kernel", "column_backward_kernel"):
+        assert bench.stored_traffic(kernel, "c4_cone_512_aniso") > 0
+    csrc = tmp_path / "csrc"
+    csrc.mkdir()
+    for name in os.listdir(bench.CSRC):
+        (csrc / name).write_text(open(os.path.join(bench.CSRC, name)).read())
+    monkeypatch.setattr(bench, "CSRC", str(csrc))
+    kernel = "column_forward_kernel"
+    h = bench.source_hash(kernel)
+    f = csrc / "ctp_column.cuh"
+    text = f.read_text()
+    f.write_text(text.replace("namespace ctp {", "namespace ctp {\n// a new comment\n\n", 1))
+    assert bench.source_hash(kernel) == h  # comments and blank lines do not count
+    assert bench.stored_traffic(kernel, "c4_cone_512_aniso") > 0
+    f.write_text(text.replace("constexpr int kHalo = 2;", "constexpr int kHalo = 3;", 1))
+    assert bench.source_hash(kernel) != h
+    assert bench.stored_traffic(kernel, "c4_cone_512_aniso") is None
+    (csrc / "ctp_fdk.cuh").write_text("// unrelated file changed\nint x;\n")
+    f.write_text(text)
+    assert bench.stored_traffic(kernel, "c4_cone_512_aniso") > 0
