@@ -48,12 +48,40 @@ class _Volume(ctypes.Structure):
                 ("ox", ctypes.c_double), ("oy", ctypes.c_double), ("oz", ctypes.c_double)]
 
 
+class _PlanOptions(ctypes.Structure):
+    _fields_ = [("rows_forward", ctypes.c_int), ("rows_backward", ctypes.c_int),
+                ("backward_rows_adjacent", ctypes.c_int), ("plane_backward", ctypes.c_int),
+                ("host_chunks", ctypes.c_int), ("geometry_walk", ctypes.c_int)]
+
+
+# Work-layout options of a plan (include/ctp.h, ctp_plan_options); keyword values
+# accepted by ctp_plan(..., options=...).
+PLANE_BACKWARD = {"auto": 0, "tiled": 1, "privatised": 2}
+GEOMETRY_WALK = {"auto": 0, "ray": 1}
+
+
+def _plan_options(options):
+    if not options:
+        return None
+    o = _PlanOptions()
+    for key, value in options.items():
+        if key == "plane_backward":
+            value = PLANE_BACKWARD[value] if isinstance(value, str) else value
+        elif key == "geometry_walk":
+            value = GEOMETRY_WALK[value] if isinstance(value, str) else value
+        elif key not in ("rows_forward", "rows_backward", "backward_rows_adjacent",
+                         "host_chunks"):
+            raise ValueError(f"unknown plan option {key!r}")
+        setattr(o, key, int(value))
+    return o
+
+
 class _PlanInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("device", ctypes.c_int), ("n_rays", ctypes.c_longlong),
                 ("n_cells", ctypes.c_longlong), ("device_bytes", ctypes.c_ulonglong)]
 
 
-EXPORTS = ("ctp_plan", "ctp_destroy", "ctp_plan_info_get", "ctp_forward", "ctp_backward",
+EXPORTS = ("ctp_plan", "ctp_plan_ex", "ctp_destroy", "ctp_plan_info_get", "ctp_forward", "ctp_backward",
            "ctp_segment_count", "ctp_forward_host", "ctp_backward_host", "ctp_status_string",
            "ctp_forward_static", "ctp_ramp_filter", "ctp_weighted_backproject",
            "ctp_weighted_backproject_transpose", "ctp_fdk", "ctp_geometry_vjp",
@@ -78,6 +106,8 @@ def load_library(path: str | None = None):
         P, I = ctypes.c_void_p, ctypes.c_int
         lib.ctp_plan.argtypes = [ctypes.POINTER(_Geometry), ctypes.POINTER(_Volume), I,
                                  ctypes.POINTER(ctypes.c_void_p)]
+        lib.ctp_plan_ex.argtypes = [ctypes.POINTER(_Geometry), ctypes.POINTER(_Volume), I,
+                                    ctypes.POINTER(_PlanOptions), ctypes.POINTER(ctypes.c_void_p)]
         lib.ctp_destroy.argtypes = [P]
         lib.ctp_destroy.restype = None
         lib.ctp_plan_info_get.argtypes = [P, ctypes.POINTER(_PlanInfo)]
@@ -218,7 +248,15 @@ def _pixel_offsets(geometry: Geometry, g: _Geometry):
 
 def ctp_forward_static(geometry: Geometry, volume: Volume, vol, sino, stream=None):
     """sino <- A vol with no allocation (per-view frames in a fixed device array of
-    at most 4096 views); equals ctp_forward of a "ray" plan of the same scan."""
+    at most 4096 views); equals ctp_forward of a "ray" plan of the same scan.
+    ``vol`` and ``sino`` must live on the current CUDA device, where the call
+    runs."""
+    import torch
+    cur = torch.cuda.current_device()
+    for name, t in (("vol", vol), ("sino", sino)):
+        if isinstance(t, torch.Tensor) and t.is_cuda and t.device.index != cur:
+            raise ValueError(f"{name} is on cuda:{t.device.index}, the current device is "
+                             f"cuda:{cur}")
     g, v, arrays = _c_scan(geometry, volume)
     n_views = arrays[0].shape[0]
     shape_v = tuple(int(s) for s in volume.shape)
@@ -230,8 +268,14 @@ def ctp_forward_static(geometry: Geometry, volume: Volume, vol, sino, stream=Non
     return sino
 
 
-def ctp_plan(geometry: Geometry, volume: Volume, path: str = "auto") -> Plan:
+def ctp_plan(geometry: Geometry, volume: Volume, path: str = "auto", options=None) -> Plan:
+    """Plan a scan on the current CUDA device.  ``options``: None, or a dict of
+    work-layout options (``rows_forward``, ``rows_backward``,
+    ``backward_rows_adjacent``, ``plane_backward`` ("auto" / "tiled" /
+    "privatised"), ``host_chunks``, ``geometry_walk`` ("auto" / "ray")); they
+    select among layouts that compute the same operator."""
     lib = load_library()
+    opts = _plan_options(options)
     arrays = [np.ascontiguousarray(a, dtype=np.float32).reshape(-1, 3)
               for a in (geometry.src, geometry.det_centre, geometry.det_u, geometry.det_v)]
     n_views = arrays[0].shape[0]
@@ -251,8 +295,12 @@ def ctp_plan(geometry: Geometry, volume: Volume, path: str = "auto") -> Plan:
     v.dx, v.dy, v.dz = dx, dy, dz
     v.ox, v.oy, v.oz = (float(s) for s in volume.origin)
     h = ctypes.c_void_p()
-    _check(lib.ctp_plan(ctypes.byref(g), ctypes.byref(v), PATHS[path], ctypes.byref(h)),
-           "ctp_plan")
+    if opts is None:
+        _check(lib.ctp_plan(ctypes.byref(g), ctypes.byref(v), PATHS[path], ctypes.byref(h)),
+               "ctp_plan")
+    else:
+        _check(lib.ctp_plan_ex(ctypes.byref(g), ctypes.byref(v), PATHS[path], ctypes.byref(opts),
+                               ctypes.byref(h)), "ctp_plan_ex")
     geometry = dataclasses.replace(geometry, src=arrays[0], det_centre=arrays[1],
                                    det_u=arrays[2], det_v=arrays[3], pixel_offsets=offsets)
     return Plan(h.value, geometry, volume)

@@ -12,6 +12,9 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libctp.so")
 # bounds-checked debug build (-DCTP_CHECK): every walk access tested and counted
 CHECK_LIB = os.path.join(HERE, "libctp_check.so")
+# bandwidth probes of the benchmark's L2 roofline (measurement only)
+PROBE_LIB = os.path.join(HERE, "libctp_probe.so")
+PROBE_SOURCE = "ctp_probe.cu"
 SOURCES = ["ctp_api.cu"]
 DEPS = ["ctp_api.cu", "ctp_ray.cuh", "ctp_column.cuh", "ctp_plane.cuh", "ctp_fdk.cuh",
         "ctp_geometry.cuh", "ctp_internal.h", "ctp_check.h"]
@@ -43,6 +46,23 @@ def build(force: bool = False, verbose: bool = False, check: bool = False) -> st
     return lib
 
 
+def build_probe(force: bool = False) -> str:
+    """Build ``libctp_probe.so``, the benchmark's L2 bandwidth probes."""
+    src = os.path.join(CSRC, PROBE_SOURCE)
+    if (not force and os.path.exists(PROBE_LIB)
+            and os.path.getmtime(PROBE_LIB) >= os.path.getmtime(src)):
+        return PROBE_LIB
+    nvcc = os.environ.get("NVCC", "nvcc")
+    tmp = PROBE_LIB + f".tmp{os.getpid()}"
+    subprocess.run([nvcc, *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
+                    "-shared", "-o", tmp, src], check=True)
+    os.replace(tmp, PROBE_LIB)
+    return PROBE_LIB
+
+
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                check="--check" in sys.argv))
+    if "--probe" in sys.argv:
+        print(build_probe(force="--force" in sys.argv))
+    else:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                    check="--check" in sys.argv))

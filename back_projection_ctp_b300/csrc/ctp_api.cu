@@ -9,10 +9,11 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
-#include <atomic>
+#include <mutex>
 #include <new>
 #include <vector>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "ctp.h"
@@ -55,6 +56,7 @@ struct ctp_plan {
     ctp::FdkView *d_fdk = nullptr;
     float *d_ramp[ctp::kRampKinds] = {};    // ramp kernels (2 n_u - 1) by ctp_ramp value
     unsigned long long device_bytes = 0;
+    ctp_plan_options opt{};                 // work-layout options (all zero: defaults)
 };
 
 namespace {
@@ -161,7 +163,8 @@ int forward_walk(const ctp_plan_t *plan, int v0, int nv, const float *vol, float
 // Small 2-D scans take a single tiled launch over all views instead.
 bool backward_whole(const ctp_plan_t *plan)
 {
-    return plan->path == CTP_PATH_PLANE && ctp::plane_backward_tiled(ray_params(plan));
+    return plan->path == CTP_PATH_PLANE &&
+           ctp::plane_backward_tiled(ray_params(plan), plan->opt.plane_backward);
 }
 
 int backward_in(const ctp_plan_t *plan, float *vol, cudaStream_t s)
@@ -333,12 +336,64 @@ int fdk_setup(ctp_plan_t *p, const ctp_geometry *g, const ctp_volume *v)
     return CTP_OK;
 }
 
-// CTP_GEOMETRY_RAY = 1 runs the geometry gradients on the ray walk for every
-// plan (a cross-check of the column walk).
-bool column_gvjp_disabled()
+// Per-view frame of a flat detector in cell coordinates (float64): the source
+// (divergent) or ray direction (parallel) a, pixel (0, 0) p00 and the pixel
+// steps du, dv along u and v.  ctp_plan and ctp_forward_static both take their
+// frames from here.
+void flat_view_frame(const ctp_geometry *g, const ctp_volume *v, int s, ctp::ViewFrame *F)
 {
-    const char *env = getenv("CTP_GEOMETRY_RAY");
-    return env && env[0] == '1';
+    const double spacing[3] = {v->dx, v->dy, v->dz};
+    const double origin[3] = {v->ox, v->oy, v->oz};
+    const double cu = 0.5 * (g->n_u - 1) - g->offset_u;
+    const double cv = 0.5 * (g->n_v - 1) - g->offset_v;
+    const float *S = g->src + 3 * s, *C = g->det_centre + 3 * s;
+    const float *U = g->det_u + 3 * s, *V = g->det_v + 3 * s;
+    for (int a = 0; a < 3; ++a) {
+        const double d = spacing[a], o = origin[a];
+        const double pu = g->pitch_u * (double)U[a];
+        const double pv = g->pitch_v * (double)V[a];
+        // pixel (0, 0) = centre - cu * pitch_u * u - cv * pitch_v * v
+        const double p00 = (double)C[a] - cu * pu - cv * pv;
+        F->a[a] = g->beam == CTP_DIVERGENT ? ((double)S[a] - o) / d : (double)S[a] / d;
+        F->p00[a] = (p00 - o) / d;
+        F->du[a] = pu / d;
+        F->dv[a] = pv / d;
+        F->dn[a] = 0.0;
+    }
+}
+
+// Per-view frame of a curved detector: pixel = centre + t u + s v + e n with
+// per-pixel offsets in physical units; p00 holds the centre, du / dv / dn the
+// unit axes and the unit normal n = u x v / |u x v|, all in cell coordinates.
+void curved_view_frame(const ctp_geometry *g, const ctp_volume *v, int s, ctp::ViewFrame *F)
+{
+    const double spacing[3] = {v->dx, v->dy, v->dz};
+    const double origin[3] = {v->ox, v->oy, v->oz};
+    const float *S = g->src + 3 * s, *C = g->det_centre + 3 * s;
+    const float *U = g->det_u + 3 * s, *V = g->det_v + 3 * s;
+    const double Ud[3] = {U[0], U[1], U[2]}, Vd[3] = {V[0], V[1], V[2]};
+    double N[3];
+    cross3(Ud, Vd, N);
+    const double nn = norm3(N);
+    for (int a = 0; a < 3; ++a) {
+        const double d = spacing[a], o = origin[a];
+        F->a[a] = g->beam == CTP_DIVERGENT ? ((double)S[a] - o) / d : (double)S[a] / d;
+        F->p00[a] = ((double)C[a] - o) / d;
+        F->du[a] = Ud[a] / d;
+        F->dv[a] = Vd[a] / d;
+        F->dn[a] = N[a] / nn / d;
+    }
+}
+
+int validate_options(const ctp_plan_options *o)
+{
+    if (!o) return CTP_OK;
+    const bool ok = o->rows_forward >= 0 && o->rows_forward <= 4 && o->rows_backward >= 0 &&
+                    o->rows_backward <= 4 &&
+                    (o->backward_rows_adjacent == 0 || o->backward_rows_adjacent == 1) &&
+                    o->plane_backward >= 0 && o->plane_backward <= 2 && o->host_chunks >= 0 &&
+                    o->host_chunks <= 64 && (o->geometry_walk == 0 || o->geometry_walk == 1);
+    return ok ? CTP_OK : CTP_E_OPTION;
 }
 
 int fdk_check(const ctp_plan_t *plan)
@@ -399,17 +454,26 @@ int ctp_check_violations(unsigned long long *count, long long *index, long long 
 
 int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan_t **out)
 {
+    return ctp_plan_ex(geom, vol, path, nullptr, out);
+}
+
+int ctp_plan_ex(const ctp_geometry *geom, const ctp_volume *vol, int path,
+                const ctp_plan_options *options, ctp_plan_t **out)
+{
     if (!out) return CTP_E_NULL;
     *out = nullptr;
     if (!geom || !vol) return CTP_E_NULL;
     if (path != CTP_PATH_AUTO && path != CTP_PATH_RAY && path != CTP_PATH_COLUMN &&
         path != CTP_PATH_PLANE)
         return CTP_E_OPTION;
-    int st = validate(geom, vol);
+    int st = validate_options(options);
+    if (st != CTP_OK) return st;
+    st = validate(geom, vol);
     if (st != CTP_OK) return st;
 
     ctp_plan_t *p = new (std::nothrow) ctp_plan_t();
     if (!p) return CTP_E_CUDA;
+    if (options) p->opt = *options;
     if (cudaGetDevice(&p->device) != cudaSuccess) {
         delete p;
         return CTP_E_CUDA;
@@ -446,38 +510,11 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
     // Per-view frames in cell coordinates, float64.
     p->frames.resize(geom->n_views > 0 ? geom->n_views : 1);
     bool v_is_z = geom->ndim == 3;
-    const double cu = 0.5 * (geom->n_u - 1) - geom->offset_u;
-    const double cv = 0.5 * (geom->n_v - 1) - geom->offset_v;
     const bool curved = geom->pixel_offsets != nullptr;
     for (int s = 0; s < geom->n_views; ++s) {
-        const float *S = geom->src + 3 * s, *C = geom->det_centre + 3 * s;
-        const float *U = geom->det_u + 3 * s, *V = geom->det_v + 3 * s;
-        ctp::ViewFrame &F = p->frames[s];
-        // unit normal of the detector, for curved detectors' depth offsets
-        const double Ud[3] = {U[0], U[1], U[2]}, Vd[3] = {V[0], V[1], V[2]};
-        double N[3];
-        cross3(Ud, Vd, N);
-        const double nn = norm3(N);
-        for (int a = 0; a < 3; ++a) {
-            const double d = p->spacing[a], o = p->origin[a];
-            F.a[a] = geom->beam == CTP_DIVERGENT ? ((double)S[a] - o) / d : (double)S[a] / d;
-            if (curved) {
-                // pixel = centre + t u + s v + e n (per-pixel offsets in physical units)
-                F.p00[a] = ((double)C[a] - o) / d;
-                F.du[a] = Ud[a] / d;
-                F.dv[a] = Vd[a] / d;
-                F.dn[a] = N[a] / nn / d;
-                continue;
-            }
-            const double pu = geom->pitch_u * (double)U[a];
-            const double pv = geom->pitch_v * (double)V[a];
-            // pixel (0, 0) = centre - cu * pitch_u * u - cv * pitch_v * v
-            const double p00 = (double)C[a] - cu * pu - cv * pv;
-            F.p00[a] = (p00 - o) / d;
-            F.du[a] = pu / d;
-            F.dv[a] = pv / d;
-            F.dn[a] = 0.0;
-        }
+        if (curved) curved_view_frame(geom, vol, s, &p->frames[s]);
+        else flat_view_frame(geom, vol, s, &p->frames[s]);
+        const float *V = geom->det_v + 3 * s;
         if (!(V[0] == 0.0f && V[1] == 0.0f && V[2] != 0.0f)) v_is_z = false;
     }
     // A curved detector runs on the column path when its columns are straight
@@ -552,7 +589,9 @@ int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan
     }
     if (chosen == CTP_PATH_COLUMN || chosen == CTP_PATH_PLANE) {
         if (chosen == CTP_PATH_COLUMN)
-            st = ctp::column_plan_build(ray_params(p), &p->col, &p->d_table, &p->d_work_fwd,
+            st = ctp::column_plan_build(ray_params(p), p->opt.rows_forward, p->opt.rows_backward,
+                                        p->opt.backward_rows_adjacent != 0, &p->col,
+                                        &p->d_table, &p->d_work_fwd,
                                         &p->d_work_bwd, &p->device_bytes);
         else
             st = ctp::plane_plan_build(ray_params(p), &p->d_table, &p->d_work_fwd,
@@ -677,15 +716,12 @@ static int ensure_stage(ctp_plan_t *plan)
 
 // Number of view chunks the host-buffer entry points pipeline: one per 64 MiB
 // of sinogram, at most 8 (each chunk's walk still fills the GPU many times
-// over), at most one per view.  CTP_HOST_CHUNKS = 1..64 overrides.
+// over), at most one per view.  The plan option host_chunks (1..64) overrides.
 static int host_chunks(const ctp_plan_t *plan)
 {
     long long c = (long long)(sizeof(float) * (unsigned long long)plan->n_rays >> 26);
     if (c > 8) c = 8;
-    if (const char *env = getenv("CTP_HOST_CHUNKS")) {
-        const long long e = atoll(env);
-        if (e >= 1 && e <= 64) c = e;
-    }
+    if (plan->opt.host_chunks >= 1) c = plan->opt.host_chunks;
     if (c > plan->n_views) c = plan->n_views;
     return c < 1 ? 1 : (int)c;
 }
@@ -876,7 +912,7 @@ int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *
     Q.pitch_u = (float)plan->pitch_u;
     Q.pitch_v = (float)plan->pitch_v;
     cudaStream_t s = (cudaStream_t)stream;
-    if (plan->path == CTP_PATH_COLUMN && !column_gvjp_disabled()) {
+    if (plan->path == CTP_PATH_COLUMN && plan->opt.geometry_walk == 0) {
         // the column walk reads the plan's padded z-fastest working copy
         if ((st = forward_in(plan, vol_dev, s)) != CTP_OK) return st;
         return ctp::column_geometry_vjp(ray_params(plan), Q, (const ctp::ColumnTrace *)plan->d_table,
@@ -920,42 +956,71 @@ constexpr int kStaticChunk = 32;        // frames staged per host-to-device copy
 // library until the process exits; keeps the last call's frames.
 static __device__ __align__(256) ctp::ViewFrame g_static_frames[kStaticMaxViews];
 
-std::atomic<void *> g_static_frames_addr[kStaticMaxDevices];
+// Driver calls that identify the current context, fetched through the runtime
+// (the library does not link the driver library itself).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
 
-// Device address of g_static_frames on the current device (looked up once per
-// device; host code may not use the symbol itself as a device pointer).
-int static_frames_address(int device, ctp::ViewFrame **out)
+struct StaticLookup {
+    std::mutex lock;
+    bool fetched = false;
+    CtxGetCurrentFn get_current = nullptr;
+    CtxGetIdFn get_id = nullptr;
+    unsigned long long ctx_id[kStaticMaxDevices] = {};  // 0: not looked up yet
+    void *addr[kStaticMaxDevices] = {};
+};
+
+StaticLookup &static_lookup()
 {
-    void *ptr = g_static_frames_addr[device].load(std::memory_order_acquire);
-    if (!ptr) {
-        if (cudaGetSymbolAddress(&ptr, g_static_frames) != cudaSuccess || !ptr)
-            return CTP_E_CUDA;
-        g_static_frames_addr[device].store(ptr, std::memory_order_release);
-    }
-    *out = static_cast<ctp::ViewFrame *>(ptr);
-    return CTP_OK;
+    static StaticLookup L;
+    return L;
 }
 
-// Per-view frame in cell coordinates, the same arithmetic as ctp_plan's.
-void static_frame(const ctp_geometry *g, const ctp_volume *v, int s, ctp::ViewFrame *F)
+// Unique id of the current context (0 when it cannot be told).
+unsigned long long current_context_id(StaticLookup &L)
 {
-    const double spacing[3] = {v->dx, v->dy, v->dz};
-    const double origin[3] = {v->ox, v->oy, v->oz};
-    const double cu = 0.5 * (g->n_u - 1) - g->offset_u;
-    const double cv = 0.5 * (g->n_v - 1) - g->offset_v;
-    const float *S = g->src + 3 * s, *C = g->det_centre + 3 * s;
-    const float *U = g->det_u + 3 * s, *V = g->det_v + 3 * s;
-    for (int a = 0; a < 3; ++a) {
-        const double d = spacing[a], o = origin[a];
-        const double pu = g->pitch_u * (double)U[a];
-        const double pv = g->pitch_v * (double)V[a];
-        const double p00 = (double)C[a] - cu * pu - cv * pv;
-        F->p00[a] = (p00 - o) / d;
-        F->du[a] = pu / d;
-        F->dv[a] = pv / d;
-        F->a[a] = g->beam == CTP_DIVERGENT ? ((double)S[a] - o) / d : (double)S[a] / d;
-        F->dn[a] = 0.0;
+    if (!L.fetched) {
+        L.fetched = true;
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            L.get_current = (CtxGetCurrentFn)fn;
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            L.get_id = (CtxGetIdFn)fn;
     }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!L.get_current || !L.get_id || L.get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        L.get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_static_frames on the current device (host code may not
+// use the symbol itself as a device pointer).  Looked up once per device and
+// context: a context that was reset and recreated gets a fresh lookup.  When
+// the context cannot be identified, every call looks the address up.
+int static_frames_address(int device, ctp::ViewFrame **out)
+{
+    StaticLookup &L = static_lookup();
+    std::lock_guard<std::mutex> guard(L.lock);
+    unsigned long long id = current_context_id(L);
+    if (id != 0 && L.ctx_id[device] == id) {
+        *out = static_cast<ctp::ViewFrame *>(L.addr[device]);
+        return CTP_OK;
+    }
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_frames) != cudaSuccess || !ptr) return CTP_E_CUDA;
+    if (id == 0) id = current_context_id(L);  // the lookup made the context current
+    L.ctx_id[device] = id;
+    L.addr[device] = ptr;
+    *out = static_cast<ctp::ViewFrame *>(ptr);
+    return CTP_OK;
 }
 
 }  // namespace
@@ -980,8 +1045,9 @@ extern "C" int ctp_forward_static(const ctp_geometry *geom, const ctp_volume *vo
     ctp::ViewFrame chunk[kStaticChunk];
     for (int s0 = 0; s0 < geom->n_views; s0 += kStaticChunk) {
         const int n = geom->n_views - s0 < kStaticChunk ? geom->n_views - s0 : kStaticChunk;
-        for (int q = 0; q < n; ++q) static_frame(geom, vol, s0 + q, &chunk[q]);
-        // pageable source: the call returns once `chunk` has been staged
+        for (int q = 0; q < n; ++q) flat_view_frame(geom, vol, s0 + q, &chunk[q]);
+        // pageable source: the copy may wait for the stream's earlier work, and it
+        // returns once `chunk` has been staged, so the buffer can be refilled
         if (cudaMemcpyAsync(frames + s0, chunk, sizeof(ctp::ViewFrame) * n,
                             cudaMemcpyHostToDevice, s) != cudaSuccess)
             return CTP_E_CUDA;

@@ -47,8 +47,9 @@ constexpr int kRowFrac = 40;  // fractional bits of the rows' fixed-point z line
 
 struct ColumnPlan {
     int n_columns;       // n_views * n_u
-    int rows_fwd;        // detector rows per thread of the forward (1, 2 or 4)
+    int rows_fwd;        // detector rows per thread of the forward (1 to 4)
     int rows_bwd;        // ... of the backward and the counter
+    bool bwd_interleave; // backward with 2 rows: rows interleaved across lanes
 };
 
 // Zero halo (cells) around x and y of the padded working copies: the walk's
@@ -630,12 +631,11 @@ __global__ void __launch_bounds__(256) zfast_to_xfast_kernel(const float *__rest
 // Rows per thread.  The shared xy walk is paid once per R rows, at the cost of
 // registers.  The forward gather runs 4 rows (4 blocks of 256 threads per SM,
 // 64 registers; 2 rows at 5 blocks on short detectors); the backward, bound by
-// its atomics' L1/L2 throughput, runs 2 rows at 4 blocks per SM.
-// CTP_COLUMN_ROWS_FWD / CTP_COLUMN_ROWS_BWD = 1, 2, 3 or 4 override the choice.
-inline int column_rows(const RayParams &P, const char *env_name, int preferred)
+// its atomics' L1/L2 throughput, runs 2 rows at 4 blocks per SM.  A plan
+// option (1 to 4; 0 = this choice) overrides it.
+inline int column_rows(const RayParams &P, int requested, int preferred)
 {
-    const char *env = getenv(env_name);
-    if (env && env[0] >= '1' && env[0] <= '4' && env[1] == '\0') return env[0] - '0';
+    if (requested >= 1 && requested <= 4) return requested;
     int r = preferred;
     while (r > 1 && P.n_v < 24 * r) r /= 2;
     return r;
@@ -644,14 +644,19 @@ inline int column_rows(const RayParams &P, const char *env_name, int preferred)
 // Builds the column table and the two padded working copies (forward: halo
 // zeroed once here and never written again; backward: zeroed per call).
 // Returns 0, 9 (CUDA error) or 11 (scan not eligible for the column path).
-inline int column_plan_build(const RayParams &P, ColumnPlan *plan, void **d_columns,
-                             float **d_zfwd, float **d_zbwd, unsigned long long *bytes)
+// rows_fwd / rows_bwd: requested rows per thread (0 = the measured default);
+// bwd_adjacent: the 2-row backward covers 32 adjacent rows per instruction
+// instead of interleaving a thread's rows across lanes.
+inline int column_plan_build(const RayParams &P, int rows_fwd, int rows_bwd, bool bwd_adjacent,
+                             ColumnPlan *plan, void **d_columns, float **d_zfwd, float **d_zbwd,
+                             unsigned long long *bytes)
 {
     if ((long long)P.n_views * P.n_u >= (1LL << 31)) return 11;
     if (column_padded_cells(P) >= (1ULL << 31)) return 11;
     plan->n_columns = P.n_views * P.n_u;
-    plan->rows_fwd = column_rows(P, "CTP_COLUMN_ROWS_FWD", 4);
-    plan->rows_bwd = column_rows(P, "CTP_COLUMN_ROWS_BWD", 2);
+    plan->rows_fwd = column_rows(P, rows_fwd, 4);
+    plan->rows_bwd = column_rows(P, rows_bwd, 2);
+    plan->bwd_interleave = !bwd_adjacent;
     const size_t cbytes = sizeof(ColumnTrace) * (size_t)(plan->n_columns > 0 ? plan->n_columns : 1);
     const size_t vbytes = sizeof(float) * column_padded_cells(P);
     int *d_flag = nullptr;
@@ -721,10 +726,8 @@ inline int column_walk_backward(const RayParams &P, const ColumnPlan &plan, cons
     if (P.view_count <= 0 || P.n_u <= 0 || P.n_v <= 0) return 0;
     const ColumnTrace *T = (const ColumnTrace *)d_columns;
     const int R = plan.rows_bwd;
-    // rows interleaved across lanes (measured 1-4 % faster on the cone scans);
-    // CTP_COLUMN_BWD_INTERLEAVE=0 restores 32 adjacent rows per instruction
-    const char *env = getenv("CTP_COLUMN_BWD_INTERLEAVE");
-    const bool il = !(env && env[0] == '0');
+    // rows interleaved across lanes (measured 1-4 % faster on the cone scans)
+    const bool il = plan.bwd_interleave;
     if (R == 4) column_backward_kernel<4><<<column_grid(P, 4), 256, 0, s>>>(P, T, sino, d_zbwd);
     else if (R == 3) column_backward_kernel<3><<<column_grid(P, 3), 256, 0, s>>>(P, T, sino, d_zbwd);
     else if (R == 2 && il)

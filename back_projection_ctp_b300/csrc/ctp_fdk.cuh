@@ -73,16 +73,10 @@ struct FdkParams {
     int tx;            // warp tile width in x (32, 16, 8 or 4)
 };
 
-// Warp tile width: CTP_FDK_TX = 32, 16, 8 or 4 overrides the default 8.
-inline int fdk_tile_x()
-{
-    const char *env = getenv("CTP_FDK_TX");
-    if (env) {
-        const int t = atoi(env);
-        if (t == 32 || t == 16 || t == 8 || t == 4) return t;
-    }
-    return 8;
-}
+// Warp tile width in x: 8 x 4 columns per warp (measured against 32 x 1,
+// 16 x 2 and 4 x 8 on the cone scans: the warp's stencils of one view then fall
+// on the fewest detector rows).
+constexpr int kFdkTileX = 8;
 
 // A 64-bit integer as float from its two 32-bit halves (relative error below
 // 2^-23): 32-bit conversions, where a 64-bit conversion would run on the slow
@@ -476,7 +470,7 @@ inline int fdk_build(int ndim, int beam, int n_views, int n_u, int n_v, const fl
     const double cu = 0.5 * (n_u - 1) - offset_u, cv = 0.5 * (n_v - 1) - offset_v;
     P.cu = (float)cu;
     P.cv = (float)cv;
-    P.tx = fdk_tile_x();
+    P.tx = kFdkTileX;
     const double iso[3] = {o[0] + 0.5 * n[0] * d[0], o[1] + 0.5 * n[1] * d[1],
                            o[2] + 0.5 * n[2] * d[2]};
     const double x0[3] = {o[0] + 0.5 * d[0], o[1] + 0.5 * d[1], o[2] + 0.5 * d[2]};
@@ -659,28 +653,15 @@ inline dim3 fdk_grid(const FdkParams &F, int K)
 constexpr int kFdkK = 16;  // z voxels per thread of the scatter
 
 // z voxels per thread of the gather: the per-(column, view) set-up is shared by
-// K voxels, at the cost of registers.  CTP_FDK_K = 8, 16, 32 or 64 overrides
-// the default 16.
-inline int fdk_gather_k()
-{
-    const char *env = getenv("CTP_FDK_K");
-    if (env) {
-        const int k = atoi(env);
-        if (k == 8 || k == 16 || k == 32 || k == 64) return k;
-    }
-    return 16;
-}
+// K voxels, at the cost of registers (16 measured faster than 8, 32 and 64).
+constexpr int kFdkGatherK = 16;
 
 inline int fdk_gather(const FdkParams &F, const float *q, float *vol, cudaStream_t s)
 {
     if (F.ndim == 2) {
         wbp_gather_kernel<1><<<fdk_grid(F, 1), 256, 0, s>>>(F, q, vol);
     } else {
-        const int K = fdk_gather_k();
-        if (K == 8) wbp_gather_kernel<8><<<fdk_grid(F, 8), 256, 0, s>>>(F, q, vol);
-        else if (K == 32) wbp_gather_kernel<32><<<fdk_grid(F, 32), 256, 0, s>>>(F, q, vol);
-        else if (K == 64) wbp_gather_kernel<64><<<fdk_grid(F, 64), 256, 0, s>>>(F, q, vol);
-        else wbp_gather_kernel<16><<<fdk_grid(F, 16), 256, 0, s>>>(F, q, vol);
+        wbp_gather_kernel<kFdkGatherK><<<fdk_grid(F, kFdkGatherK), 256, 0, s>>>(F, q, vol);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }

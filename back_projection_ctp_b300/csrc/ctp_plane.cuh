@@ -613,11 +613,12 @@ inline dim3 plane_tgrid(const PlaneLayout &G)
 // tiled backward, which walks all views in one launch (plane_backward_whole).
 // Larger ones use fire-and-forget global reductions into the privatised padded
 // copies, which measured faster than shared-memory float atomics (C2: 0.46 vs
-// 0.66 ms).  CTP_PLANE_BACKWARD = t / r forces either.
-inline bool plane_backward_tiled(const RayParams &P)
+// 0.66 ms).  mode: 0 = by size, 1 = tiled, 2 = privatised (a plan option).
+inline bool plane_backward_tiled(const RayParams &P, int mode)
 {
-    const char *mode = getenv("CTP_PLANE_BACKWARD");
-    return mode ? mode[0] == 't' : (long long)P.n_views * P.n_u <= 65536;
+    if (mode == 1) return true;
+    if (mode == 2) return false;
+    return (long long)P.n_views * P.n_u <= 65536;
 }
 
 inline int plane_layout_in(const RayParams &P, float *d_fwd, const float *img, cudaStream_t s)

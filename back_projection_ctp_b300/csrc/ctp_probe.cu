@@ -1,0 +1,115 @@
+// Bandwidth probes for the benchmark's L2 roofline (measurement only; not part
+// of the projector library).
+//
+// The projector's segment stream is served by L1 and L2, not DRAM: the
+// backward's float reductions travel from L1 to L2 in 32-byte sectors and the
+// forward's gathers hit in L1 / L2.  The roofline that bounds them is therefore
+// the rate at which L2 takes reductions (and serves loads), which these probes
+// measure on the machine they run on:
+//
+//   ctp_probe_l2_reduction  every warp instruction is a float reduction of 32
+//                           consecutive floats (4 full sectors) into a buffer
+//                           that stays in L2: the highest rate at which useful
+//                           reduction bytes reach L2 (8 floats per sector).
+//                           sparse = 1: each lane reduces one float into its own
+//                           sector instead (1 float per sector), the sector rate.
+//   ctp_probe_l2_load       coalesced 16-byte loads that bypass L1 (ld.global.cg)
+//                           from a buffer that stays in L2.
+//
+// Both walk the buffer with a per-warp stride so that concurrent warps touch
+// different lines; the caller times them with CUDA events on `stream`.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace {
+
+__global__ void __launch_bounds__(256) probe_red_kernel(float *__restrict__ buf, long long n,
+                                                        int iters, int sparse)
+{
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long span = sparse ? 256 : 32;  // floats one warp instruction covers
+    const long long lines = n / span;
+    long long line = warp % lines;
+    const float v = 1.0f + 1e-3f * lane;
+    for (int it = 0; it < iters; ++it) {
+        const long long base = line * span;
+        atomicAdd(buf + base + (sparse ? 8 * lane : lane), v);
+        line += nwarps;
+        if (line >= lines) line -= lines;
+    }
+}
+
+__global__ void __launch_bounds__(256) probe_load_kernel(const float4 *__restrict__ buf,
+                                                         long long n4, int iters,
+                                                         float *__restrict__ sink)
+{
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long lines = n4 / 32;
+    long long line = warp % lines;
+    float acc = 0.0f;
+    for (int it = 0; it < iters; ++it) {
+        const float4 q = __ldcg(buf + line * 32 + lane);
+        acc += q.x + q.y + q.z + q.w;
+        line += nwarps;
+        if (line >= lines) line -= lines;
+    }
+    if (acc == 1.2345e-30f) sink[0] = acc;  // keeps the loads; never true for the probe's data
+}
+
+int blocks_for(int sms) { return sms * 8; }
+
+}  // namespace
+
+extern "C" {
+
+// Adds to buf[0, n): grid of 8 blocks of 256 threads per SM, `iters` reductions
+// per thread; n / (32 floats, or 256 when sparse) must be at least the grid's
+// warps.  Returns 0, 1 (bad arguments) or 9 (launch failed).  Useful bytes per launch:
+// 4 * (threads) * iters.
+int ctp_probe_l2_reduction(float *buf, long long n, int iters, int sparse, void *stream)
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 9;
+    // every warp must own a distinct line: the walk wraps with one subtraction
+    const long long span = sparse ? 256 : 32, warps = (long long)blocks_for(sms) * 256 / 32;
+    if (!buf || n < 256 || iters < 1 || n / span < warps) return 1;
+    probe_red_kernel<<<blocks_for(sms), 256, 0, (cudaStream_t)stream>>>(buf, n, iters,
+                                                                        sparse ? 1 : 0);
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+// Reads buf[0, n) (n a multiple of 128 floats, buf 16-byte aligned): 16 bytes per
+// thread per iteration.  sink: one device float (written only in a case that
+// does not occur).  Returns 0, 1 (bad arguments) or 9.
+int ctp_probe_l2_load(const float *buf, long long n, int iters, float *sink, void *stream)
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 9;
+    const long long warps = (long long)blocks_for(sms) * 256 / 32;
+    if (!buf || !sink || n < 128 || n % 128 != 0 || ((uintptr_t)buf & 15) || iters < 1 ||
+        n / 128 < warps)
+        return 1;
+    probe_load_kernel<<<blocks_for(sms), 256, 0, (cudaStream_t)stream>>>(
+        reinterpret_cast<const float4 *>(buf), n / 4, iters, sink);
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+// SM count of the current device (the probes' grid is 8 blocks of 256 threads per SM).
+int ctp_probe_sm_count(int *out)
+{
+    int dev = 0;
+    if (!out || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 9;
+    return 0;
+}
+
+}  // extern "C"

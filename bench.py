@@ -38,6 +38,9 @@ UNIT = "Gseg/s"
 DEFAULT_CONFIG = 4
 FALLBACK_HBM_GBS = 6400.0
 CSRC = os.path.join(ROOT, "back_projection_ctp_b300", "csrc")
+# ncu figures of profiled kernels (DRAM bytes per launch, limiting units), each
+# with the hash of the kernel sources it was captured on
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 
 # ----------------------------------------------------------------- helpers
@@ -79,10 +82,65 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "of fallback"
 
 
+# ------------------------------------------------------------ L2 bandwidth probes
+def l2_peaks(dev, stream, repeats=5):
+    """Measured L2 rates of this GPU (``libctp_probe.so``), best of ``repeats``:
+    useful bytes/s of float reductions at full sector density (32 consecutive
+    floats per warp instruction), 32-byte sectors/s of reductions at one float
+    per sector, and bytes/s of coalesced loads that bypass L1; the buffers
+    (64 MiB) stay in L2."""
+    import ctypes
+    import torch
+    from back_projection_ctp_b300 import build as ctp_build
+    lib = ctypes.CDLL(ctp_build.build_probe())
+    lib.ctp_probe_l2_reduction.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_void_p]
+    lib.ctp_probe_l2_load.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_void_p]
+    lib.ctp_probe_sm_count.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    sms = ctypes.c_int(0)
+    if lib.ctp_probe_sm_count(ctypes.byref(sms)) != 0:
+        raise RuntimeError("ctp_probe_sm_count failed")
+    threads = sms.value * 8 * 256
+    n = 16 << 20
+    buf = torch.zeros(n, dtype=torch.float32, device=dev)
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
+    sp = stream.cuda_stream
+
+    def best(launch, units):
+        launch()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(repeats):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b) * 1e-3)
+        return units / min(times)
+
+    def check(st):
+        if st != 0:
+            raise RuntimeError(f"L2 probe failed ({st})")
+
+    it_red, it_load = 16000, 4000
+    red = best(lambda: check(lib.ctp_probe_l2_reduction(buf.data_ptr(), n, it_red, 0, sp)),
+               4.0 * threads * it_red)
+    sectors = best(lambda: check(lib.ctp_probe_l2_reduction(buf.data_ptr(), n, it_load, 1, sp)),
+                   1.0 * threads * it_load)
+    load = best(lambda: check(lib.ctp_probe_l2_load(buf.data_ptr(), n, it_load, sink.data_ptr(),
+                                                    sp)), 16.0 * threads * it_load)
+    return {"reduction_gbs": red / 1e9, "reduction_sectors_per_s": sectors,
+            "load_gbs": load / 1e9,
+            "how": "libctp_probe.so: 8 blocks x 256 threads per SM over a 64 MiB buffer held "
+                   "in L2; best of 5 launches timed with CUDA events"}
+
+
 def stored_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    path = TRAFFIC_JSON
     try:
         with open(path) as fh:
             rec = json.load(fh)
@@ -248,6 +306,104 @@ def run_reference(args, w, world, rank):
 
 
 # ------------------------------------------------------------------ GPU arm
+def time_pair(ctp, plan, d_vol, d_y, d_sino, d_g, steps, warmup, dev, stream):
+    """Device times (ms) of one forward call, one backward call and one step
+    (forward + backward) on the caller's stream: each from one CUDA graph of
+    ``steps`` calls replayed between CUDA events.  Returns (step, fwd, bwd) and
+    the step graph's timing function for the caller's timed region."""
+    import torch
+
+    for _ in range(warmup):
+        ctp.ctp_forward(plan, d_vol, d_sino, stream)
+        ctp.ctp_backward(plan, d_y, d_g, stream)
+    torch.cuda.synchronize(dev)
+
+    # The calls only enqueue kernels and a memset, so they capture as they are.
+    def capture(body):
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side), torch.cuda.graph(graph, stream=side):
+            cur = torch.cuda.current_stream(dev)
+            for _ in range(steps):
+                body(cur)
+        torch.cuda.synchronize(dev)
+        return graph
+
+    g_steps = capture(lambda st: (ctp.ctp_forward(plan, d_vol, d_sino, st),
+                                  ctp.ctp_backward(plan, d_y, d_g, st)))
+    g_fwd = capture(lambda st: ctp.ctp_forward(plan, d_vol, d_sino, st))
+    g_bwd = capture(lambda st: ctp.ctp_backward(plan, d_y, d_g, st))
+    g_steps.replay()  # one untimed replay of the captured steps
+    torch.cuda.synchronize(dev)
+
+    def timed(graph):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b)
+
+    return timed, g_steps, timed(g_fwd) / steps, timed(g_bwd) / steps
+
+
+def kernel_of(path, call):
+    return {"column": {"forward": "column_forward_kernel", "backward": "column_backward_kernel"},
+            "plane": {"forward": "plane_forward_kernel", "backward": "plane_backward_kernel"},
+            "ray": {"forward": "ray_forward_kernel", "backward": "ray_backward_kernel"}}[path][call]
+
+
+# ncu figures of the committed summaries (profiles/): the unit that limits each
+# dominant kernel, by kernel and workload
+def stored_ncu(kernel: str, workload: str):
+    path = TRAFFIC_JSON
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(kernel, {}).get(workload)
+    if not entry or entry.get("source_hash") != source_hash(kernel):
+        return None
+    return entry.get("ncu")
+
+
+def per_workload(args, ctp, dev, stream, peaks, skip):
+    """Forward and backward device times of every workload but ``skip`` (the
+    headline one), with the same graphs and the same units; each workload's
+    phantom and N(0,1) sinogram as in the parity tests."""
+    import torch
+    out = {}
+    hbm, _ = hbm_peak()
+    for idx in sorted(ci.WORKLOADS):
+        if idx == skip:
+            continue
+        w = ci.get(idx)
+        plan = ctp.ctp_plan(geometry_of(w, ci.frames(w)), volume_of(w), args.path)
+        d_vol = torch.from_numpy(ci.phantom(w)).to(dev)
+        d_y = torch.from_numpy(ci.sinogram_noise(w)).to(dev)
+        d_sino = torch.empty(plan.sino_shape, dtype=torch.float32, device=dev)
+        d_g = torch.empty(plan.vol_shape, dtype=torch.float32, device=dev)
+        timed, g_steps, fwd_ms, bwd_ms = time_pair(ctp, plan, d_vol, d_y, d_sino, d_g,
+                                                   args.steps, args.warmup, dev, stream)
+        step_ms = timed(g_steps) / args.steps
+        seg = golden_segments(idx)
+        out[w.name] = {
+            "path": plan.path, "segments_per_pass": seg, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "ms_per_step": step_ms, "gseg_per_s": 2.0 * seg / (step_ms * 1e-3) / 1e9,
+            "fwd_frac_l2_load": 4.0 * seg / (fwd_ms * 1e-3) / 1e9 / peaks["load_gbs"],
+            "bwd_frac_l2_reduction": 4.0 * seg / (bwd_ms * 1e-3) / 1e9 / peaks["reduction_gbs"],
+            "fwd_frac_hbm_equivalent": 4.0 * seg / (fwd_ms * 1e-3) / 1e9 / hbm,
+            "bwd_frac_hbm_equivalent": 4.0 * seg / (bwd_ms * 1e-3) / 1e9 / hbm,
+        }
+        del g_steps
+        plan.destroy()
+        del d_vol, d_y, d_sino, d_g
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args, w, world, rank, local):
     """Time K steps of forward + backward on this rank's GPU."""
     import torch
@@ -272,43 +428,8 @@ def run_gpu(args, w, world, rank, local):
     d_sino = torch.empty(plan.sino_shape, dtype=torch.float32, device=dev)
     d_g = torch.empty(plan.vol_shape, dtype=torch.float32, device=dev)
 
-    def step():
-        ctp.ctp_forward(plan, d_vol, d_sino, stream)
-        ctp.ctp_backward(plan, d_y, d_g, stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-
-    # The timed region replays one CUDA graph holding K steps (the calls only
-    # enqueue kernels and a memset, so they capture as they are); per-call times
-    # for the roofline come from graphs of K forward and K backward calls.
-    def capture(body):
-        graph = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(side), torch.cuda.graph(graph, stream=side):
-            cur = torch.cuda.current_stream(dev)
-            for _ in range(args.steps):
-                body(cur)
-        torch.cuda.synchronize(dev)
-        return graph
-
-    g_steps = capture(lambda st: (ctp.ctp_forward(plan, d_vol, d_sino, st),
-                                  ctp.ctp_backward(plan, d_y, d_g, st)))
-    g_fwd = capture(lambda st: ctp.ctp_forward(plan, d_vol, d_sino, st))
-    g_bwd = capture(lambda st: ctp.ctp_backward(plan, d_y, d_g, st))
-    g_steps.replay()  # one untimed replay of the captured steps
-    torch.cuda.synchronize(dev)
-
-    def timed(graph):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        graph.replay()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        return a.elapsed_time(b)
-
+    timed, g_steps, fwd_ms, bwd_ms = time_pair(ctp, plan, d_vol, d_y, d_sino, d_g, args.steps,
+                                               args.warmup, dev, stream)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -319,8 +440,6 @@ def run_gpu(args, w, world, rank, local):
     barrier(world)
     clocks = sampler.stop()
     total_ms = max_over_ranks(total_ms, world)
-    fwd_ms = timed(g_fwd) / args.steps
-    bwd_ms = timed(g_bwd) / args.steps
     ms_per_step = total_ms / args.steps
     value = world * 2.0 * segments / (ms_per_step * 1e-3) / 1e9
 
@@ -344,17 +463,30 @@ def run_gpu(args, w, world, rank, local):
     e2e_value = world * 2.0 * segments / e2e_s / 1e9
     bytes_io = 4 * (w.n_voxels + w.n_rays)
 
-    # roofline of the dominant call (4 algorithmic bytes per segment: one voxel
-    # read per forward segment, one float atomic per backward segment)
+    # Roofline of the dominant call.  Its segment stream (4 algorithmic bytes
+    # per segment: one voxel read per forward piece, one float reduction per
+    # backward piece) is served by L1 / L2, so the bound is L2: the backward
+    # against the measured rate at which L2 takes float reductions at full
+    # sector density, the forward against L2's load rate.  The same bytes over
+    # the measured HBM copy bandwidth (an HBM-equivalent fraction) and the ncu
+    # DRAM traffic over it (the measured DRAM fraction) are reported beside it.
+    del g_steps
+    peaks = l2_peaks(dev, stream)
     dominant = "backward" if bwd_ms >= fwd_ms else "forward"
     dom_ms = max(bwd_ms, fwd_ms)
     achieved = 4.0 * segments / (dom_ms * 1e-3) / 1e9
-    peak, peak_src = hbm_peak()
-    kernel_name = {"column": {"forward": "column_forward_kernel", "backward": "column_backward_kernel"},
-                   "plane": {"forward": "plane_forward_kernel", "backward": "plane_backward_kernel"},
-                   "ray": {"forward": "ray_forward_kernel", "backward": "ray_backward_kernel"}}[plan.path][dominant]
+    l2_peak = peaks["reduction_gbs"] if dominant == "backward" else peaks["load_gbs"]
+    hbm, hbm_src = hbm_peak()
+    kernel_name = kernel_of(plan.path, dominant)
+    traffic = stored_traffic(kernel_name, w.name)
     # kernels of this library per step: column / plane = layout pass + walk, twice
     launches_per_step = 2 if plan.path == "ray" else 4
+    plan_path = plan.path
+    plan.destroy()
+    del d_vol, d_y, d_sino, d_g
+    torch.cuda.empty_cache()
+    others = per_workload(args, ctp, dev, stream, peaks, args.config) \
+        if (world == 1 and args.views is None and not args.no_per_workload) else None
 
     if rank == 0:
         cpu = None
@@ -369,14 +501,27 @@ def run_gpu(args, w, world, rank, local):
                        "spacing_DHW": list(w.spacing), "views": w.n_views,
                        "detector_vu": [w.n_v, w.n_u], "segments_per_pass": segments,
                        "segments_from": seg_source,
-                       "path": plan.path, "parallelism": f"replicas{world}",
+                       "path": plan_path, "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (no flush)" if 4 * w.n_voxels > 126e6
                        else "inputs smaller than L2 (no flush)",
-                       "fwd_ms": fwd_ms, "bwd_ms": bwd_ms},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": stored_traffic(kernel_name, w.name),
-                         "kernel": kernel_name, "call": dominant,
-                         "note": f"4 B per segment over the {dominant} call's event time; peak {peak_src}"},
+                       "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                       "per_workload": others},
+            "roofline": {
+                "bound": "l2", "achieved": achieved, "peak": l2_peak, "unit": "GB/s",
+                "frac": achieved / l2_peak, "traffic": traffic, "kernel": kernel_name,
+                "call": dominant,
+                "peak_source": ("measured in this run: L2 float reductions at full sector "
+                                "density" if dominant == "backward" else
+                                "measured in this run: L2 loads bypassing L1"),
+                "l2_probe": peaks,
+                "hbm_equivalent": {"peak": hbm, "frac": achieved / hbm,
+                                   "note": f"the same 4 B per segment over the HBM copy "
+                                           f"bandwidth ({hbm_src}); not a DRAM measurement"},
+                "dram_frac": (traffic / (dom_ms * 1e-3) / 1e9 / hbm) if traffic else None,
+                "ncu": stored_ncu(kernel_name, w.name),
+                "note": f"4 algorithmic bytes per segment over the {dominant} call's event "
+                        "time; dram_frac = the ncu DRAM bytes of one launch over the same "
+                        "time and the HBM copy bandwidth"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bytes_io,
                     "d2h_bytes_per_step": bytes_io, "ms_per_step": e2e_s * 1e3},
@@ -385,7 +530,6 @@ def run_gpu(args, w, world, rank, local):
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
-    plan.destroy()
     return 0
 
 
@@ -650,6 +794,8 @@ def main(argv=None):
     ap.add_argument("--path", default="auto", choices=["auto", "ray", "column"])
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the forward / backward timings of the other four workloads")
     ap.add_argument("--op", default="siddon", choices=["siddon", "fdk", "geometry"],
                     help="siddon: the projector pair (default); fdk: the analytical "
                          "filtered backprojection on the same workload; geometry: the "

@@ -59,7 +59,7 @@ typedef enum ctp_status {
     CTP_E_AXES = 8,        /* detector axes zero or parallel; parallel ray direction zero */
     CTP_E_CUDA = 9,        /* a CUDA runtime call failed */
     CTP_E_DEVICE = 10,     /* called with a different current device than the plan's */
-    CTP_E_OPTION = 11,     /* unknown beam / ndim / path value */
+    CTP_E_OPTION = 11,     /* unknown beam / ndim / path value or plan option */
     CTP_E_LIMIT = 12,      /* request beyond a fixed size limit of this entry point */
     CTP_E_GEOMETRY = 13    /* scan outside the analytical operators' class (see ctp_fdk) */
 } ctp_status;
@@ -119,6 +119,36 @@ typedef struct ctp_volume {
 
 typedef struct ctp_plan ctp_plan_t;
 
+/*
+ * Work-layout options of a plan.  None changes what the operators compute;
+ * they select among work layouts that compute the same operator (used to test
+ * each layout and to measure them against each other).  Zero in every field
+ * (or a NULL pointer to ctp_plan_ex) is the measured default.
+ *   rows_forward, rows_backward  column path: detector rows per thread of the
+ *                 forward walk / of the backward walk and the segment counter,
+ *                 1 to 4 (0: 4 and 2, halved on detectors under 96 / 48 rows).
+ *   backward_rows_adjacent  column path with 2 rows per backward thread: 1 =
+ *                 each reduction instruction covers 32 adjacent rows; 0 = a
+ *                 thread's two rows are interleaved across lanes (default).
+ *   plane_backward  plane path: 0 = by scan size (one shared-memory tiled launch
+ *                 up to 65536 rays, else privatised global reductions); 1 =
+ *                 always tiled; 2 = always privatised.
+ *   host_chunks   host-buffer calls: number of view chunks the walk and the
+ *                 sinogram copies are pipelined in, 1 to 64 (0: one per 64 MiB
+ *                 of sinogram, at most 8); never more than the views.
+ *   geometry_walk ctp_geometry_vjp on column-path plans: 0 = the column walk,
+ *                 1 = the ray walk (other plans always take the ray walk).
+ * Values outside these ranges make ctp_plan_ex return CTP_E_OPTION.
+ */
+typedef struct ctp_plan_options {
+    int rows_forward;
+    int rows_backward;
+    int backward_rows_adjacent;
+    int plane_backward;
+    int host_chunks;
+    int geometry_walk;
+} ctp_plan_options;
+
 typedef struct ctp_plan_info {
     int path;                         /* ctp_path actually used */
     int device;                       /* CUDA device the plan lives on */
@@ -139,6 +169,12 @@ typedef struct ctp_plan_info {
  * Synchronous: allocates and fills the plan's device tables.
  */
 int ctp_plan(const ctp_geometry *geom, const ctp_volume *vol, int path, ctp_plan_t **out);
+
+/* ctp_plan with work-layout options (host struct, read during the call; NULL =
+ * all defaults, the same plan as ctp_plan).  Errors as ctp_plan, plus
+ * CTP_E_OPTION for an option out of range. */
+int ctp_plan_ex(const ctp_geometry *geom, const ctp_volume *vol, int path,
+                const ctp_plan_options *options, ctp_plan_t **out);
 
 /* Release a plan (NULL is ignored).  Synchronises the device before freeing. */
 void ctp_destroy(ctp_plan_t *plan);
@@ -182,8 +218,8 @@ int ctp_segment_count(const ctp_plan_t *plan, unsigned long long *out, void *str
  * Results equal the device calls' (the forward bit for bit, the backward up to
  * its atomics' summation order).  Host buffers may be pageable or pinned; with
  * pinned buffers the sinogram transfer overlaps the walk: the walk runs in view
- * chunks on `stream` (one chunk per 64 MiB of sinogram, at most 8; the
- * environment variable CTP_HOST_CHUNKS = 1..64 overrides) and each chunk's
+ * chunks on `stream` (one chunk per 64 MiB of sinogram, at most 8; the plan
+ * option host_chunks overrides) and each chunk's
  * sinogram rows move on a second stream owned by the plan -- down as soon as the
  * chunk is walked (forward), up just before it is walked (backward).  The
  * volume moves on `stream`.  The plan allocates one device volume, one device
@@ -201,19 +237,25 @@ int ctp_backward_host(ctp_plan_t *plan, const float *sino_host, float *vol_host,
  * owned by their own pool allocator (a raw cudaMalloc would bypass the pool's
  * budget and can fail once the pool has reserved the rest), and loops that must
  * not take the implicit device synchronisation of cudaMalloc / cudaFree.  The
- * reference has no counterpart; the result equals ctp_forward of a RAY-path plan
- * of the same scan.
+ * pages have no counterpart; the result equals ctp_forward of a RAY-path plan
+ * of the same scan (the per-view frames come from the same host function).
  * geom, vol: host structs as for ctp_plan (validated the same way, same error
  * codes).  vol_dev / sino_dev: device float32 buffers as for ctp_forward (may be
- * NULL when n_views is 0).  stream: a cudaStream_t (NULL = default stream).
+ * NULL when n_views is 0), on the current device.  stream: a cudaStream_t
+ * (NULL = default stream).
  * Scratch: the per-view frame table lives in a fixed device array of
  * 4096 views (480 KiB) that every device loading the library holds until exit;
  * n_views above 4096 returns CTP_E_LIMIT, and so does a current device ordinal
- * of 64 or more.  The first call on a device looks the array up
+ * of 64 or more.  The first call on a device (and the first after its context
+ * was reset and recreated) looks the array's device address up
  * (cudaGetSymbolAddress); make that first call before any stream capture.
- * Every call rewrites the frames it uses from the host and reads nothing left
- * by earlier calls; calls that overlap on the GPU (other streams, other host
- * threads) share the array and race.  Calls no cudaMalloc / cudaFree.
+ * The frames are converted on the host into a buffer on the call's stack and
+ * copied with cudaMemcpyAsync from that pageable memory: the copy may make the
+ * host wait for the stream's earlier work, and the call returns only once the
+ * frames have left the buffer.  Every call rewrites the frames it uses and
+ * reads nothing left by earlier calls; calls that overlap on the GPU (other
+ * streams, other host threads) share the array and race.  Calls no
+ * cudaMalloc / cudaFree.
  */
 int ctp_forward_static(const ctp_geometry *geom, const ctp_volume *vol, const float *vol_dev,
                        float *sino_dev, void *stream);
@@ -325,8 +367,8 @@ int ctp_parker_weights(const ctp_plan_t *plan, float *weight_dev, void *stream);
  * (n_views, n_v, n_u).  grad_dev: device float64 (n_views, 12), overwritten.
  * Column-path plans run the sums over the column walk on the plan's working
  * copy of vol_dev (ordered with the plan's other calls, as ctp_forward); other
- * plans run the ray path's walk (the environment variable CTP_GEOMETRY_RAY=1
- * forces it for column plans too).  Asynchronous on `stream`.  Errors:
+ * plans run the ray path's walk (the plan option geometry_walk = 1 selects it
+ * for column plans too).  Asynchronous on `stream`.  Errors:
  * CTP_E_NULL, CTP_E_DEVICE, CTP_E_OPTION (curved detectors: the chain rule
  * above assumes the pitch grid), CTP_E_CUDA.
  */

@@ -25,6 +25,15 @@ def rel_l2(got, want):
     return float(np.linalg.norm(got - want) / den) if den > 0 else float(np.linalg.norm(got))
 
 
+def max_rel_err(got, want):
+    """max |got - want| / max |want| (element by element, float64)."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    scale = float(np.max(np.abs(want))) if want.size else 0.0
+    err = float(np.max(np.abs(got - want))) if want.size else 0.0
+    return err / scale if scale > 0 else err
+
+
 def adjoint_mismatch(Ax, y, x, Aty):
     """|<Ax, y> - <x, A^T y>| / (||Ax|| ||y||) and the raw relative value."""
     lhs = float(np.dot(np.asarray(Ax, np.float64).ravel(), np.asarray(y, np.float64).ravel()))
@@ -38,6 +47,12 @@ def adjoint_mismatch(Ax, y, x, Aty):
 TOL_FORWARD = 1e-5
 TOL_BACKWARD = 1e-4
 TOL_ADJOINT = 1e-5
+# Element by element (the per-pixel / per-voxel reading of the same bars):
+# |gpu - oracle| <= tol * max|oracle| over the compared sample.  Float32
+# accumulation of a path sum of ~1e3 pieces errs by ~1e-7 of the largest
+# values; the backward's atomics add order-dependent rounding of the same size.
+TOL_FORWARD_MAX = 1e-5
+TOL_BACKWARD_MAX = 1e-4
 
-__all__ = ["ci", "geometry_of", "volume_of", "rel_l2", "adjoint_mismatch", "TOL_FORWARD",
-           "TOL_BACKWARD", "TOL_ADJOINT"]
+__all__ = ["ci", "geometry_of", "volume_of", "rel_l2", "max_rel_err", "adjoint_mismatch", "TOL_FORWARD",
+           "TOL_BACKWARD", "TOL_ADJOINT", "TOL_FORWARD_MAX", "TOL_BACKWARD_MAX"]

@@ -112,6 +112,32 @@ def test_shape_and_option_errors():
         _plan_status(path="sideways")
 
 
+@pytest.mark.parametrize("options", [
+    {"rows_forward": 5}, {"rows_backward": -1}, {"backward_rows_adjacent": 2},
+    {"plane_backward": 3}, {"host_chunks": 65}, {"geometry_walk": 2},
+])
+def test_plan_options_out_of_range_are_rejected_on_the_host(options):
+    """ctp_plan_ex checks its work-layout options before any CUDA call."""
+    f = _cone()
+    g = ctp.Geometry(ndim=3, beam="divergent", n_u=8, n_v=8, pitch_u=1.0, pitch_v=1.0, **f)
+    with pytest.raises(ctp.CtpError) as e:
+        ctp.ctp_plan(g, ctp.Volume((8, 8, 8), (1.0, 1.0, 1.0), (-4.0, -4.0, -4.0)),
+                     options=options)
+    assert e.value.status == 11
+    with pytest.raises(ValueError):
+        ctp.ctp_plan(g, ctp.Volume((8, 8, 8), (1.0, 1.0, 1.0), (-4.0, -4.0, -4.0)),
+                     options={"colour": 1})
+
+
+def test_library_reads_no_environment():
+    """Work layouts are plan options, not process-wide variables: the library's
+    sources call no getenv."""
+    csrc = os.path.join(ROOT, "back_projection_ctp_b300", "csrc")
+    for name in os.listdir(csrc):
+        with open(os.path.join(csrc, name)) as fh:
+            assert "getenv" not in fh.read(), name
+
+
 def test_curved_detector_offsets_are_validated_on_the_host():
     f = _cone()
     off = np.zeros((8, 8, 3), np.float32)

@@ -83,8 +83,6 @@ def test_stored_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     kernel's own sources (comments and blank space aside) match the capture."""
     sys.path.insert(0, ROOT)
     import bench
-    for kernel in ("column_forward_kernel", "column_backward_kernel"):
-        assert bench.stored_traffic(kernel, "c4_cone_512_aniso") > 0
     csrc = tmp_path / "csrc"
     csrc.mkdir()
     for name in os.listdir(bench.CSRC):
@@ -92,14 +90,33 @@ def test_stored_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "CSRC", str(csrc))
     kernel = "column_forward_kernel"
     h = bench.source_hash(kernel)
+    record = tmp_path / "traffic.json"
+    record.write_text(json.dumps({kernel: {"c4_cone_512_aniso": {
+        "dram_bytes_per_launch": 123.0, "source_hash": h, "ncu": {"l1tex_pct": 50.0}}}}))
+    monkeypatch.setattr(bench, "TRAFFIC_JSON", str(record))
+    assert bench.stored_traffic(kernel, "c4_cone_512_aniso") == 123.0
+    assert bench.stored_ncu(kernel, "c4_cone_512_aniso") == {"l1tex_pct": 50.0}
     f = csrc / "ctp_column.cuh"
     text = f.read_text()
     f.write_text(text.replace("namespace ctp {", "namespace ctp {\n// a new comment\n\n", 1))
     assert bench.source_hash(kernel) == h  # comments and blank lines do not count
-    assert bench.stored_traffic(kernel, "c4_cone_512_aniso") > 0
+    assert bench.stored_traffic(kernel, "c4_cone_512_aniso") == 123.0
     f.write_text(text.replace("constexpr int kHalo = 2;", "constexpr int kHalo = 3;", 1))
     assert bench.source_hash(kernel) != h
     assert bench.stored_traffic(kernel, "c4_cone_512_aniso") is None
+    assert bench.stored_ncu(kernel, "c4_cone_512_aniso") is None
     (csrc / "ctp_fdk.cuh").write_text("// unrelated file changed\nint x;\n")
     f.write_text(text)
-    assert bench.stored_traffic(kernel, "c4_cone_512_aniso") > 0
+    assert bench.stored_traffic(kernel, "c4_cone_512_aniso") == 123.0
+
+
+def test_stored_traffic_record_is_well_formed():
+    """Every committed ncu record names its capture and the hash it belongs to."""
+    sys.path.insert(0, ROOT)
+    import bench
+    with open(bench.TRAFFIC_JSON) as fh:
+        rec = json.load(fh)
+    for kernel, by_workload in rec.items():
+        for workload, entry in by_workload.items():
+            assert entry["dram_bytes_per_launch"] > 0, (kernel, workload)
+            assert len(entry["source_hash"]) == 16 and entry["captured_on"], (kernel, workload)

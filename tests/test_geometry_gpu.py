@@ -42,15 +42,13 @@ def _weights(oracle_mod, scan, seed):
 
 @pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("walk", ["auto", "ray"])
-def test_small_cases_match_oracle(torch, ctp, oracle_mod, monkeypatch, idx, walk):
+def test_small_cases_match_oracle(torch, ctp, oracle_mod, idx, walk):
     """AUTO runs the column walk on the 3-D circular / helical scans and the ray
-    walk elsewhere; CTP_GEOMETRY_RAY=1 forces the ray walk."""
-    if walk == "ray":
-        monkeypatch.setenv("CTP_GEOMETRY_RAY", "1")
+    walk elsewhere; the plan option geometry_walk = "ray" forces the ray walk."""
     w = SMALL[idx]
     f = ci.frames(w)
     scan = oracle_mod.Scan.from_workload(w, f)
-    plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w))
+    plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w), options={"geometry_walk": walk})
     vol = ci.phantom(w)
     wt = _weights(oracle_mod, scan, 50 + idx)
     g = ctp.ctp_geometry_vjp(plan, torch.from_numpy(vol).cuda(),

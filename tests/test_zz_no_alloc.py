@@ -16,7 +16,7 @@ from cases import TOL_FORWARD, ci, geometry_of, rel_l2, volume_of
 pytestmark = pytest.mark.gpu
 
 
-def test_forward_static_matches_planned_forward_on_consecutive_calls():
+def test_forward_static_matches_planned_forward_and_oracle_on_consecutive_calls(oracle_mod):
     import torch
     import back_projection_ctp_b300 as ctp
 
@@ -28,15 +28,24 @@ def test_forward_static_matches_planned_forward_on_consecutive_calls():
         w = ci.small_cases()[idx]
         f = ci.frames(w)
         geom, volg = geometry_of(w, f), volume_of(w)
-        vol = torch.from_numpy(ci.phantom(w)).cuda()
+        vol_h = ci.phantom(w)
+        vol = torch.from_numpy(vol_h).cuda()
         plan = ctp.ctp_plan(geom, volg, "ray")
         ref = torch.empty(plan.sino_shape, dtype=torch.float32, device="cuda")
         ctp.ctp_forward(plan, vol, ref)
         out = torch.full(plan.sino_shape, float("nan"), dtype=torch.float32, device="cuda")
         ctp.ctp_forward_static(geom, volg, vol, out)
         torch.cuda.synchronize()
-        err = rel_l2(out.cpu().numpy(), ref.cpu().numpy())
+        got = out.cpu().numpy()
+        err = rel_l2(got, ref.cpu().numpy())
         assert err <= TOL_FORWARD, (w.name, err)
+        # and directly against the float64 oracle (rays in a cell-face plane,
+        # where the + side rule decides, left out as in the parity tests)
+        scan = oracle_mod.Scan.from_workload(w, f)
+        amb = oracle_mod.ambiguous(scan)
+        p_ref = oracle_mod.forward(scan, vol_h)
+        err_ref = rel_l2(got[~amb], p_ref[~amb])
+        assert err_ref <= TOL_FORWARD, (w.name, err_ref)
         results.append(err)
         plan.destroy()
     assert len(results) == 2
