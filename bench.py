@@ -12,6 +12,9 @@ the plan's own counter agrees to 1e-6, tested).
 
 With --gpus N > 1 (under torchrun) every rank runs an independent replica of the
 workload; the line reports the units of all ranks over the slowest rank's time.
+With --partition views the ranks share one workload instead: each projects its
+contiguous shard of views, and the backward's partial volumes are summed with
+one all-reduce (strong scaling).
 """
 
 from __future__ import annotations
@@ -533,6 +536,115 @@ def run_gpu(args, w, world, rank, local):
     return 0
 
 
+# ------------------------------------------------- view-partitioned (strong scaling)
+def run_partitioned(args, w, world, rank, local):
+    """One workload sharded by views over the ranks (one GPU each): each rank
+    projects its views and backprojects them into a full-volume partial, and
+    one all-reduce (sum) of the volume per backward gives A^T y on every rank.
+    Total work is fixed as ranks are added ("strong" scaling)."""
+    import torch
+    import back_projection_ctp_b300 as ctp
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    frames = ci.frames(w)
+    proj = ctp.ViewShardedProjector(geometry_of(w, frames), volume_of(w), args.path)
+    segments = golden_segments(args.config) if args.views is None else None
+    vol_h = ci.phantom(w)
+    y_h = np.ascontiguousarray(ci.sinogram_noise(w)[proj.v0:proj.v1])
+    d_vol = torch.from_numpy(vol_h).to(dev)
+    d_y = torch.from_numpy(y_h).to(dev)
+    d_sino = torch.empty(proj.local_sino_shape, dtype=torch.float32, device=dev)
+    d_g = torch.empty(w.shape, dtype=torch.float32, device=dev)
+    if segments is None:
+        counts = torch.tensor([float(ctp.ctp_segment_count(proj.op.plan))], dtype=torch.float64,
+                              device=dev)
+        proj.all_reduce(counts)
+        segments = int(counts.item())
+
+    def step():
+        proj.forward(d_vol, d_sino)
+        proj.backward(d_y, d_g)
+
+    def timed(body, n):
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            body()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return a.elapsed_time(b)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    total_ms = max_over_ranks(timed(step, args.steps), world)
+    clocks = sampler.stop()
+    ms_per_step = total_ms / args.steps
+    value = 2.0 * segments / (ms_per_step * 1e-3) / 1e9
+    fwd_ms = max_over_ranks(timed(lambda: proj.forward(d_vol, d_sino), args.steps), world) / args.steps
+    bwd_ms = max_over_ranks(timed(lambda: proj.backward(d_y, d_g), args.steps), world) / args.steps
+
+    # end to end: every step each rank uploads the volume and its sinogram rows
+    # from pinned memory, runs the pair (with the all-reduce) and downloads its
+    # sinogram rows and the volume
+    vol_pin = torch.from_numpy(vol_h).pin_memory()
+    y_pin = torch.from_numpy(y_h).pin_memory()
+    sino_pin = torch.empty(proj.local_sino_shape, dtype=torch.float32).pin_memory()
+    g_pin = torch.empty(w.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        d_vol.copy_(vol_pin, non_blocking=True)
+        proj.forward(d_vol, d_sino)
+        sino_pin.copy_(d_sino, non_blocking=True)
+        d_y.copy_(y_pin, non_blocking=True)
+        proj.backward(d_y, d_g)
+        g_pin.copy_(d_g, non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    e2e_step()
+    e2e_steps = max(1, min(args.steps, 3))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+    e2e_value = 2.0 * segments / e2e_s / 1e9
+    io = 4 * (world * w.n_voxels + w.n_rays)
+    plan_path = proj.op.plan.path
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "views": w.n_views, "detector_vu": [w.n_v, w.n_u],
+                       "segments_per_pass": segments, "path": plan_path,
+                       "parallelism": f"views{world}",
+                       "views_per_rank": [list(ctp.view_shard(w.n_views, world, r))
+                                          for r in range(world)],
+                       "collective": "one all-reduce (sum) of the volume per backward",
+                       "fwd_ms": fwd_ms, "bwd_ms_with_all_reduce": bwd_ms,
+                       "l2": "inputs larger than L2 (no flush)" if 4 * w.n_voxels > 126e6
+                       else "inputs smaller than L2 (no flush)"},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": io,
+                    "d2h_bytes_per_step": io, "ms_per_step": e2e_s * 1e3},
+            "gpu_launches": (2 if plan_path == "ray" else 4) * args.steps * world,
+            "timing": "K eager steps between CUDA events on the calls' stream, max over ranks",
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    proj.destroy()
+    return 0
+
+
 # ------------------------------------------------------ analytical FDK (second op)
 FDK_METRIC = "FDK voxel-view updates/s (ramp filter + weighted gather) on 1 B300"
 FDK_UNIT = "Gvox-view/s"
@@ -794,6 +906,10 @@ def main(argv=None):
     ap.add_argument("--path", default="auto", choices=["auto", "ray", "column"])
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--partition", default="replicas", choices=["replicas", "views"],
+                    help="replicas: every rank runs the whole workload (weak scaling, the "
+                         "default); views: the workload's views are sharded over the ranks "
+                         "and the backward's volume is all-reduced (strong scaling)")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the forward / backward timings of the other four workloads")
     ap.add_argument("--op", default="siddon", choices=["siddon", "fdk", "geometry"],
@@ -815,6 +931,8 @@ def main(argv=None):
             return run_fdk(args, w, world, rank, local)
         if args.op == "geometry":
             return run_geometry(args, w, world, rank, local)
+        if args.partition == "views":
+            return run_partitioned(args, w, world, rank, local)
         return run_gpu(args, w, world, rank, local)
     finally:
         if world > 1:
