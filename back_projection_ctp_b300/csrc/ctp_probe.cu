@@ -15,6 +15,9 @@
 //                           sector instead (1 float per sector), the sector rate.
 //   ctp_probe_l2_load       coalesced 16-byte loads that bypass L1 (ld.global.cg)
 //                           from a buffer that stays in L2.
+//   ctp_probe_smem_accumulate  float accumulation in shared memory: atomics,
+//                           plain load-add-store, and atomics with 4 lanes per
+//                           word (a work-layout question of the backward walks).
 //
 // Both walk the buffer with a per-warp stride so that concurrent warps touch
 // different lines; the caller times them with CUDA events on `stream`.
@@ -60,6 +63,29 @@ __global__ void __launch_bounds__(256) probe_load_kernel(const float4 *__restric
     if (acc == 1.2345e-30f) sink[0] = acc;  // keeps the loads; never true for the probe's data
 }
 
+// Shared-memory float accumulation: every thread adds `iters` times into its
+// own word of a block-wide array (no two lanes on one word).  mode 0: atomicAdd
+// on shared memory; mode 1: plain load, add and store; mode 2: atomicAdd where
+// the 32 lanes of a warp share 8 words (4 lanes per word).
+__global__ void __launch_bounds__(256) probe_smem_kernel(int iters, int mode, float *__restrict__ sink)
+{
+    __shared__ float acc[256];
+    acc[threadIdx.x] = 0.0f;
+    __syncthreads();
+    const int w = mode == 2 ? (threadIdx.x & ~31) + ((threadIdx.x & 31) >> 2) : threadIdx.x;
+    const float v = 1.0f + 1e-3f * (threadIdx.x & 31);
+    if (mode == 1) {
+        for (int it = 0; it < iters; ++it) {
+            volatile float *a = acc;
+            a[w] = a[w] + v;
+        }
+    } else {
+        for (int it = 0; it < iters; ++it) atomicAdd(acc + w, v);
+    }
+    __syncthreads();
+    if (acc[threadIdx.x] == 1.2345e-30f) sink[0] = acc[threadIdx.x];
+}
+
 int blocks_for(int sms) { return sms * 8; }
 
 }  // namespace
@@ -99,6 +125,19 @@ int ctp_probe_l2_load(const float *buf, long long n, int iters, float *sink, voi
         return 1;
     probe_load_kernel<<<blocks_for(sms), 256, 0, (cudaStream_t)stream>>>(
         reinterpret_cast<const float4 *>(buf), n / 4, iters, sink);
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+// Shared-memory accumulation rate (see probe_smem_kernel): 8 blocks of 256
+// threads per SM, `iters` adds per thread.  Returns 0, 1 or 9.
+int ctp_probe_smem_accumulate(int iters, int mode, float *sink, void *stream)
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 9;
+    if (!sink || iters < 1 || mode < 0 || mode > 2) return 1;
+    probe_smem_kernel<<<blocks_for(sms), 256, 0, (cudaStream_t)stream>>>(iters, mode, sink);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 
