@@ -56,7 +56,7 @@ class _PlanOptions(ctypes.Structure):
 
 # Work-layout options of a plan (include/ctp.h, ctp_plan_options); keyword values
 # accepted by ctp_plan(..., options=...).
-PLANE_BACKWARD = {"auto": 0, "tiled": 1, "privatised": 2, "tiled_groups": 3}
+PLANE_BACKWARD = {"auto": 0, "tiled": 1, "privatised": 2}
 GEOMETRY_WALK = {"auto": 0, "ray": 1}
 
 
@@ -272,8 +272,7 @@ def ctp_plan(geometry: Geometry, volume: Volume, path: str = "auto", options=Non
     """Plan a scan on the current CUDA device.  ``options``: None, or a dict of
     work-layout options (``rows_forward``, ``rows_backward``,
     ``backward_rows_adjacent``, ``plane_backward`` ("auto" / "tiled" /
-    "privatised" / "tiled_groups"), ``host_chunks``, ``geometry_walk`` ("auto" /
-    "ray")); they
+    "privatised"), ``host_chunks``, ``geometry_walk`` ("auto" / "ray")); they
     select among layouts that compute the same operator."""
     lib = load_library()
     opts = _plan_options(options)

@@ -155,8 +155,8 @@ int forward_walk(const ctp_plan_t *plan, int v0, int nv, const float *vol, float
         return ctp::column_walk_forward(P, plan->col, plan->d_table, plan->d_work_fwd, sino, s)
                    ? CTP_E_CUDA : CTP_OK;
     if (plan->path == CTP_PATH_PLANE)
-        return ctp::plane_walk_forward(P, plan->d_table, plan->d_work_fwd, vol, sino, s)
-                   ? CTP_E_CUDA : CTP_OK;
+        return ctp::plane_walk_forward(P, plan->d_table, plan->d_work_fwd, sino, s) ? CTP_E_CUDA
+                                                                                    : CTP_OK;
     return launch_ray(P, 0, vol, sino, nullptr, s);
 }
 
@@ -391,7 +391,7 @@ int validate_options(const ctp_plan_options *o)
     const bool ok = o->rows_forward >= 0 && o->rows_forward <= 4 && o->rows_backward >= 0 &&
                     o->rows_backward <= 4 &&
                     (o->backward_rows_adjacent == 0 || o->backward_rows_adjacent == 1) &&
-                    o->plane_backward >= 0 && o->plane_backward <= 3 && o->host_chunks >= 0 &&
+                    o->plane_backward >= 0 && o->plane_backward <= 2 && o->host_chunks >= 0 &&
                     o->host_chunks <= 64 && (o->geometry_walk == 0 || o->geometry_walk == 1);
     return ok ? CTP_OK : CTP_E_OPTION;
 }
@@ -657,8 +657,7 @@ int ctp_backward(const ctp_plan_t *plan, const float *sino_dev, float *vol_dev, 
     if (st != CTP_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     if (backward_whole(plan))
-        return ctp::plane_backward_whole(ray_params(plan), plan->d_table, sino_dev, vol_dev,
-                                         plan->opt.plane_backward, s)
+        return ctp::plane_backward_whole(ray_params(plan), plan->d_table, sino_dev, vol_dev, s)
                    ? CTP_E_CUDA : CTP_OK;
     if ((st = backward_in(plan, vol_dev, s)) != CTP_OK) return st;
     if (plan->n_rays > 0 && (st = backward_walk(plan, 0, plan->n_views, sino_dev, vol_dev, s)) != CTP_OK)
@@ -801,8 +800,7 @@ int ctp_backward_host(ctp_plan_t *plan, const float *sino_host, float *vol_host,
                             cudaMemcpyHostToDevice, s) != cudaSuccess)
             return host_fail(plan, s, CTP_E_CUDA);
         const float *sino = plan->n_rays > 0 ? plan->d_stage_sino : vol;
-        if (ctp::plane_backward_whole(ray_params(plan), plan->d_table, sino, vol,
-                                      plan->opt.plane_backward, s))
+        if (ctp::plane_backward_whole(ray_params(plan), plan->d_table, sino, vol, s))
             return host_fail(plan, s, CTP_E_CUDA);
     } else {
         if (cudaEventRecord(plan->ev_start, s) != cudaSuccess ||

@@ -52,7 +52,7 @@ enum CheckSite {
     kSiteColumnGather = 10, kSiteColumnScatter, kSiteColumnSinoStore, kSiteColumnSinoLoad,
     kSiteColumnLayoutIn, kSiteColumnLayoutOut,
     kSitePlaneGather = 20, kSitePlaneScatter, kSitePlaneSinoStore, kSitePlaneSinoLoad,
-    kSitePlaneTile, kSitePlaneTileOut, kSitePlaneStage
+    kSitePlaneTile, kSitePlaneTileOut
 };
 
 #ifdef CTP_CHECK

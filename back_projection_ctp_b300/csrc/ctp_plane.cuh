@@ -278,16 +278,6 @@ struct PlaneGather {
     }
 };
 
-struct PlaneGatherShared {
-    const float *img;  // shared memory: the staged padded copies
-    float acc;
-    int lim;
-    __device__ __forceinline__ void operator()(int a, float d, bool on, int)
-    {
-        if (on && ctp_in(a, lim, kSitePlaneStage)) acc = __fmaf_rn(d, img[a], acc);
-    }
-};
-
 struct PlaneScatter {
     float *__restrict__ img;
     float w;
@@ -333,64 +323,22 @@ __global__ void __launch_bounds__(32 * CH) plane_forward_kernel(RayParams P,
     R.k0 = 0;
     R.k1 = -1;
     R.ell = 0.0f;
-    if (iu < P.n_u) R = T[ray];
-    int ka, kb, la, lb;
-    if (plane_lockstep_range<CH>(R, iu < P.n_u && R.k0 <= R.k1, chunk, ka, kb, la, lb)) {
-        PlaneGather op{img, 0.0f, plane_cells(P)};
-        plane_walk_lockstep(R, ka, kb, la, lb, op);
-        acc = op.acc;
-    }
-    part[chunk][lane] = acc;
-    __syncthreads();
-    if (chunk == 0 && iu < P.n_u) {
-        float sum = 0.0f;
-#pragma unroll
-        for (int c = 0; c < CH; ++c) sum = __fadd_rn(sum, part[c][lane]);
-        if (ctp_in(ray, sino_cells(P), kSitePlaneSinoStore)) sino[ray] = __fmul_rn(sum, R.ell);
-    }
-}
-
-// Small images: the forward stages the image itself in shared memory -- both
-// padded copies, zero halo included, in the layout the rays' addresses index --
-// and walks it there, so a call is one launch (no layout pass).  img: the
-// caller's (ny, nx) x-fastest image.  Dynamic shared memory: plane_cells(P)
-// floats.
-template <int CH>
-__global__ void __launch_bounds__(32 * CH) plane_forward_staged_kernel(RayParams P,
-                                                                       const PlaneRay *__restrict__ T,
-                                                                       const float *__restrict__ img,
-                                                                       float *__restrict__ sino)
-{
-    extern __shared__ float stage[];
-    __shared__ float part[CH][32];
-    const int nx = P.n[0], ny = P.n[1];
-    const int px = nx + 2 * kPlaneHalo, py = ny + 2 * kPlaneHalo, off1 = px * py;
-    const int cells = 2 * off1;
-    for (int i = threadIdx.x; i < cells; i += blockDim.x) stage[i] = 0.0f;
-    __syncthreads();
-    for (int i = threadIdx.x; i < nx * ny; i += blockDim.x) {
-        const int x = i % nx, y = i / nx;
-        const float v = __ldg(img + i);
-        const int a = (y + kPlaneHalo) * px + x + kPlaneHalo;
-        const int b = off1 + (x + kPlaneHalo) * py + y + kPlaneHalo;
-        if (ctp_in(a, cells, kSitePlaneStage)) stage[a] = v;
-        if (ctp_in(b, cells, kSitePlaneStage)) stage[b] = v;
-    }
-    __syncthreads();
-    const int lane = threadIdx.x & 31, chunk = threadIdx.x >> 5;
-    const int iu = blockIdx.x * 32 + lane;
-    const long long ray = (long long)(P.view0 + (int)blockIdx.y) * P.n_u + iu;
-    float acc = 0.0f;
-    PlaneRay R;
-    R.k0 = 0;
-    R.k1 = -1;
-    R.ell = 0.0f;
-    if (iu < P.n_u) R = T[ray];
-    int ka, kb, la, lb;
-    if (plane_lockstep_range<CH>(R, iu < P.n_u && R.k0 <= R.k1, chunk, ka, kb, la, lb)) {
-        PlaneGatherShared op{stage, 0.0f, cells};
-        plane_walk_lockstep(R, ka, kb, la, lb, op);
-        acc = op.acc;
+    // Each ray walks its own chunk of its own slab range (a lockstep walk over
+    // the warp's union of ranges measured slower for the gather: C2 forward
+    // 0.162 -> 0.193 ms, the idle iterations cost more issue than the wider
+    // loads did).
+    if (iu < P.n_u) {
+        R = T[ray];
+        if (R.k0 <= R.k1) {
+            const int len = (R.k1 - R.k0 + CH) / CH;
+            const int ka = R.k0 + chunk * len;
+            const int kb = min(ka + len - 1, R.k1);
+            if (ka <= kb) {
+                PlaneGather op{img, 0.0f, plane_cells(P)};
+                plane_walk_range(R, ka, kb, op);
+                acc = op.acc;
+            }
+        }
     }
     part[chunk][lane] = acc;
     __syncthreads();
@@ -516,19 +464,17 @@ __global__ void __launch_bounds__(256) plane_unpack_kernel(PlaneLayout G,
 // is added to the zeroed output once.  Every (slab, cell) piece of a ray lies in
 // exactly one tile, so the tiles together visit exactly the pieces of the walk.
 // ---------------------------------------------------------------------------
-constexpr int kTile = 32;       // tile of the multi-launch tiled backward
-constexpr int kTileSmall = 8;   // tile of the one-launch backward of small scans
+constexpr int kTile = 32;
 
-template <int TILE>
 struct TileScatter {
-    float *tile;      // shared memory, (TILE) x (TILE + 1), x fastest
+    float *tile;      // shared memory, (kTile) x (kTile + 1), x fastest
     float w;
     int jlo;          // mirrored transverse index of the tile's first in-tile cell
     unsigned tb;      // tile extent along the transverse axis
     __device__ __forceinline__ void operator()(int a, float d, bool on, int jb)
     {
         if (on && d > 0.0f && (unsigned)(jb - jlo) < tb &&
-            ctp_in(a, TILE * (TILE + 1), kSitePlaneTile))
+            ctp_in(a, kTile * (kTile + 1), kSitePlaneTile))
             atomicAdd(tile + a, __fmul_rn(d, w));
     }
 };
@@ -558,21 +504,17 @@ __device__ __forceinline__ float plane_project_u(const ViewFrame &V, int beam, f
     return num / den;
 }
 
-// STORE: one block per tile walks every view and stores its finished tile (zeros
-// included) -- the whole backward in one launch, no zero-fill, no global
-// atomics; else blocks take view groups and add their tiles to a zeroed output.
-template <int TILE, bool STORE>
 __global__ void __launch_bounds__(256) plane_backward_tiled_kernel(RayParams P,
                                                                    const PlaneRay *__restrict__ T,
                                                                    const float *__restrict__ sino,
                                                                    float *__restrict__ out,
                                                                    int views_per_block)
 {
-    __shared__ float tile[TILE * (TILE + 1)];
-    const int ntx = (P.n[0] + TILE - 1) / TILE;
-    const int tx0 = (blockIdx.x % ntx) * TILE, ty0 = (blockIdx.x / ntx) * TILE;
-    const int tnx = min(TILE, P.n[0] - tx0), tny = min(TILE, P.n[1] - ty0);
-    for (int i = threadIdx.x; i < TILE * (TILE + 1); i += blockDim.x) tile[i] = 0.0f;
+    __shared__ float tile[kTile * (kTile + 1)];
+    const int ntx = (P.n[0] + kTile - 1) / kTile;
+    const int tx0 = (blockIdx.x % ntx) * kTile, ty0 = (blockIdx.x / ntx) * kTile;
+    const int tnx = min(kTile, P.n[0] - tx0), tny = min(kTile, P.n[1] - ty0);
+    for (int i = threadIdx.x; i < kTile * (kTile + 1); i += blockDim.x) tile[i] = 0.0f;
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int s_begin = blockIdx.y * views_per_block;
@@ -619,8 +561,8 @@ __global__ void __launch_bounds__(256) plane_backward_tiled_kernel(RayParams P,
             const int jlo = mb ? nbv - tb0 - tbn : tb0;
             const int ka = max(R.k0, klo), kb = min(R.k1, klo + tpn - 1);
             if (ka > kb) continue;
-            // shared-memory address of mirrored cell (k, j): x fastest, row pitch TILE + 1
-            const int pitch = TILE + 1;
+            // shared-memory address of mirrored cell (k, j): x fastest, row pitch kTile + 1
+            const int pitch = kTile + 1;
             const int sp = (p == 0 ? 1 : pitch) * (mp ? -1 : 1);
             const int sb = (p == 0 ? pitch : 1) * (mb ? -1 : 1);
             // natural local index of mirrored k is (mp ? np-1-k : k) - tp0, likewise for j
@@ -630,21 +572,18 @@ __global__ void __launch_bounds__(256) plane_backward_tiled_kernel(RayParams P,
             L.addr = cp + cb + sp * R.k0 + sb * R.jb;
             L.sp = sp;
             L.sb = sb;
-            TileScatter<TILE> op{tile, __fmul_rn(R.ell, y), jlo, (unsigned)tbn};
+            TileScatter op{tile, __fmul_rn(R.ell, y), jlo, (unsigned)tbn};
             plane_walk_range(L, ka, kb, op);
         }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < TILE * TILE; i += blockDim.x) {
-        const int ly = i / TILE, lx = i % TILE;
+    for (int i = threadIdx.x; i < kTile * kTile; i += blockDim.x) {
+        const int ly = i / kTile, lx = i % kTile;
         if (lx < tnx && ly < tny) {
-            const float v = tile[ly * (TILE + 1) + lx];
+            const float v = tile[ly * (kTile + 1) + lx];
             const long long o = (long long)(ty0 + ly) * P.n[0] + tx0 + lx;
-            if (STORE) {
-                if (ctp_in(o, (long long)P.n[0] * P.n[1], kSitePlaneTileOut)) out[o] = v;
-            } else if (v != 0.0f && ctp_in(o, (long long)P.n[0] * P.n[1], kSitePlaneTileOut)) {
+            if (v != 0.0f && ctp_in(o, (long long)P.n[0] * P.n[1], kSitePlaneTileOut))
                 atomicAdd(out + o, v);
-            }
         }
     }
 }
@@ -726,54 +665,26 @@ inline dim3 plane_tgrid(const PlaneLayout &G)
 // tiled backward, which walks all views in one launch (plane_backward_whole).
 // Larger ones use fire-and-forget global reductions into the privatised padded
 // copies, which measured faster than shared-memory float atomics (C2: 0.46 vs
-// 0.66 ms).  mode (a plan option): 0 = by size, 1 = tiled (one launch where
-// the scan allows, else view groups), 2 = privatised, 3 = tiled in view groups.
+// 0.66 ms).  mode: 0 = by size, 1 = tiled, 2 = privatised (a plan option).
 inline bool plane_backward_tiled(const RayParams &P, int mode)
 {
-    if (mode == 1 || mode == 3) return true;
+    if (mode == 1) return true;
     if (mode == 2) return false;
     return (long long)P.n_views * P.n_u <= 65536;
 }
 
-// Images whose two padded copies fit in 48 KiB of shared memory (about 74 x 74
-// cells) take the one-launch forward: the walk kernel stages the caller's image.
-inline bool plane_forward_staged(const RayParams &P)
-{
-    return plane_cells(P) * (long long)sizeof(float) <= 48 * 1024;
-}
-
-// Small scans whose image splits into at least 16 tiles of 8 x 8 take the
-// one-launch backward (a block per tile over every view).
-inline bool plane_backward_one_launch(const RayParams &P)
-{
-    const long long tiles = (long long)((P.n[0] + kTileSmall - 1) / kTileSmall) *
-                            ((P.n[1] + kTileSmall - 1) / kTileSmall);
-    return (long long)P.n_views * P.n_u <= 16384 && tiles >= 16 && tiles <= 4096;
-}
-
 inline int plane_layout_in(const RayParams &P, float *d_fwd, const float *img, cudaStream_t s)
 {
-    if (plane_forward_staged(P)) return 0;  // the walk reads the caller's image
     const PlaneLayout G = plane_layout(P);
     plane_pack_kernel<<<plane_tgrid(G), 256, 0, s>>>(G, img, d_fwd);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 
 inline int plane_walk_forward(const RayParams &P, const void *d_rays, const float *d_fwd,
-                              const float *img, float *sino, cudaStream_t s)
+                              float *sino, cudaStream_t s)
 {
     if (P.view_count <= 0) return 0;
     const PlaneRay *T = (const PlaneRay *)d_rays;
-    if (plane_forward_staged(P)) {
-        const size_t smem = sizeof(float) * (size_t)plane_cells(P);
-        switch (plane_chunks(P)) {
-        case 8: plane_forward_staged_kernel<8><<<plane_chunk_grid(P), 256, smem, s>>>(P, T, img, sino); break;
-        case 4: plane_forward_staged_kernel<4><<<plane_chunk_grid(P), 128, smem, s>>>(P, T, img, sino); break;
-        case 2: plane_forward_staged_kernel<2><<<plane_chunk_grid(P), 64, smem, s>>>(P, T, img, sino); break;
-        default: plane_forward_staged_kernel<1><<<plane_chunk_grid(P), 32, smem, s>>>(P, T, img, sino); break;
-        }
-        return cudaGetLastError() == cudaSuccess ? 0 : 9;
-    }
     switch (plane_chunks(P)) {
     case 8: plane_forward_kernel<8><<<plane_chunk_grid(P), 256, 0, s>>>(P, T, d_fwd, sino); break;
     case 4: plane_forward_kernel<4><<<plane_chunk_grid(P), 128, 0, s>>>(P, T, d_fwd, sino); break;
@@ -817,19 +728,13 @@ inline int plane_layout_out(const RayParams &P, const float *d_bwd, float *img, 
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 
-// Small scans: one block per 8 x 8 tile over every view, storing the output
-// (one launch); or zero the output and take one block per (32 x 32 tile, view
-// group), all views.
+// Small scans: zero the output, one block per (32 x 32 tile, view group), all
+// views.  (A one-launch variant -- one block per 8 x 8 tile over every view,
+// storing its tile -- measured slower on the 64 x 64 scan: 0.048 against
+// 0.022 ms; a block then walks all 90 views serially.)
 inline int plane_backward_whole(const RayParams &P, const void *d_rays, const float *sino,
-                                float *img, int mode, cudaStream_t s)
+                                float *img, cudaStream_t s)
 {
-    if ((long long)P.n_views * P.n_u > 0 && mode != 3 && plane_backward_one_launch(P)) {
-        const int tiles = ((P.n[0] + kTileSmall - 1) / kTileSmall) *
-                          ((P.n[1] + kTileSmall - 1) / kTileSmall);
-        plane_backward_tiled_kernel<kTileSmall, true><<<dim3(tiles, 1), 256, 0, s>>>(
-            P, (const PlaneRay *)d_rays, sino, img, P.n_views);
-        return cudaGetLastError() == cudaSuccess ? 0 : 9;
-    }
     if (cudaMemsetAsync(img, 0, sizeof(float) * (size_t)P.n[0] * P.n[1], s) != cudaSuccess)
         return 9;
     if ((long long)P.n_views * P.n_u == 0) return 0;
@@ -838,7 +743,7 @@ inline int plane_backward_whole(const RayParams &P, const void *d_rays, const fl
     groups = max(1, min(groups, (P.n_views + 7) / 8));
     const int vpb = (P.n_views + groups - 1) / groups;
     groups = (P.n_views + vpb - 1) / vpb;
-    plane_backward_tiled_kernel<kTile, false><<<dim3(tiles, groups), 256, 0, s>>>(
+    plane_backward_tiled_kernel<<<dim3(tiles, groups), 256, 0, s>>>(
         P, (const PlaneRay *)d_rays, sino, img, vpb);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }

@@ -417,7 +417,7 @@ def run_gpu(args, w, world, rank, local):
     frames = ci.frames(w)
     vol_h = ci.phantom(w)
     y_h = ci.sinogram_noise(w)
-    plan = ctp.ctp_plan(geometry_of(w, frames), volume_of(w), args.path)
+    plan = ctp.ctp_plan(geometry_of(w, frames), volume_of(w), args.path, options=args.plan_options)
     if args.views is None:
         segments = golden_segments(args.config)
         seg_source = "float64 oracle (tests/golden/segment_counts.json)"
@@ -910,6 +910,9 @@ def main(argv=None):
                     help="replicas: every rank runs the whole workload (weak scaling, the "
                          "default); views: the workload's views are sharded over the ranks "
                          "and the backward's volume is all-reduced (strong scaling)")
+    ap.add_argument("--plan-options", type=json.loads, default=None,
+                    help="work-layout options of the plan as JSON, e.g. "
+                         "'{\"backward_staged\": \"direct\"}' (ctp_plan_options)")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the forward / backward timings of the other four workloads")
     ap.add_argument("--op", default="siddon", choices=["siddon", "fdk", "geometry"],

@@ -130,12 +130,9 @@ typedef struct ctp_plan ctp_plan_t;
  *   backward_rows_adjacent  column path with 2 rows per backward thread: 1 =
  *                 each reduction instruction covers 32 adjacent rows; 0 = a
  *                 thread's two rows are interleaved across lanes (default).
- *   plane_backward  plane path: 0 = by scan size (shared-memory tiles up to
- *                 65536 rays -- one launch of a block per 8 x 8 tile over every
- *                 view up to 16384 rays, else 32 x 32 tiles in view groups added
- *                 to a zero-filled output -- else privatised global
- *                 reductions); 1 = always tiles (as for 0); 2 = always
- *                 privatised; 3 = always 32 x 32 tiles in view groups.
+ *   plane_backward  plane path: 0 = by scan size (shared-memory tiles in view
+ *                 groups up to 65536 rays, else privatised global reductions);
+ *                 1 = always tiled; 2 = always privatised.
  *   host_chunks   host-buffer calls: number of view chunks the walk and the
  *                 sinogram copies are pipelined in, 1 to 64 (0: one per 64 MiB
  *                 of sinogram, at most 8); never more than the views.

@@ -115,11 +115,10 @@ def test_ray_and_plane_paths_agree(torch, ctp, idx):
     assert rel_l2(out["plane"][1], out["ray"][1]) <= TOL_BACKWARD
 
 
-@pytest.mark.parametrize("mode", ["tiled", "privatised", "tiled_groups"])
+@pytest.mark.parametrize("mode", ["tiled", "privatised"])
 def test_plane_backward_variants_match_oracle(torch, ctp, oracle_mod, mode):
-    """The plane backward's work layouts (shared-memory tiles for small scans --
-    one launch of 8 x 8 tiles over every view, or 32 x 32 tiles in view groups --
-    and privatised global accumulators for larger ones) on the same scan."""
+    """The plane backward's two work layouts (shared-memory tiles for small
+    scans, privatised global accumulators for larger ones) on the same scan."""
     w = SMALL[2]
     f = ci.frames(w)
     scan = oracle_mod.Scan.from_workload(w, f)
@@ -175,7 +174,7 @@ def test_tilted_2d_frames_fall_back_to_ray_path(torch, ctp, oracle_mod):
 
 @pytest.mark.parametrize("idx,path,backward", [(3, "auto", None), (3, "ray", None),
                                                (2, "auto", "privatised"), (2, "auto", "tiled"),
-                                               (2, "auto", "tiled_groups"), (5, "auto", None)])
+                                               (5, "auto", None)])
 @pytest.mark.parametrize("chunks", [0, 1, 3, 7])
 @pytest.mark.parametrize("pinned", [False, True])
 def test_host_entry_points_match_device(torch, ctp, idx, path, backward, chunks, pinned):
