@@ -39,7 +39,7 @@ class _Geometry(ctypes.Structure):
                 ("det_u", ctypes.c_void_p), ("det_v", ctypes.c_void_p),
                 ("pitch_u", ctypes.c_double), ("pitch_v", ctypes.c_double),
                 ("offset_u", ctypes.c_double), ("offset_v", ctypes.c_double),
-                ("pixel_offsets", ctypes.c_void_p)]
+                ("pixel_offsets", ctypes.c_void_p), ("offsets_per_view", ctypes.c_int)]
 
 
 class _Volume(ctypes.Structure):
@@ -85,7 +85,7 @@ EXPORTS = ("ctp_plan", "ctp_plan_ex", "ctp_destroy", "ctp_plan_info_get", "ctp_f
            "ctp_segment_count", "ctp_forward_host", "ctp_backward_host", "ctp_status_string",
            "ctp_forward_static", "ctp_ramp_filter", "ctp_weighted_backproject",
            "ctp_weighted_backproject_transpose", "ctp_fdk", "ctp_geometry_vjp",
-           "ctp_parker_weights", "ctp_check_violations")
+           "ctp_parker_weights", "ctp_check_violations", "ctp_surface_vjp")
 
 RAMPS = {"ramlak": 0, "shepp_logan": 1, "cosine": 2, "hamming": 3, "hann": 4}
 
@@ -122,6 +122,7 @@ def load_library(path: str | None = None):
         lib.ctp_fdk.argtypes = [P, P, P, P, P, P, I, P]
         lib.ctp_parker_weights.argtypes = [P, P, P]
         lib.ctp_geometry_vjp.argtypes = [P, P, P, P, P]
+        lib.ctp_surface_vjp.argtypes = [P, P, P, P, P]
         lib.ctp_check_violations.argtypes = [ctypes.POINTER(ctypes.c_ulonglong),
                                              ctypes.POINTER(ctypes.c_longlong),
                                              ctypes.POINTER(ctypes.c_longlong),
@@ -160,7 +161,8 @@ class Geometry:
     offset_u: float = 0.0
     offset_v: float = 0.0
     # curved detector: (n_v, n_u, 3) per-pixel (t, s, e) offsets from det_centre
-    # along det_u, det_v and the unit normal det_u x det_v; None = the pitch grid
+    # along det_u, det_v and the unit normal det_u x det_v, shared by all views,
+    # or (n_views, n_v, n_u, 3) one table per view; None = the pitch grid
     pixel_offsets: np.ndarray | None = None
 
 
@@ -235,13 +237,19 @@ def _c_scan(geometry: Geometry, volume: Volume):
 
 
 def _pixel_offsets(geometry: Geometry, g: _Geometry):
-    """Sets g.pixel_offsets; returns the array that must outlive the call."""
+    """Sets g.pixel_offsets (and g.offsets_per_view); returns the array that must
+    outlive the call."""
+    g.offsets_per_view = 0
     if geometry.pixel_offsets is None:
         g.pixel_offsets = None
         return None
     off = np.ascontiguousarray(geometry.pixel_offsets, dtype=np.float32)
-    if off.size != 3 * int(geometry.n_u) * int(geometry.n_v):
-        raise ValueError("pixel_offsets must hold (n_v, n_u, 3) values")
+    per = 3 * int(geometry.n_u) * int(geometry.n_v)
+    n_views = np.asarray(geometry.src).reshape(-1, 3).shape[0]
+    if off.ndim == 4 and off.size == per * n_views:
+        g.offsets_per_view = 1
+    elif off.size != per:
+        raise ValueError("pixel_offsets must hold (n_v, n_u, 3) or (n_views, n_v, n_u, 3) values")
     g.pixel_offsets = off.ctypes.data
     return off
 
@@ -479,4 +487,25 @@ def ctp_geometry_vjp(plan: Plan, vol, weight, grad=None, stream=None):
         plan.handle, _device_f32(vol, plan.vol_shape, "vol"),
         _device_f32(weight, plan.sino_shape, "weight"), grad.data_ptr(), _stream_ptr(stream)),
         "ctp_geometry_vjp")
+    return grad
+
+
+def ctp_surface_vjp(plan: Plan, vol, weight, grad=None, stream=None):
+    """grad[iv, iu, m] = sum over views of weight[view, iv, iu] * d (A vol)[ray] / d
+    offset_m of pixel (iu, iv), offsets (t, s, e) along det_u, det_v and the unit
+    normal: a float64 CUDA tensor (n_v, n_u, 3); with one offset table per view
+    (n_views, n_v, n_u, 3), each view's pixel its own gradient."""
+    import torch
+    per_view = plan.geometry.pixel_offsets is not None and plan.geometry.pixel_offsets.ndim == 4
+    shape = ((plan.sino_shape[0],) if per_view else ()) + (plan.sino_shape[1],
+                                                           plan.sino_shape[2], 3)
+    if grad is None:
+        grad = torch.empty(shape, dtype=torch.float64, device=vol.device)
+    if not (isinstance(grad, torch.Tensor) and grad.is_cuda and grad.dtype == torch.float64
+            and grad.is_contiguous() and grad.numel() == int(np.prod(shape))):
+        raise TypeError(f"grad must be a contiguous float64 CUDA tensor of {shape} elements")
+    _check(load_library().ctp_surface_vjp(
+        plan.handle, _device_f32(vol, plan.vol_shape, "vol"),
+        _device_f32(weight, plan.sino_shape, "weight"), grad.data_ptr(), _stream_ptr(stream)),
+        "ctp_surface_vjp")
     return grad

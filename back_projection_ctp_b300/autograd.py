@@ -17,7 +17,7 @@ import torch
 import dataclasses
 
 from ._binding import (Geometry, Plan, Volume, ctp_backward, ctp_forward, ctp_geometry_vjp,
-                       ctp_plan, ctp_ramp_filter, ctp_weighted_backproject,
+                       ctp_plan, ctp_ramp_filter, ctp_surface_vjp, ctp_weighted_backproject,
                        ctp_weighted_backproject_transpose)
 
 
@@ -160,24 +160,37 @@ FRAME_NAMES = ("src", "det_centre", "det_u", "det_v")
 
 def project_with_geometry(vol: torch.Tensor, geometry: Geometry, volume: Volume,
                           src: torch.Tensor, det_centre: torch.Tensor, det_u: torch.Tensor,
-                          det_v: torch.Tensor, path: str = "auto") -> torch.Tensor:
+                          det_v: torch.Tensor, path: str = "auto",
+                          pixel_offsets: torch.Tensor | None = None) -> torch.Tensor:
     """A vol with the per-view frames as differentiable inputs: the gradient
     with respect to each frame tensor (n_views, 3) is the first-order geometry
     gradient of the pages ("first-order source / centre / axis gradients";
     trajectory tensors that require gradients receive geometry gradients,
     README "Arbitrary trajectories").  ``geometry`` supplies the detector size,
     pitches and offsets; its frame arrays are replaced by the tensors' values
-    (a plan is built for them on every call).  vol: (..., D, H, W); the
-    geometry gradient sums over leading dims.  First order in the frames."""
-    return _ProjectGeometry.apply(vol, geometry, volume, path, src, det_centre, det_u, det_v)
+    (a plan is built for them on every call).  ``pixel_offsets`` (n_v, n_u, 3)
+    or (n_views, n_v, n_u, 3), optional: a curved detector's per-pixel (t, s,
+    e) offsets along det_u, det_v and the unit normal, shared by the views or
+    one table per view, replacing ``geometry.pixel_offsets``; its
+    gradient is the first-order surface gradient (README "Curved detectors":
+    projection supports first-order surface gradients).  vol: (..., D, H, W);
+    the geometry and surface gradients sum over leading dims.  First order."""
+    return _ProjectGeometry.apply(vol, geometry, volume, path, pixel_offsets, src, det_centre,
+                                  det_u, det_v)
 
 
 class _ProjectGeometry(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, vol, geometry, volume, path, *frames):
+    def forward(ctx, vol, geometry, volume, path, offsets, *frames):
         values = [f.detach().to(device="cpu", dtype=torch.float32).contiguous().numpy()
                   for f in frames]
         geo = dataclasses.replace(geometry, **dict(zip(FRAME_NAMES, values)))
+        ctx.off_meta = None
+        if offsets is not None:
+            geo = dataclasses.replace(
+                geo, pixel_offsets=offsets.detach().to(device="cpu", dtype=torch.float32)
+                .contiguous().numpy())
+            ctx.off_meta = (offsets.dtype, offsets.device, tuple(offsets.shape))
         proj = Projector(geo, volume, path)
         ctx.proj = proj
         ctx.frame_meta = [(f.dtype, f.device) for f in frames]
@@ -194,19 +207,33 @@ class _ProjectGeometry(torch.autograd.Function):
         if ctx.needs_input_grad[0]:
             g_vol = _Backproject.apply(grad, proj).to(dtype=ctx.in_dtype, device=ctx.in_device)
         g_frames = [None] * 4
-        if any(ctx.needs_input_grad[4:]):
+        g_off = None
+        want_frames = any(ctx.needs_input_grad[5:])
+        want_off = ctx.off_meta is not None and ctx.needs_input_grad[4]
+        if want_frames or want_off:
             grad = grad.detach().to(device=proj.device, dtype=torch.float32).contiguous()
             _batched(grad, proj.sino_shape, "grad")
             v = vol.reshape((-1,) + tuple(proj.vol_shape))
             gr = grad.reshape((-1,) + tuple(proj.sino_shape))
-            total = torch.zeros((proj.sino_shape[0], 4, 3), dtype=torch.float64,
-                                device=proj.device)
-            part = torch.empty_like(total)
             stream = torch.cuda.current_stream(proj.device)
-            for i in range(gr.shape[0]):   # leading dims of vol and grad agree
-                ctp_geometry_vjp(proj.plan, v[i].contiguous(), gr[i].contiguous(), part, stream)
-                total += part
-            for q, (dt, dev) in enumerate(ctx.frame_meta):
-                if ctx.needs_input_grad[4 + q]:
-                    g_frames[q] = total[:, q, :].to(dtype=dt, device=dev)
-        return (g_vol, None, None, None, *g_frames)
+            if want_frames:
+                total = torch.zeros((proj.sino_shape[0], 4, 3), dtype=torch.float64,
+                                    device=proj.device)
+                part = torch.empty_like(total)
+                for i in range(gr.shape[0]):   # leading dims of vol and grad agree
+                    ctp_geometry_vjp(proj.plan, v[i].contiguous(), gr[i].contiguous(), part,
+                                     stream)
+                    total += part
+                for q, (dt, dev) in enumerate(ctx.frame_meta):
+                    if ctx.needs_input_grad[5 + q]:
+                        g_frames[q] = total[:, q, :].to(dtype=dt, device=dev)
+            if want_off:
+                # (n_v, n_u, 3) shared by the views, or (n_views, n_v, n_u, 3)
+                total = torch.zeros(ctx.off_meta[2], dtype=torch.float64, device=proj.device)
+                part = torch.empty_like(total)
+                for i in range(gr.shape[0]):
+                    ctp_surface_vjp(proj.plan, v[i].contiguous(), gr[i].contiguous(), part,
+                                    stream)
+                    total += part
+                g_off = total.to(dtype=ctx.off_meta[0], device=ctx.off_meta[1])
+        return (g_vol, None, None, None, g_off, *g_frames)

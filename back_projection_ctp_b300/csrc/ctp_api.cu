@@ -37,7 +37,8 @@ struct ctp_plan {
     std::vector<ctp::ViewFrame> frames;     // host copy
     std::vector<float> raw;                 // the caller's frames: src, centre, u, v (n_views x 12)
     ctp::ViewFrame *d_frames = nullptr;     // device copy
-    float *d_offsets = nullptr;             // curved detector: (n_v, n_u, 3) pixel offsets
+    float *d_offsets = nullptr;             // curved detector: pixel offsets (t, s, e)
+    int offsets_per_view = 0;               // 1: one (n_v, n_u, 3) table per view
     ctp::ColumnOffsets *d_columns = nullptr;  // curved detector, column path: per column
     unsigned long long *d_counter = nullptr;
     // column and plane paths
@@ -99,6 +100,7 @@ ctp::RayParams ray_params(const ctp_plan_t *plan)
     P.view0 = 0;
     P.view_count = plan->n_views;
     P.offsets = plan->d_offsets;
+    P.offsets_per_view = plan->offsets_per_view;
     P.columns = plan->d_columns;
     return P;
 }
@@ -252,9 +254,12 @@ int validate(const ctp_geometry *g, const ctp_volume *v)
     if (g->ndim == 2 && !(sp[2] > 0.0)) return CTP_E_SPACING;
     if (smax / smin > 1e4) return CTP_E_SPACING;
     if (!(g->pitch_u > 0.0) || !(g->pitch_v > 0.0)) return CTP_E_SHAPE;
-    if (g->pixel_offsets)
-        for (long long q = 0; q < 3LL * g->n_u * g->n_v; ++q)
+    if (g->offsets_per_view != 0 && g->offsets_per_view != 1) return CTP_E_OPTION;
+    if (g->pixel_offsets) {
+        const long long tables = g->offsets_per_view ? g->n_views : 1;
+        for (long long q = 0; q < 3LL * g->n_u * g->n_v * tables; ++q)
             if (!std::isfinite(g->pixel_offsets[q])) return CTP_E_NONFINITE;
+    }
     if (g->n_views == 0) return CTP_OK;
     if (!g->src || !g->det_centre || !g->det_u || !g->det_v) return CTP_E_NULL;
 
@@ -522,21 +527,25 @@ int ctp_plan_ex(const ctp_geometry *geom, const ctp_volume *vol, int path,
     // in every row, vertical offsets affine in the row to 1e-6 of the column's
     // span): circular / helical scans with cylindrical detectors.  Other curved
     // detectors run on the ray path; the plane path assumes the pitch grid.
+    // With one table per view, every view's columns are checked and tabled.
     std::vector<ctp::ColumnOffsets> colq;
+    p->offsets_per_view = curved && geom->offsets_per_view ? 1 : 0;
+    const int tables = p->offsets_per_view ? geom->n_views : 1;
     if (curved) {
         bool columnar = geom->ndim == 3 && geom->n_v >= 2;
-        for (int iu = 0; iu < geom->n_u && columnar; ++iu) {
-            const float *q0 = geom->pixel_offsets + 3 * (long long)iu;
-            const float *q1 = q0 + 3LL * geom->n_u;
-            const double s0 = q0[1], ds = (double)q1[1] - (double)q0[1];
-            const double span = std::fabs(ds) * (geom->n_v - 1);
-            for (int iv = 1; iv < geom->n_v && columnar; ++iv) {
-                const float *q = q0 + 3LL * geom->n_u * iv;
-                columnar = q[0] == q0[0] && q[2] == q0[2] &&
-                           std::fabs((double)q[1] - (s0 + ds * iv)) <= 1e-6 * span;
+        for (int t = 0; t < tables && columnar; ++t)
+            for (int iu = 0; iu < geom->n_u && columnar; ++iu) {
+                const float *q0 = geom->pixel_offsets + 3LL * geom->n_u * geom->n_v * t + 3LL * iu;
+                const float *q1 = q0 + 3LL * geom->n_u;
+                const double s0 = q0[1], ds = (double)q1[1] - (double)q0[1];
+                const double span = std::fabs(ds) * (geom->n_v - 1);
+                for (int iv = 1; iv < geom->n_v && columnar; ++iv) {
+                    const float *q = q0 + 3LL * geom->n_u * iv;
+                    columnar = q[0] == q0[0] && q[2] == q0[2] &&
+                               std::fabs((double)q[1] - (s0 + ds * iv)) <= 1e-6 * span;
+                }
+                colq.push_back(ctp::ColumnOffsets{q0[0], q0[2], s0, ds});
             }
-            colq.push_back(ctp::ColumnOffsets{q0[0], q0[2], s0, ds});
-        }
         if (!columnar) {
             colq.clear();
             v_is_z = false;
@@ -568,7 +577,7 @@ int ctp_plan_ex(const ctp_geometry *geom, const ctp_volume *vol, int path,
     }
     p->device_bytes = fbytes + sizeof(unsigned long long);
     if (curved) {
-        const size_t ob = sizeof(float) * 3 * (size_t)geom->n_u * geom->n_v;
+        const size_t ob = sizeof(float) * 3 * (size_t)geom->n_u * geom->n_v * (size_t)tables;
         if (cudaMalloc(&p->d_offsets, ob) != cudaSuccess ||
             cudaMemcpy(p->d_offsets, geom->pixel_offsets, ob, cudaMemcpyHostToDevice) !=
                 cudaSuccess) {
@@ -608,7 +617,9 @@ int ctp_plan_ex(const ctp_geometry *geom, const ctp_volume *vol, int path,
             p->d_work_bwd = nullptr;
             p->d_columns = nullptr;
             p->device_bytes = fbytes + sizeof(unsigned long long) +
-                              (curved ? sizeof(float) * 3 * (size_t)geom->n_u * geom->n_v : 0);
+                              (curved ? sizeof(float) * 3 * (size_t)geom->n_u * geom->n_v *
+                                            (size_t)tables
+                                      : 0);
             p->path = CTP_PATH_RAY;
             st = CTP_OK;
         }
@@ -896,6 +907,18 @@ int ctp_weighted_backproject_transpose(const ctp_plan_t *plan, const float *vol_
                                                                                 : CTP_OK;
 }
 
+static ctp::GeomParams geom_params(const ctp_plan_t *plan)
+{
+    ctp::GeomParams Q;
+    Q.cu = (float)(0.5 * (plan->n_u - 1) - plan->offset_u);
+    Q.cv = (float)(0.5 * (plan->n_v - 1) - plan->offset_v);
+    Q.pitch_u = (float)plan->pitch_u;
+    Q.pitch_v = (float)plan->pitch_v;
+    Q.pitch_ud = plan->pitch_u;
+    Q.pitch_vd = plan->pitch_v;
+    return Q;
+}
+
 int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *weight_dev,
                      double *grad_dev, void *stream)
 {
@@ -904,15 +927,11 @@ int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *
     if (plan->n_rays > 0 && (!vol_dev || !weight_dev)) return CTP_E_NULL;
     int st = check_device(plan);
     if (st != CTP_OK) return st;
-    if (plan->d_offsets) return CTP_E_OPTION;  // the chain rule assumes the pitch grid
     if (plan->n_views == 0) return CTP_OK;
-    ctp::GeomParams Q;
-    Q.cu = (float)(0.5 * (plan->n_u - 1) - plan->offset_u);
-    Q.cv = (float)(0.5 * (plan->n_v - 1) - plan->offset_v);
-    Q.pitch_u = (float)plan->pitch_u;
-    Q.pitch_v = (float)plan->pitch_v;
+    const ctp::GeomParams Q = geom_params(plan);
     cudaStream_t s = (cudaStream_t)stream;
-    if (plan->path == CTP_PATH_COLUMN && plan->opt.geometry_walk == 0) {
+    // the column walk takes flat detectors; curved ones run the ray walk
+    if (plan->path == CTP_PATH_COLUMN && plan->opt.geometry_walk == 0 && !plan->d_offsets) {
         // the column walk reads the plan's padded z-fastest working copy
         if ((st = forward_in(plan, vol_dev, s)) != CTP_OK) return st;
         return ctp::column_geometry_vjp(ray_params(plan), Q, (const ctp::ColumnTrace *)plan->d_table,
@@ -921,6 +940,24 @@ int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *
     }
     return ctp::geometry_vjp(ray_params(plan), Q, vol_dev, weight_dev, grad_dev, s) ? CTP_E_CUDA
                                                                                    : CTP_OK;
+}
+
+int ctp_surface_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *weight_dev,
+                    double *grad_dev, void *stream)
+{
+    if (!plan) return CTP_E_NULL;
+    if (!grad_dev || (plan->n_rays > 0 && (!vol_dev || !weight_dev))) return CTP_E_NULL;
+    int st = check_device(plan);
+    if (st != CTP_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (plan->n_rays == 0)  // nothing to sum (a per-view table has no views to write)
+        return plan->offsets_per_view ||
+                       cudaMemsetAsync(grad_dev, 0,
+                                       sizeof(double) * 3 * (size_t)plan->n_u * plan->n_v, s) ==
+                           cudaSuccess
+                   ? CTP_OK : CTP_E_CUDA;
+    return ctp::surface_vjp(ray_params(plan), geom_params(plan), vol_dev, weight_dev, grad_dev, s)
+               ? CTP_E_CUDA : CTP_OK;
 }
 
 int ctp_fdk(const ctp_plan_t *plan, const float *sino_dev, float *work_dev, float *vol_dev,

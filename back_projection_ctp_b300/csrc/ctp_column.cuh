@@ -91,7 +91,7 @@ __global__ void column_setup_kernel(RayParams P, ColumnTrace *__restrict__ T,
     // detector's column (t, e fixed, s = s0 + iv ds; frames hold unit axes)
     double P0[3], dvz = V.dv[2];
     if (P.columns) {
-        const ColumnOffsets q = P.columns[iu];
+        const ColumnOffsets q = P.columns[(P.offsets_per_view ? view * P.n_u : 0) + iu];
 #pragma unroll
         for (int a = 0; a < 3; ++a)
             P0[a] = __fma_rn(q.e, V.dn[a], __fma_rn(q.s0, V.dv[a], __fma_rn(q.t, V.du[a], V.p00[a])));

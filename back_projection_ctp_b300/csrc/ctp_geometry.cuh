@@ -44,6 +44,7 @@ namespace ctp {
 struct GeomParams {
     float cu, cv;            // pixel index of the detector centre: (n - 1)/2 - offset
     float pitch_u, pitch_v;
+    double pitch_ud, pitch_vd;  // the pitches in float64 (unit axes of a flat detector)
 };
 
 // Axes, mirrored start and world direction of the ray through pixel (iu, iv):
@@ -59,10 +60,18 @@ __device__ __forceinline__ void ray_axes(const RayParams &P, int view, int iu, i
 {
     const ViewFrame &V = P.views[view];
     double X0[3], w[3];
-    const double fu = (double)iu, fv = (double)iv;
+    double fu = (double)iu, fv = (double)iv, fe = 0.0;
+    if (P.offsets) {
+        // curved detector: the pixel's (t, s, e) offsets along du, dv, dn (as slab_setup)
+        const float *q = pixel_offsets_of(P, view, iu, iv);
+        fu = (double)q[0];
+        fv = (double)q[1];
+        fe = (double)q[2];
+    }
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
-        const double pix = __fma_rn(fv, V.dv[a], __fma_rn(fu, V.du[a], V.p00[a]));
+        double pix = __fma_rn(fv, V.dv[a], __fma_rn(fu, V.du[a], V.p00[a]));
+        if (P.offsets) pix = __fma_rn(fe, V.dn[a], pix);
         X0[a] = P.beam == 1 ? V.a[a] : pix;
         w[a] = P.beam == 1 ? __dsub_rn(pix, V.a[a]) : V.a[a];
     }
@@ -174,6 +183,83 @@ __device__ __forceinline__ void grad_walk(const SlabRay &R, const RayAxes &A,
     }
 }
 
+// Gradient of one ray's path sum with respect to the ray's start and end:
+// dsrc = dp/d source (parallel: dp/d src, the direction) and dpix = dp/d pixel,
+// world axes, from the walk's crossing sums.  False when the ray misses.
+__device__ __forceinline__ bool ray_gradient(const RayParams &P, int view, int iu, int iv,
+                                             const float *__restrict__ vol, float dsrc[3],
+                                             float dpix[3])
+{
+    SlabRay R;
+    if (!slab_setup(P, view, iu, iv, R)) return false;
+    RayAxes A;
+    ray_axes(P, view, iu, iv, A);
+    GradSums S;
+    grad_walk(R, A, vol, volume_cells(P), S);
+    const float p = __fmul_rn(S.path, R.ell);
+    const float rn2 = __fmul_rn(A.rn, A.rn);
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        // the walk axis that is world axis a
+        const int q = A.ax[0] == a ? 0 : (A.ax[1] == a ? 1 : 2);
+        const float df = q == 0 ? S.df[0] : (q == 1 ? S.df[1] : S.df[2]);
+        const float dft = q == 0 ? S.dft[0] : (q == 1 ? S.dft[1] : S.dft[2]);
+        const float ra = A.r[a];
+        const float gx = ra != 0.0f ? -A.rn * df / ra : 0.0f;
+        const float gr = (ra != 0.0f ? -A.rn * dft / ra : 0.0f) + p * ra / rn2;
+        dsrc[a] = P.beam == 1 ? gx - gr : gr;
+        dpix[a] = P.beam == 1 ? gr : gx;
+    }
+    return true;
+}
+
+// Physical detector axes of a view (float64): u, v, the unit normal n = u x v /
+// |u x v| and |u x v|.  Curved frames store the unit axes (and n) over the
+// spacing; flat frames the pitch-scaled axes over the spacing.
+__device__ __forceinline__ void detector_axes(const RayParams &P, const GeomParams &Q, int view,
+                                              double u[3], double v[3], double n[3], double &cn)
+{
+    const ViewFrame &V = P.views[view];
+    const double su = P.offsets ? 1.0 : Q.pitch_ud, sv = P.offsets ? 1.0 : Q.pitch_vd;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        u[a] = __ddiv_rn(__dmul_rn(V.du[a], P.spacing[a]), su);
+        v[a] = __ddiv_rn(__dmul_rn(V.dv[a], P.spacing[a]), sv);
+    }
+    n[0] = __fma_rn(u[1], v[2], -__dmul_rn(u[2], v[1]));
+    n[1] = __fma_rn(u[2], v[0], -__dmul_rn(u[0], v[2]));
+    n[2] = __fma_rn(u[0], v[1], -__dmul_rn(u[1], v[0]));
+    cn = sqrt(__fma_rn(n[0], n[0], __fma_rn(n[1], n[1], __dmul_rn(n[2], n[2]))));
+#pragma unroll
+    for (int a = 0; a < 3; ++a) n[a] = __ddiv_rn(n[a], cn);
+}
+
+// Chain rule of a curved detector's pixel = centre + t u + s v + e n to the
+// axes: with g = dp / d pixel and h = (g - (n.g) n) / |u x v| (dn = (I - n n^T)
+// d(u x v) / |u x v|), dp/du = t g + e v x h and dp/dv = s g - e u x h.
+__device__ __forceinline__ void curved_axis_gradients(const RayParams &P, int view, int iu,
+                                                      int iv, const float g[3], float gu[3],
+                                                      float gv[3])
+{
+    const float *q = pixel_offsets_of(P, view, iu, iv);
+    const GeomParams unused{};
+    double u[3], v[3], n[3], cn;
+    detector_axes(P, unused, view, u, v, n, cn);
+    const double ng = n[0] * g[0] + n[1] * g[1] + n[2] * g[2];
+    double h[3];
+#pragma unroll
+    for (int a = 0; a < 3; ++a) h[a] = ((double)g[a] - ng * n[a]) / cn;
+    const double vh[3] = {v[1] * h[2] - v[2] * h[1], v[2] * h[0] - v[0] * h[2],
+                          v[0] * h[1] - v[1] * h[0]};
+    const double uh[3] = {u[1] * h[2] - u[2] * h[1], u[2] * h[0] - u[0] * h[2],
+                          u[0] * h[1] - u[1] * h[0]};
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        gu[a] = (float)((double)q[0] * g[a] + (double)q[2] * vh[a]);
+        gv[a] = (float)((double)q[1] * g[a] - (double)q[2] * uh[a]);
+    }
+}
+
 template <int TU, int TV>
 __global__ void __launch_bounds__(TU *TV) geometry_vjp_kernel(RayParams P, GeomParams Q,
                                                               const float *__restrict__ vol,
@@ -191,31 +277,26 @@ __global__ void __launch_bounds__(TU *TV) geometry_vjp_kernel(RayParams P, GeomP
     if (iu < P.n_u && iv < P.n_v) {
         const long long ray = ((long long)view * P.n_v + iv) * P.n_u + iu;
         const float wr = w[ray];
-        SlabRay R;
-        if (wr != 0.0f && slab_setup(P, view, iu, iv, R)) {
-            RayAxes A;
-            ray_axes(P, view, iu, iv, A);
-            GradSums S;
-            grad_walk(R, A, vol, volume_cells(P), S);
-            const float p = __fmul_rn(S.path, R.ell);
-            const float rn2 = __fmul_rn(A.rn, A.rn);
-            const float alpha = ((float)iu - Q.cu) * Q.pitch_u;
-            const float beta = ((float)iv - Q.cv) * Q.pitch_v;
+        float dsrc[3], dpix[3];
+        if (wr != 0.0f && ray_gradient(P, view, iu, iv, vol, dsrc, dpix)) {
+            float gu[3], gv[3];
+            if (P.offsets) {
+                curved_axis_gradients(P, view, iu, iv, dpix, gu, gv);
+            } else {
+                const float alpha = ((float)iu - Q.cu) * Q.pitch_u;
+                const float beta = ((float)iv - Q.cv) * Q.pitch_v;
+#pragma unroll
+                for (int a = 0; a < 3; ++a) {
+                    gu[a] = alpha * dpix[a];
+                    gv[a] = beta * dpix[a];
+                }
+            }
 #pragma unroll
             for (int a = 0; a < 3; ++a) {
-                // the walk axis that is world axis a
-                const int q = A.ax[0] == a ? 0 : (A.ax[1] == a ? 1 : 2);
-                const float df = q == 0 ? S.df[0] : (q == 1 ? S.df[1] : S.df[2]);
-                const float dft = q == 0 ? S.dft[0] : (q == 1 ? S.dft[1] : S.dft[2]);
-                const float ra = A.r[a];
-                const float gx = ra != 0.0f ? -A.rn * df / ra : 0.0f;
-                const float gr = (ra != 0.0f ? -A.rn * dft / ra : 0.0f) + p * ra / rn2;
-                const float dsrc = P.beam == 1 ? gx - gr : gr;
-                const float dpix = P.beam == 1 ? gr : gx;
-                g[a] = wr * dsrc;
-                g[3 + a] = wr * dpix;
-                g[6 + a] = wr * alpha * dpix;
-                g[9 + a] = wr * beta * dpix;
+                g[a] = wr * dsrc[a];
+                g[3 + a] = wr * dpix[a];
+                g[6 + a] = wr * gu[a];
+                g[9 + a] = wr * gv[a];
             }
         }
     }
@@ -454,6 +535,65 @@ inline int column_geometry_vjp(const RayParams &P, const GeomParams &Q, const Co
         return 9;
     if (P.view_count <= 0) return 0;
     column_gvjp_kernel<2><<<column_grid(P, 2), 256, 0, s>>>(P, Q, T, zvol, w, out);
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+// Surface gradient: one thread per pixel walks that pixel's ray in every view
+// and sums w * dp/d pixel projected on the view's u, v and unit normal (the
+// gradients with respect to the pixel's offsets t, s, e); out (n_v, n_u, 3)
+// float64 -- (n_views, n_v, n_u, 3) with one offset table per view --
+// overwritten; each pixel's sums are its thread's, no atomics.
+template <int TU, int TV>
+__global__ void __launch_bounds__(TU *TV) surface_vjp_kernel(RayParams P, GeomParams Q,
+                                                             const float *__restrict__ vol,
+                                                             const float *__restrict__ w,
+                                                             double *__restrict__ out)
+{
+    const int iu = blockIdx.x * TU + (int)(threadIdx.x % TU);
+    const int iv = blockIdx.y * TV + (int)(threadIdx.x / TU);
+    if (iu >= P.n_u || iv >= P.n_v) return;
+    // one offset table per view: every view's pixel has its own sums (out is
+    // (n_views, n_v, n_u, 3)); else the sums run over the views
+    const bool per_view = P.offsets && P.offsets_per_view;
+    const long long nout = 3LL * P.n_u * P.n_v * (per_view ? P.n_views : 1);
+    double acc[3] = {0.0, 0.0, 0.0};
+    for (int view = 0; view < P.n_views; ++view) {
+        const long long ray = ((long long)view * P.n_v + iv) * P.n_u + iu;
+        if (per_view) acc[0] = acc[1] = acc[2] = 0.0;
+        const float wr = (true CTP_AND_IN(ray, sino_cells(P), kSiteGeomSinoLoad)) ? w[ray] : 0.0f;
+        float dsrc[3], dpix[3];
+        if (wr != 0.0f && ray_gradient(P, view, iu, iv, vol, dsrc, dpix)) {
+            double u[3], v[3], n[3], cn;
+            detector_axes(P, Q, view, u, v, n, cn);
+            double gu = 0.0, gv = 0.0, gn = 0.0;
+#pragma unroll
+            for (int a = 0; a < 3; ++a) {
+                gu = __fma_rn((double)dpix[a], u[a], gu);
+                gv = __fma_rn((double)dpix[a], v[a], gv);
+                gn = __fma_rn((double)dpix[a], n[a], gn);
+            }
+            acc[0] = __fma_rn((double)wr, gu, acc[0]);
+            acc[1] = __fma_rn((double)wr, gv, acc[1]);
+            acc[2] = __fma_rn((double)wr, gn, acc[2]);
+        }
+        if (per_view) {
+#pragma unroll
+            for (int m = 0; m < 3; ++m)
+                if (true CTP_AND_IN(3 * ray + m, nout, kSiteGeomOut)) out[3 * ray + m] = acc[m];
+        }
+    }
+    if (per_view) return;
+    const long long o = 3 * ((long long)iv * P.n_u + iu);
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+        if (true CTP_AND_IN(o + m, nout, kSiteGeomOut)) out[o + m] = acc[m];
+}
+
+inline int surface_vjp(const RayParams &P, const GeomParams &Q, const float *vol, const float *w,
+                       double *out, cudaStream_t s)
+{
+    dim3 grid((P.n_u + 31) / 32, (P.n_v + 3) / 4, 1);
+    surface_vjp_kernel<32, 4><<<grid, 128, 0, s>>>(P, Q, vol, w, out);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 

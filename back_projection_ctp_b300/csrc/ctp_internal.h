@@ -36,8 +36,10 @@ struct RayParams {
     float min_len;        // segment counter: pieces longer than this (physical units)
     int view0;            // first view of a launch (grid row y handles view view0 + y)
     int view_count;       // views of a launch
-    const float *offsets; // curved detector: (n_v, n_u, 3) per-pixel offsets; else null
-    const ColumnOffsets *columns;  // curved detector on the column path: per column; else null
+    const float *offsets; // curved detector: per-pixel offsets (t, s, e); else null
+    int offsets_per_view; // 0: offsets (n_v, n_u, 3) shared; 1: (n_views, n_v, n_u, 3)
+    const ColumnOffsets *columns;  // curved detector on the column path: per column
+                                   // (per view and column with per-view tables); else null
 };
 
 // Bounds-checked debug build (compiled with -DCTP_CHECK): the projector walks
@@ -76,6 +78,14 @@ __device__ __forceinline__ bool ctp_in(long long i, long long n, int site)
 #else
 __device__ __forceinline__ constexpr bool ctp_in(long long, long long, int) { return true; }
 #endif
+
+// The (t, s, e) offsets of pixel (iu, iv) of view `view` (curved detectors).
+__host__ __device__ __forceinline__ const float *pixel_offsets_of(const RayParams &P, int view,
+                                                                 int iu, int iv)
+{
+    const long long pix = (long long)iv * P.n_u + iu;
+    return P.offsets + 3 * (P.offsets_per_view ? (long long)view * P.n_u * P.n_v + pix : pix);
+}
 
 // Elements of the sinogram buffer (n_views, n_v, n_u).
 __host__ __device__ __forceinline__ long long sino_cells(const RayParams &P)

@@ -239,13 +239,12 @@ __device__ __forceinline__ void plane_walk_lockstep(const PlaneRay &R, int ka, i
     uint32_t fb = (uint32_t)F;
     int jb = R.jb + carries;
     int addr = R.addr + (int)n * R.sp + carries * R.sb;
+    // every slab clamps to [lo, hi] (the ray's own ends, else [0, 1]): one code
+    // path for the whole warp, no branch on the first / last slab
     for (int k = ka; k <= kb; ++k) {
         if (k < la || k > lb) continue;
-        if (k == R.k0 || k == R.k1)
-            plane_slab<true>(fb, R.bb, R.ib, jb, addr, R.sp, R.sb, k == R.k0 ? R.tlo : 0.0f,
-                             k == R.k1 ? R.thi : 1.0f, op);
-        else
-            plane_slab<false>(fb, R.bb, R.ib, jb, addr, R.sp, R.sb, 0.0f, 1.0f, op);
+        plane_slab<true>(fb, R.bb, R.ib, jb, addr, R.sp, R.sb, k == R.k0 ? R.tlo : 0.0f,
+                         k == R.k1 ? R.thi : 1.0f, op);
     }
 }
 
@@ -278,13 +277,15 @@ struct PlaneGather {
     }
 };
 
+// A piece of zero length adds 0 (no test: the first piece of a slab is all
+// but never empty, the second goes out only after a crossing).
 struct PlaneScatter {
     float *__restrict__ img;
     float w;
     long long lim;
     __device__ __forceinline__ void operator()(int a, float d, bool on, int)
     {
-        if (on && d > 0.0f && ctp_in(a, lim, kSitePlaneScatter)) atomicAdd(img + a, __fmul_rn(d, w));
+        if (on && ctp_in(a, lim, kSitePlaneScatter)) atomicAdd(img + a, __fmul_rn(d, w));
     }
 };
 

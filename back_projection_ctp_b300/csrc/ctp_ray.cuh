@@ -60,7 +60,7 @@ __device__ __forceinline__ bool slab_setup(const RayParams &P, int view, int iu,
     double fu = (double)iu, fv = (double)iv, fe = 0.0;
     if (P.offsets) {
         // curved detector: the pixel's (t, s, e) offsets along du, dv, dn
-        const float *q = P.offsets + 3 * ((long long)iv * P.n_u + iu);
+        const float *q = pixel_offsets_of(P, view, iu, iv);
         fu = (double)q[0];
         fv = (double)q[1];
         fe = (double)q[2];

@@ -101,6 +101,8 @@ def l2_peaks(dev, stream, repeats=5):
     lib.ctp_probe_l2_load.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int,
                                       ctypes.c_void_p, ctypes.c_void_p]
     lib.ctp_probe_sm_count.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.ctp_probe_smem_accumulate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p]
     sms = ctypes.c_int(0)
     if lib.ctp_probe_sm_count(ctypes.byref(sms)) != 0:
         raise RuntimeError("ctp_probe_sm_count failed")
@@ -134,10 +136,18 @@ def l2_peaks(dev, stream, repeats=5):
                    1.0 * threads * it_load)
     load = best(lambda: check(lib.ctp_probe_l2_load(buf.data_ptr(), n, it_load, sink.data_ptr(),
                                                     sp)), 16.0 * threads * it_load)
+    # shared-memory float accumulation (adds per clock per SM at the maximum clock)
+    smem = {}
+    for mode, name in ((0, "atomic_distinct_words"), (1, "load_add_store"),
+                       (2, "atomic_4_lanes_per_word")):
+        rate = best(lambda: check(lib.ctp_probe_smem_accumulate(it_load, mode, sink.data_ptr(),
+                                                                sp)), 1.0 * threads * it_load)
+        smem[name] = rate / sms.value / 2.032e9
     return {"reduction_gbs": red / 1e9, "reduction_sectors_per_s": sectors,
-            "load_gbs": load / 1e9,
+            "load_gbs": load / 1e9, "smem_adds_per_clock_per_sm": smem,
             "how": "libctp_probe.so: 8 blocks x 256 threads per SM over a 64 MiB buffer held "
-                   "in L2; best of 5 launches timed with CUDA events"}
+                   "in L2 (shared memory: 256 words per block); best of 5 launches timed "
+                   "with CUDA events"}
 
 
 def stored_traffic(kernel: str, workload: str):

@@ -104,10 +104,17 @@ typedef struct ctp_geometry {
                                  (t and e the same in every row, s affine in the row
                                  to 1e-6 of the column's span: cylindrical detectors)
                                  may take the column path; others take the ray path;
-                                 the plane path is refused.  ctp_forward_static, the
-                                 analytical operators and ctp_geometry_vjp refuse
-                                 curved detectors (CTP_E_OPTION / CTP_E_GEOMETRY).
+                                 the plane path is refused.  ctp_forward_static and
+                                 the analytical operators refuse curved detectors
+                                 (CTP_E_OPTION / CTP_E_GEOMETRY); ctp_geometry_vjp
+                                 and ctp_surface_vjp take them.
                                  Offsets must be finite (CTP_E_NONFINITE). */
+    int offsets_per_view;     /* 0: pixel_offsets is one (n_v, n_u, 3) table shared by
+                                 all views; 1: one table per view, (n_views, n_v, n_u,
+                                 3) (the pages sample surfaces in view and pixel
+                                 batches: each view may see its own surface).  With
+                                 per-view tables the column path needs every view's
+                                 columns straight.  Other values: CTP_E_OPTION. */
 } ctp_geometry;
 
 typedef struct ctp_volume {
@@ -360,20 +367,48 @@ int ctp_parker_weights(const ctp_plan_t *plan, float *weight_dev, void *stream);
  * plane x_a = const at t_k (value outside the grid 0; the ray's own end points
  * are not crossings) contributes -(f_before - f_after) |r| (dX0_a + t_k dr_a) / r_a,
  * and the length scale contributes p r.dr / |r|^2; pixel = centre + alpha u +
- * beta v.  The gradient of the backprojection <A^T y, h> with respect to the
- * geometry is the same call with vol = h and w = y.  Rays through a cell edge
- * or corner are kinks of p; the jump goes to one of the coincident crossings.
+ * beta v (flat detectors: the pitch grid), or centre + t u + s v + e n with n =
+ * u x v / |u x v| (curved detectors: the pixel's offsets), whose u and v
+ * gradients also carry the normal's derivative: with g = dp/d pixel and h =
+ * (g - (n.g) n) / |u x v|, dp/du = t g + e v x h and dp/dv = s g - e u x h.
+ * The gradient of the backprojection <A^T y, h> with respect to the geometry is
+ * the same call with vol = h and w = y.  Rays through a cell edge or corner are
+ * kinks of p; the jump goes to one of the coincident crossings.
  * vol_dev: device float32 (nz, ny, nx).  weight_dev: device float32
  * (n_views, n_v, n_u).  grad_dev: device float64 (n_views, 12), overwritten.
- * Column-path plans run the sums over the column walk on the plan's working
- * copy of vol_dev (ordered with the plan's other calls, as ctp_forward); other
- * plans run the ray path's walk (the plan option geometry_walk = 1 selects it
- * for column plans too).  Asynchronous on `stream`.  Errors:
- * CTP_E_NULL, CTP_E_DEVICE, CTP_E_OPTION (curved detectors: the chain rule
- * above assumes the pitch grid), CTP_E_CUDA.
+ * Column-path plans of flat detectors run the sums over the column walk on the
+ * plan's working copy of vol_dev (ordered with the plan's other calls, as
+ * ctp_forward); other plans run the ray path's walk (the plan option
+ * geometry_walk = 1 selects it for column plans too).  Asynchronous on
+ * `stream`.  Errors: CTP_E_NULL, CTP_E_DEVICE, CTP_E_CUDA.
  */
 int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *weight_dev,
                      double *grad_dev, void *stream);
+
+/*
+ * ctp_surface_vjp -- first-order gradients with respect to the detector
+ * surface: every pixel's offsets (t, s, e) along det_u, det_v and the unit
+ * normal n = det_u x det_v / |det_u x det_v|, shared by all views (the pages'
+ * curved detectors: "Projection and matched backprojection support first-order
+ * surface gradients", diffct release diff 2.1.0 -> 2.2.1, README "Curved
+ * detectors"; the point centre + tangent u + vertical v + depth n, release diff
+ * 2.4.1 -> 2.4.2, kernels/surface_geometry.py compose_surface):
+ *
+ *     grad[iv][iu][m] = sum over views s of w[s][iv][iu] * (dp/d pixel) . (u_s, v_s, n_s)[m]
+ *
+ * with dp/d pixel the end-point derivative of ctp_geometry_vjp.  Flat detectors
+ * are included: their offsets are the pitch grid (e = 0), and the result is the
+ * gradient with respect to moving each pixel along the view's axes.
+ * With one offset table per view (offsets_per_view = 1) every view's pixel has
+ * its own gradient: grad_dev is (n_views, n_v, n_u, 3), no sum over views.
+ * vol_dev: device float32 (nz, ny, nx); weight_dev: device float32 (n_views,
+ * n_v, n_u); grad_dev: device float64 (n_v, n_u, 3), overwritten (every
+ * pixel's sums are one thread's: deterministic, no atomics).  Runs the
+ * ray path's walk on vol_dev on any plan.  Asynchronous on `stream`.  Errors:
+ * CTP_E_NULL, CTP_E_DEVICE, CTP_E_CUDA.
+ */
+int ctp_surface_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *weight_dev,
+                    double *grad_dev, void *stream);
 
 /*
  * ctp_check_violations -- the bounds-checked debug build (the library compiled

@@ -23,8 +23,12 @@ Functions and what pins them (the tests under ``tests/test_oracle_*.py``):
   (the benchmark's unit); pinned by :func:`brute_count`.
 * :func:`ambiguous` -- rays lying on a cell-face plane; pinned on hand-built rays.
 * :func:`geometry_vjp` -- first-order gradients of the path sums with respect to
-  the per-view frames; pinned by central finite differences of :func:`forward`
-  and by the invariance of chords under sliding a ray's end points along it.
+  the per-view frames (flat and curved detectors); pinned by central finite
+  differences of :func:`forward` and by the invariance of chords under sliding a
+  ray's end points along it.
+* :func:`surface_vjp` -- first-order gradients with respect to every pixel's
+  offsets along the detector axes and normal; pinned by central finite
+  differences of :func:`forward` in the offsets.
 * :func:`kinks` -- rays through a cell edge or corner (no geometry derivative);
   pinned on hand-built rays.
 """
@@ -71,7 +75,7 @@ class _Ctx(ctypes.Structure):
         ("offset_u", ctypes.c_double), ("offset_v", ctypes.c_double),
         ("n", ctypes.c_int * 3), ("pad_", ctypes.c_int),
         ("d", ctypes.c_double * 3), ("o", ctypes.c_double * 3),
-        ("offsets", ctypes.c_void_p),
+        ("offsets", ctypes.c_void_p), ("offsets_per_view", ctypes.c_int), ("pad2_", ctypes.c_int),
     ]
 
 
@@ -94,6 +98,7 @@ def _load():
                 "ora_supersampled": [C, P, P, L, L, P, I],
                 "ora_trace_ray": [C, L, P, P],
                 "ora_geometry_vjp": [C, P, P, P, I],
+                "ora_surface_vjp": [C, P, P, P, I],
                 "ora_kinks": [C, D, P, I],
             }
             for name, args in sigs.items():
@@ -133,12 +138,18 @@ class Scan:
         c.n[0], c.n[1], c.n[2] = W, H, D
         c.d[0], c.d[1], c.d[2] = dx, dy, dz
         c.o[0], c.o[1], c.o[2] = self.origin
-        # curved detector: per-pixel (tangent, vertical, depth) offsets (n_v, n_u, 3)
+        # curved detector: per-pixel (tangent, vertical, depth) offsets, (n_v, n_u, 3)
+        # shared by all views or (n_views, n_v, n_u, 3) one table per view
         self.pixel_offsets = None
+        self.offsets_per_view = False
         if pixel_offsets is not None:
-            self.pixel_offsets = np.ascontiguousarray(pixel_offsets, dtype=np.float32).reshape(
-                self.n_v, self.n_u, 3)
+            off = np.ascontiguousarray(pixel_offsets, dtype=np.float32)
+            self.offsets_per_view = off.size == 3 * self.n_views * self.n_u * self.n_v and \
+                off.ndim == 4
+            shape = ((self.n_views,) if self.offsets_per_view else ()) + (self.n_v, self.n_u, 3)
+            self.pixel_offsets = off.reshape(shape)
             c.offsets = self.pixel_offsets.ctypes.data
+            c.offsets_per_view = int(self.offsets_per_view)
         self._ctx = c
 
     @classmethod
@@ -289,6 +300,21 @@ def geometry_vjp(scan: Scan, vol, weights, threads=0):
     out = np.zeros((scan.n_views, 4, 3), dtype=np.float64)
     _check(_load().ora_geometry_vjp(scan.ref(), vol.ctypes.data, w.ctypes.data,
                                     out.ctypes.data, threads), "ora_geometry_vjp")
+    return out
+
+
+def surface_vjp(scan: Scan, vol, weights, threads=0):
+    """Float64 first-order gradient with respect to the detector surface: (n_v,
+    n_u, 3) array of sum over views of weights[ray] * d p(ray) / d (t, s, e),
+    the pixel's offsets along det_u, det_v and the unit normal det_u x det_v
+    (a curved detector's own offsets, or the pitch grid of a flat one); with one
+    offset table per view, (n_views, n_v, n_u, 3) without the sum over views."""
+    vol = _f32(vol, scan.shape)
+    w = _f32(weights, (scan.n_rays,))
+    shape = ((scan.n_views,) if scan.offsets_per_view else ()) + (scan.n_v, scan.n_u, 3)
+    out = np.zeros(shape, dtype=np.float64)
+    _check(_load().ora_surface_vjp(scan.ref(), vol.ctypes.data, w.ctypes.data,
+                                   out.ctypes.data, threads), "ora_surface_vjp")
     return out
 
 

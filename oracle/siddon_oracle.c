@@ -52,7 +52,9 @@ typedef struct {
     int pad_;
     double d[3];         /* spacing along x, y, z */
     double o[3];         /* world position of the min corner of cell (0, 0, 0) */
-    const float *offsets;  /* NULL (flat detector) or (n_v, n_u, 3) per-pixel offsets */
+    const float *offsets;  /* NULL (flat detector) or per-pixel offsets (t, s, e): */
+    int offsets_per_view;  /* 0: (n_v, n_u, 3) shared by all views; 1: (n_views, n_v, n_u, 3) */
+    int pad2_;
 } ora_ctx;
 
 static int ora_threads(int requested)
@@ -68,10 +70,11 @@ static int ora_threads(int requested)
 
 /* The ray of detector sample `ray` (view-major, then v, then u).  Flat
  * detector: pixel = centre + a u + b v with a, b the pitch grid.  Curved
- * (per-pixel offsets (t, s, e), shared by all views; the pages' surface
- * composition, diffct 2.4.1 -> 2.4.2, kernels/surface_geometry.py
- * `compose_surface`: point = centre + tangent u + vertical v + depth n):
- * pixel = centre + t u + s v + e n, n = (u x v) / |u x v|. */
+ * (per-pixel offsets (t, s, e), shared by all views or one table per view; the
+ * pages' surface composition, diffct 2.4.1 -> 2.4.2, kernels/surface_geometry.py
+ * `compose_surface`: point = centre + tangent u + vertical v + depth n, with
+ * view and pixel batches of offsets): pixel = centre + t u + s v + e n,
+ * n = (u x v) / |u x v|. */
 static void ora_ray(const ora_ctx *c, long ray, double X0[3], double r[3],
                     double *tlo, double *thi)
 {
@@ -83,7 +86,7 @@ static void ora_ray(const ora_ctx *c, long ray, double X0[3], double r[3],
     const float *U = c->det_u + 3 * view, *V = c->det_v + 3 * view;
     double P[3];
     if (c->offsets) {
-        const float *q = c->offsets + 3 * pix;
+        const float *q = c->offsets + 3 * (c->offsets_per_view ? ray : pix);
         double u[3] = {U[0], U[1], U[2]}, v[3] = {V[0], V[1], V[2]};
         double n[3] = {u[1] * v[2] - u[2] * v[1], u[2] * v[0] - u[0] * v[2],
                        u[0] * v[1] - u[1] * v[0]};
@@ -654,18 +657,185 @@ int ora_trace_ray(const ora_ctx *c, long ray, long *cells, double *lens)
  * dt_k = -(dX0_a + t_k dr_a) / r_a, so
  *     dp/dX0_a = -|r| sum_{k on axis a} (f_before - f_after)_k / r_a,
  *     dp/dr_a  = -|r| sum_{k on axis a} (f_before - f_after)_k t_k / r_a + p r_a / |r|^2,
- * with the value outside the volume 0 at the box faces.  The chain rule to the
- * frame: pixel = centre + alpha u + beta v (alpha, beta the pixel offsets times
- * the pitches); divergent: source = X0, pixel = X0 + r; parallel: pixel = X0,
- * src = r.  Configurations where two crossings coincide (a ray through a cell
- * edge or corner) are kinks of p and have no gradient; whatever the merge
- * order gives there is accepted.  Views run in parallel (each view's sums are
- * owned by one thread).
+ * with the value outside the volume 0 at the box faces.
+ */
+/* Gradient of one ray's path sum with respect to the ray's start X0 and its
+ * direction r (the crossing sums above, written out for ray `ray`): dsrc and
+ * dpix are dp/d source and dp/d pixel (divergent: X0 = source, r = pixel -
+ * source; parallel: X0 = pixel, r = src, so dsrc is dp/d src).  Returns 0 when
+ * the ray misses the grid (both zero).  buf: ora_buf_len(c) doubles. */
+static int ora_ray_gradient(const ora_ctx *c, const float *vol, long ray, double *buf,
+                            double dsrc[3], double dpix[3])
+{
+    for (int ax = 0; ax < 3; ++ax) dsrc[ax] = dpix[ax] = 0.0;
+    double X0[3], r[3], tlo, thi;
+    ora_ray(c, ray, X0, r, &tlo, &thi);
+    /* clip to the grid, remembering which face plane bounds it */
+    double amin = tlo, amax = thi;
+    int ain = -1, aout = -1, empty = 0;
+    for (int ax = 0; ax < 3; ++ax) {
+        double p0 = c->o[ax], p1 = c->o[ax] + (double)c->n[ax] * c->d[ax];
+        if (r[ax] == 0.0) {
+            if (!(X0[ax] >= p0 && X0[ax] < p1)) empty = 1;
+            continue;
+        }
+        double t0 = (p0 - X0[ax]) / r[ax], t1 = (p1 - X0[ax]) / r[ax];
+        double e0 = fmin(t0, t1), e1 = fmax(t0, t1);
+        if (e0 > amin) { amin = e0; ain = ax; }
+        if (e1 < amax) { amax = e1; aout = ax; }
+    }
+    if (empty || !(amin < amax)) return 0;
+    /* interior crossings per axis, merged in increasing t */
+    double *seq[3];
+    int len[3], pos[3];
+    double *next = buf;
+    for (int ax = 0; ax < 3; ++ax) {
+        seq[ax] = next;
+        len[ax] = 0;
+        pos[ax] = 0;
+        if (r[ax] == 0.0) continue;
+        for (int m = 0; m <= c->n[ax]; ++m) {
+            int k = r[ax] > 0.0 ? m : c->n[ax] - m;
+            double t = (c->o[ax] + (double)k * c->d[ax] - X0[ax]) / r[ax];
+            if (t > amin && t < amax) seq[ax][len[ax]++] = t;
+        }
+        next += len[ax];
+    }
+    double norm = ora_norm(r);
+    double sum_df[3] = {0, 0, 0}, sum_dft[3] = {0, 0, 0};
+    double p = 0.0, prev = amin, f_prev = 0.0;
+    int first = 1;
+    for (;;) {
+        double t = amax;
+        int which = -1;
+        for (int ax = 0; ax < 3; ++ax)
+            if (pos[ax] < len[ax] && seq[ax][pos[ax]] < t) {
+                t = seq[ax][pos[ax]];
+                which = ax;
+            }
+        /* the piece [prev, t) and its value (midpoint cell) */
+        double mid = 0.5 * (prev + t), f = 0.0;
+        if (t > prev) {
+            long idx[3];
+            for (int ax = 0; ax < 3; ++ax) {
+                long q = (long)floor((X0[ax] + mid * r[ax] - c->o[ax]) / c->d[ax]);
+                if (q < 0) q = 0;
+                if (q > c->n[ax] - 1) q = c->n[ax] - 1;
+                idx[ax] = q;
+            }
+            f = (double)vol[(idx[2] * c->n[1] + idx[1]) * c->n[0] + idx[0]];
+            p += (t - prev) * f;
+        } else {
+            f = f_prev;  /* zero-length piece: no value change */
+        }
+        if (first) {
+            /* entry through a face plane: outside value 0 */
+            if (ain >= 0) {
+                sum_df[ain] += 0.0 - f;
+                sum_dft[ain] += (0.0 - f) * amin;
+            }
+            first = 0;
+        }
+        f_prev = f;
+        if (which < 0) break;
+        /* crossing of axis `which` at t: value before f, after = next piece */
+        double t_next = amax;
+        for (int ax = 0; ax < 3; ++ax) {
+            int pp = pos[ax] + (ax == which ? 1 : 0);
+            if (pp < len[ax] && seq[ax][pp] < t_next) t_next = seq[ax][pp];
+        }
+        double f_after = f;
+        if (t_next > t) {
+            double m2 = 0.5 * (t + t_next);
+            long idx[3];
+            for (int ax = 0; ax < 3; ++ax) {
+                long q = (long)floor((X0[ax] + m2 * r[ax] - c->o[ax]) / c->d[ax]);
+                if (q < 0) q = 0;
+                if (q > c->n[ax] - 1) q = c->n[ax] - 1;
+                idx[ax] = q;
+            }
+            f_after = (double)vol[(idx[2] * c->n[1] + idx[1]) * c->n[0] + idx[0]];
+        }
+        sum_df[which] += f - f_after;
+        sum_dft[which] += (f - f_after) * t;
+        pos[which]++;
+        prev = t;
+    }
+    /* exit through a face plane: outside value 0 */
+    if (aout >= 0) {
+        sum_df[aout] += f_prev - 0.0;
+        sum_dft[aout] += (f_prev - 0.0) * amax;
+    }
+    p *= norm;
+    for (int ax = 0; ax < 3; ++ax) {
+        double gx = r[ax] != 0.0 ? -norm * sum_df[ax] / r[ax] : 0.0;
+        double gr = (r[ax] != 0.0 ? -norm * sum_dft[ax] / r[ax] : 0.0) +
+                    p * r[ax] / (norm * norm);
+        if (c->beam == 1) {
+            dsrc[ax] = gx - gr;
+            dpix[ax] = gr;
+        } else {
+            dsrc[ax] = gr;
+            dpix[ax] = gx;
+        }
+    }
+    return 1;
+}
+
+static void ora_cross(const double a[3], const double b[3], double out[3])
+{
+    out[0] = a[1] * b[2] - a[2] * b[1];
+    out[1] = a[2] * b[0] - a[0] * b[2];
+    out[2] = a[0] * b[1] - a[1] * b[0];
+}
+
+/* The detector frame of view `view` in float64: u, v, the unit normal
+ * n = (u x v) / |u x v| and |u x v|. */
+static void ora_frame_axes(const ora_ctx *c, long view, double u[3], double v[3], double n[3],
+                           double *cn)
+{
+    const float *U = c->det_u + 3 * view, *V = c->det_v + 3 * view;
+    for (int ax = 0; ax < 3; ++ax) {
+        u[ax] = (double)U[ax];
+        v[ax] = (double)V[ax];
+    }
+    ora_cross(u, v, n);
+    *cn = ora_norm(n);
+    for (int ax = 0; ax < 3; ++ax) n[ax] /= *cn;
+}
+
+/* Offsets (t, s, e) along u, v and n of the pixel of detector sample `ray`: a
+ * curved detector's own table (shared, or the ray's view's), or the pitch grid
+ * of a flat one (e = 0). */
+static void ora_pixel_offsets(const ora_ctx *c, long ray, double q[3])
+{
+    long pix = ray % ((long)c->n_u * c->n_v);
+    if (c->offsets) {
+        long at = c->offsets_per_view ? ray : pix;
+        for (int m = 0; m < 3; ++m) q[m] = (double)c->offsets[3 * at + m];
+    } else {
+        long iv = pix / c->n_u, iu = pix % c->n_u;
+        q[0] = ((double)iu - 0.5 * (double)(c->n_u - 1) + c->offset_u) * c->pitch_u;
+        q[1] = ((double)iv - 0.5 * (double)(c->n_v - 1) + c->offset_v) * c->pitch_v;
+        q[2] = 0.0;
+    }
+}
+
+/*
+ * The chain rule to the frame: pixel = centre + t u + s v + e n, n = (u x v) /
+ * |u x v| ((t, s, e) the pitch grid with e = 0 for flat detectors, a curved
+ * detector's per-pixel offsets otherwise); divergent: source = X0, pixel = X0 +
+ * r; parallel: pixel = X0, src = r.  With g = dp/d pixel, the normal's
+ * derivative gives d(e n)/du^T g = e v x h and d(e n)/dv^T g = -e u x h, h =
+ * (g - (n.g) n) / |u x v| (dn = (I - n n^T) d(u x v) / |u x v|).
+ * Configurations where two crossings coincide (a ray through a cell edge or
+ * corner) are kinks of p and have no gradient; whatever the merge order gives
+ * there is accepted.  Views run in parallel (each view's sums are owned by one
+ * thread).
  */
 int ora_geometry_vjp(const ora_ctx *c, const float *vol, const float *w, double *out,
                      int nthreads)
 {
-    if (c->offsets) return 2;  /* flat detectors only */
     int T = ora_threads(nthreads);
     int B = ora_buf_len(c);
     long per_view = (long)c->n_u * c->n_v;
@@ -680,136 +850,85 @@ int ora_geometry_vjp(const ora_ctx *c, const float *vol, const float *w, double 
 #pragma omp for schedule(dynamic, 1)
             for (int view = 0; view < c->n_views; ++view) {
                 double g[12] = {0};
+                double u[3], v[3], n[3], cn;
+                ora_frame_axes(c, view, u, v, n, &cn);
                 for (long pix = 0; pix < per_view; ++pix) {
                     long ray = view * per_view + pix;
                     double wr = (double)w[ray];
                     if (wr == 0.0) continue;
-                    double X0[3], r[3], tlo, thi;
-                    ora_ray(c, ray, X0, r, &tlo, &thi);
-                    /* clip to the grid, remembering which face plane bounds it */
-                    double amin = tlo, amax = thi;
-                    int ain = -1, aout = -1, empty = 0;
+                    double dsrc[3], dpix[3], q[3];
+                    if (!ora_ray_gradient(c, vol, ray, buf, dsrc, dpix)) continue;
+                    ora_pixel_offsets(c, ray, q);
+                    double h[3], vh[3], uh[3];
+                    double ng = n[0] * dpix[0] + n[1] * dpix[1] + n[2] * dpix[2];
+                    for (int ax = 0; ax < 3; ++ax) h[ax] = (dpix[ax] - ng * n[ax]) / cn;
+                    ora_cross(v, h, vh);
+                    ora_cross(u, h, uh);
                     for (int ax = 0; ax < 3; ++ax) {
-                        double p0 = c->o[ax], p1 = c->o[ax] + (double)c->n[ax] * c->d[ax];
-                        if (r[ax] == 0.0) {
-                            if (!(X0[ax] >= p0 && X0[ax] < p1)) empty = 1;
-                            continue;
-                        }
-                        double t0 = (p0 - X0[ax]) / r[ax], t1 = (p1 - X0[ax]) / r[ax];
-                        double e0 = fmin(t0, t1), e1 = fmax(t0, t1);
-                        if (e0 > amin) { amin = e0; ain = ax; }
-                        if (e1 < amax) { amax = e1; aout = ax; }
-                    }
-                    if (empty || !(amin < amax)) continue;
-                    /* interior crossings per axis, merged in increasing t */
-                    double *seq[3];
-                    int len[3], pos[3];
-                    double *next = buf;
-                    for (int ax = 0; ax < 3; ++ax) {
-                        seq[ax] = next;
-                        len[ax] = 0;
-                        pos[ax] = 0;
-                        if (r[ax] == 0.0) continue;
-                        for (int m = 0; m <= c->n[ax]; ++m) {
-                            int k = r[ax] > 0.0 ? m : c->n[ax] - m;
-                            double t = (c->o[ax] + (double)k * c->d[ax] - X0[ax]) / r[ax];
-                            if (t > amin && t < amax) seq[ax][len[ax]++] = t;
-                        }
-                        next += len[ax];
-                    }
-                    double norm = ora_norm(r);
-                    double sum_df[3] = {0, 0, 0}, sum_dft[3] = {0, 0, 0};
-                    double p = 0.0, prev = amin, f_prev = 0.0;
-                    int first = 1;
-                    for (;;) {
-                        double t = amax;
-                        int which = -1;
-                        for (int ax = 0; ax < 3; ++ax)
-                            if (pos[ax] < len[ax] && seq[ax][pos[ax]] < t) {
-                                t = seq[ax][pos[ax]];
-                                which = ax;
-                            }
-                        /* the piece [prev, t) and its value (midpoint cell) */
-                        double mid = 0.5 * (prev + t), f = 0.0;
-                        if (t > prev) {
-                            long idx[3];
-                            for (int ax = 0; ax < 3; ++ax) {
-                                long q = (long)floor((X0[ax] + mid * r[ax] - c->o[ax]) / c->d[ax]);
-                                if (q < 0) q = 0;
-                                if (q > c->n[ax] - 1) q = c->n[ax] - 1;
-                                idx[ax] = q;
-                            }
-                            f = (double)vol[(idx[2] * c->n[1] + idx[1]) * c->n[0] + idx[0]];
-                            p += (t - prev) * f;
-                        } else {
-                            f = f_prev;  /* zero-length piece: no value change */
-                        }
-                        if (first) {
-                            /* entry through a face plane: outside value 0 */
-                            if (ain >= 0) {
-                                sum_df[ain] += 0.0 - f;
-                                sum_dft[ain] += (0.0 - f) * amin;
-                            }
-                            first = 0;
-                        } else {
-                            /* the crossing at prev, recorded when it was consumed */
-                        }
-                        f_prev = f;
-                        if (which < 0) break;
-                        /* crossing of axis `which` at t: value before f, after = next piece */
-                        double t_next = amax;
-                        for (int ax = 0; ax < 3; ++ax) {
-                            int pp = pos[ax] + (ax == which ? 1 : 0);
-                            if (pp < len[ax] && seq[ax][pp] < t_next) t_next = seq[ax][pp];
-                        }
-                        double f_after = f;
-                        if (t_next > t) {
-                            double m2 = 0.5 * (t + t_next);
-                            long idx[3];
-                            for (int ax = 0; ax < 3; ++ax) {
-                                long q = (long)floor((X0[ax] + m2 * r[ax] - c->o[ax]) / c->d[ax]);
-                                if (q < 0) q = 0;
-                                if (q > c->n[ax] - 1) q = c->n[ax] - 1;
-                                idx[ax] = q;
-                            }
-                            f_after = (double)vol[(idx[2] * c->n[1] + idx[1]) * c->n[0] + idx[0]];
-                        }
-                        sum_df[which] += f - f_after;
-                        sum_dft[which] += (f - f_after) * t;
-                        pos[which]++;
-                        prev = t;
-                    }
-                    /* exit through a face plane: outside value 0 */
-                    if (aout >= 0) {
-                        sum_df[aout] += f_prev - 0.0;
-                        sum_dft[aout] += (f_prev - 0.0) * amax;
-                    }
-                    p *= norm;
-                    double gx[3], gr[3];
-                    for (int ax = 0; ax < 3; ++ax) {
-                        gx[ax] = r[ax] != 0.0 ? -norm * sum_df[ax] / r[ax] : 0.0;
-                        gr[ax] = (r[ax] != 0.0 ? -norm * sum_dft[ax] / r[ax] : 0.0) +
-                                 p * r[ax] / (norm * norm);
-                    }
-                    long iv = pix / c->n_u, iu = pix % c->n_u;
-                    double alpha = ((double)iu - 0.5 * (double)(c->n_u - 1) + c->offset_u) * c->pitch_u;
-                    double beta = ((double)iv - 0.5 * (double)(c->n_v - 1) + c->offset_v) * c->pitch_v;
-                    for (int ax = 0; ax < 3; ++ax) {
-                        double dsrc, dpix;
-                        if (c->beam == 1) {
-                            dsrc = gx[ax] - gr[ax];
-                            dpix = gr[ax];
-                        } else {
-                            dsrc = gr[ax];
-                            dpix = gx[ax];
-                        }
-                        g[ax] += wr * dsrc;
-                        g[3 + ax] += wr * dpix;
-                        g[6 + ax] += wr * alpha * dpix;
-                        g[9 + ax] += wr * beta * dpix;
+                        g[ax] += wr * dsrc[ax];
+                        g[3 + ax] += wr * dpix[ax];
+                        g[6 + ax] += wr * (q[0] * dpix[ax] + q[2] * vh[ax]);
+                        g[9 + ax] += wr * (q[1] * dpix[ax] - q[2] * uh[ax]);
                     }
                 }
                 for (int m = 0; m < 12; ++m) out[12 * view + m] = g[m];
+            }
+        }
+        free(buf);
+    }
+    return err;
+}
+
+/*
+ * Surface-offset vector-Jacobian product: first-order gradients of the path
+ * sums with respect to every pixel's offsets (t, s, e) along the detector axes
+ * u, v and the unit normal n, shared by all views (the pages' curved detectors:
+ * "Projection and matched backprojection support first-order surface
+ * gradients", diffct 2.1.0 -> 2.2.1, README "Curved detectors"; the point
+ * centre + t u + s v + e n, diffct 2.4.1 -> 2.4.2, kernels/surface_geometry.py
+ * `compose_surface`):
+ *
+ *     out[pix * 3 + m] = sum over views of w[ray] * (dp/d pixel) . (u, v, n)[m],
+ *
+ * flat detectors included (their offsets are the pitch grid); with one offset
+ * table per view, every view's pixel has its own gradient (out[ray * 3 + m],
+ * no sum over views).  Pixels run in parallel (each pixel's sums are owned by
+ * one thread).
+ */
+int ora_surface_vjp(const ora_ctx *c, const float *vol, const float *w, double *out,
+                    int nthreads)
+{
+    int T = ora_threads(nthreads);
+    int B = ora_buf_len(c);
+    long per_view = (long)c->n_u * c->n_v;
+    int per = c->offsets && c->offsets_per_view;  /* one offset table per view */
+    int err = 0;
+#pragma omp parallel num_threads(T)
+    {
+        double *buf = (double *)malloc(sizeof(double) * B);
+        if (!buf) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic, 16)
+            for (long pix = 0; pix < per_view; ++pix) {
+                double g[3] = {0, 0, 0};
+                for (long view = 0; view < c->n_views; ++view) {
+                    long ray = view * per_view + pix;
+                    double wr = (double)w[ray];
+                    double dsrc[3], dpix[3], u[3], v[3], n[3], cn;
+                    if (per) g[0] = g[1] = g[2] = 0.0;
+                    if (wr != 0.0 && ora_ray_gradient(c, vol, ray, buf, dsrc, dpix)) {
+                        ora_frame_axes(c, view, u, v, n, &cn);
+                        g[0] += wr * (dpix[0] * u[0] + dpix[1] * u[1] + dpix[2] * u[2]);
+                        g[1] += wr * (dpix[0] * v[0] + dpix[1] * v[1] + dpix[2] * v[2]);
+                        g[2] += wr * (dpix[0] * n[0] + dpix[1] * n[1] + dpix[2] * n[2]);
+                    }
+                    if (per)
+                        for (int m = 0; m < 3; ++m) out[3 * ray + m] = g[m];
+                }
+                if (!per)
+                    for (int m = 0; m < 3; ++m) out[3 * pix + m] = g[m];
             }
         }
         free(buf);

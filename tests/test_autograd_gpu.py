@@ -124,3 +124,34 @@ def test_geometry_gradients_through_autograd(oracle_mod, beam_idx):
     assert frames[0].grad.dtype == torch.float64
     back = oracle_mod.backward(scan, wt.ravel())
     assert rel_l2(x.grad.cpu().numpy(), back) <= 1e-4
+
+
+def test_surface_gradients_through_autograd(oracle_mod):
+    """loss = <A(frames, offsets) x, w> on a curved (cylindrical) detector: the
+    offsets' .grad equals the oracle's surface gradient and the frames' .grad
+    its curved geometry gradient (kink and face-plane rays carry zero weight)."""
+    import torch
+    import back_projection_ctp_b300 as ctp
+    from back_projection_ctp_b300.autograd import project_with_geometry
+    from test_oracle_curved_pins import _cylinder_offsets
+    w_ = ci.small_cases()[3]
+    f = ci.frames(ci.scaled(w_, 1.0, views=8, ragged=0))
+    n_u, n_v = 29, 23
+    off = _cylinder_offsets(n_u, n_v, 1000.0, 0.0131, 13.1)
+    scan = oracle_mod.Scan("divergent", f["src"], f["det_centre"], f["det_u"], f["det_v"], n_u,
+                           n_v, 1.0, 1.0, w_.shape, w_.spacing, w_.origin, 0.0, 0.0, 3, off)
+    skip = oracle_mod.ambiguous(scan) | oracle_mod.kinks(scan)
+    wt = np.where(skip, 0.0, np.random.default_rng(6).standard_normal(scan.sino_shape))
+    wt = wt.astype(np.float32)
+    vol = ci.phantom(w_)
+    geom = ctp.Geometry(ndim=3, beam="divergent", n_u=n_u, n_v=n_v, pitch_u=1.0, pitch_v=1.0,
+                        pixel_offsets=off, **f)
+    x = torch.from_numpy(vol).cuda()
+    offsets = torch.from_numpy(off.astype(np.float64)).requires_grad_()
+    frames = [torch.from_numpy(f[k].astype(np.float64)).requires_grad_()
+              for k in ("src", "det_centre", "det_u", "det_v")]
+    out = project_with_geometry(x, geom, volume_of(w_), *frames, pixel_offsets=offsets)
+    (out * torch.from_numpy(wt).cuda()).sum().backward()
+    assert rel_l2(offsets.grad.numpy(), oracle_mod.surface_vjp(scan, vol, wt.ravel())) <= 1e-4
+    got = np.stack([fr.grad.numpy() for fr in frames], axis=1)
+    assert rel_l2(got, oracle_mod.geometry_vjp(scan, vol, wt.ravel())) <= 1e-4
