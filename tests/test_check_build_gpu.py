@@ -5,7 +5,8 @@ FDK gather and transpose and of the geometry-gradient walks tests its index
 first and counts an index outside its buffer (skipping the access).  The suites' own checks must pass there too, and the autouse
 fixture in conftest.py requires zero counted accesses after every test --
 small ragged cases, every path, host-buffer chunking and the five workloads at
-full size in the benchmark's launch configuration."""
+full size in the benchmark's launch configuration, and the seeded random small
+scans (sources inside the grid, one-cell grids, single-row detectors)."""
 
 import os
 import subprocess
@@ -16,8 +17,9 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SUITES = ["tests/test_parity_gpu.py", "tests/test_curved_gpu.py", "tests/test_fdk_gpu.py",
-          "tests/test_geometry_gpu.py", "tests/test_autograd_gpu.py", "tests/test_zz_no_alloc.py"]
+SUITES = ["tests/test_parity_gpu.py", "tests/test_random_scans_gpu.py", "tests/test_curved_gpu.py",
+          "tests/test_fdk_gpu.py", "tests/test_geometry_gpu.py", "tests/test_autograd_gpu.py",
+          "tests/test_zz_no_alloc.py"]
 
 
 def test_walks_stay_in_bounds_in_the_checked_build():
