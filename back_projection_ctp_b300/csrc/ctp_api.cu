@@ -946,7 +946,10 @@ int ctp_surface_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *w
                     double *grad_dev, void *stream)
 {
     if (!plan) return CTP_E_NULL;
-    if (!grad_dev || (plan->n_rays > 0 && (!vol_dev || !weight_dev))) return CTP_E_NULL;
+    // the output is empty only for per-view tables of an empty scan
+    const bool empty_out = plan->offsets_per_view && plan->n_views == 0;
+    if ((!grad_dev && !empty_out) || (plan->n_rays > 0 && (!vol_dev || !weight_dev)))
+        return CTP_E_NULL;
     int st = check_device(plan);
     if (st != CTP_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;

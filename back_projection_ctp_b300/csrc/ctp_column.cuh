@@ -386,8 +386,18 @@ __device__ __forceinline__ void column_walk_sz(const ColumnTrace &C, RowZ (&Z)[R
     if (ka <= kb) {
         for (; k < ka; ++k)
             column_slab<R, false, true, SZ>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
-        for (; k <= kb; ++k)
-            column_slab<R, false, false, SZ>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
+        if constexpr (Op::kUnrollPairs) {
+            // two slabs per iteration: the next slab's reductions issue while
+            // this one's are in flight (the forward's gathers would spill)
+#pragma unroll 2
+            for (; k <= kb; ++k)
+                column_slab<R, false, false, SZ>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f,
+                                                 op);
+        } else {
+            for (; k <= kb; ++k)
+                column_slab<R, false, false, SZ>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f,
+                                                 op);
+        }
     }
     for (; k < C.k1; ++k)
         column_slab<R, false, true, SZ>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
@@ -412,8 +422,12 @@ __device__ __forceinline__ void column_walk(const ColumnTrace &C, RowZ (&Z)[R], 
     else column_walk_sz<R, 1>(C, Z, nz, op);
 }
 
+// kUnrollPairs: the walk's check-free slab loop runs two slabs per iteration
+// (measured: backward 0.7-1.4 % faster; the gather at 64 registers spills and
+// slows by up to 16 %).
 template <int R>
 struct ColumnGather {
+    static constexpr bool kUnrollPairs = false;
     const float *__restrict__ vol;
     float acc[R];
     long long lim;  // cells of the padded working copy (bounds-checked builds)
@@ -425,6 +439,7 @@ struct ColumnGather {
 
 template <int R>
 struct ColumnScatter {
+    static constexpr bool kUnrollPairs = true;
     float *__restrict__ vol;
     float w[R];  // ell * y of each row
     long long lim;
@@ -437,6 +452,7 @@ struct ColumnScatter {
 
 template <int R>
 struct ColumnCount {
+    static constexpr bool kUnrollPairs = false;
     unsigned n;
     float thr[R];
     unsigned nb;
