@@ -44,6 +44,9 @@ CSRC = os.path.join(ROOT, "back_projection_ctp_b300", "csrc")
 # ncu figures of profiled kernels (DRAM bytes per launch, limiting units), each
 # with the hash of the kernel sources it was captured on
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+# calls per CUDA graph in the other workloads' per-call timings: enough that
+# the microsecond-scale 2-D calls are not timed one launch at a time
+PER_WORKLOAD_CALLS = 20
 
 
 # ----------------------------------------------------------------- helpers
@@ -319,11 +322,14 @@ def run_reference(args, w, world, rank):
 
 
 # ------------------------------------------------------------------ GPU arm
-def time_pair(ctp, plan, d_vol, d_y, d_sino, d_g, steps, warmup, dev, stream):
-    """Device times (ms) of one forward call, one backward call and one step
-    (forward + backward) on the caller's stream: each from one CUDA graph of
-    ``steps`` calls replayed between CUDA events.  Returns (step, fwd, bwd) and
-    the step graph's timing function for the caller's timed region."""
+def time_pair(ctp, plan, d_vol, d_y, d_sino, d_g, steps, warmup, dev, stream, calls=None):
+    """Device times (ms) of one forward call and one backward call on the
+    caller's stream, each the median over three replays (after an untimed one)
+    of a CUDA graph of ``calls`` calls (default ``steps``) between CUDA events;
+    plus the graph of ``steps`` forward + backward steps and the timing function
+    for the caller's timed region."""
+    import statistics
+
     import torch
 
     for _ in range(warmup):
@@ -332,22 +338,24 @@ def time_pair(ctp, plan, d_vol, d_y, d_sino, d_g, steps, warmup, dev, stream):
     torch.cuda.synchronize(dev)
 
     # The calls only enqueue kernels and a memset, so they capture as they are.
-    def capture(body):
+    def capture(body, n):
         graph = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(dev)
         side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(side), torch.cuda.graph(graph, stream=side):
             cur = torch.cuda.current_stream(dev)
-            for _ in range(steps):
+            for _ in range(n):
                 body(cur)
         torch.cuda.synchronize(dev)
         return graph
 
+    calls = calls or steps
     g_steps = capture(lambda st: (ctp.ctp_forward(plan, d_vol, d_sino, st),
-                                  ctp.ctp_backward(plan, d_y, d_g, st)))
-    g_fwd = capture(lambda st: ctp.ctp_forward(plan, d_vol, d_sino, st))
-    g_bwd = capture(lambda st: ctp.ctp_backward(plan, d_y, d_g, st))
-    g_steps.replay()  # one untimed replay of the captured steps
+                                  ctp.ctp_backward(plan, d_y, d_g, st)), steps)
+    g_fwd = capture(lambda st: ctp.ctp_forward(plan, d_vol, d_sino, st), calls)
+    g_bwd = capture(lambda st: ctp.ctp_backward(plan, d_y, d_g, st), calls)
+    for graph in (g_steps, g_fwd, g_bwd):  # one untimed replay each (graph upload)
+        graph.replay()
     torch.cuda.synchronize(dev)
 
     def timed(graph):
@@ -358,7 +366,10 @@ def time_pair(ctp, plan, d_vol, d_y, d_sino, d_g, steps, warmup, dev, stream):
         torch.cuda.synchronize(dev)
         return a.elapsed_time(b)
 
-    return timed, g_steps, timed(g_fwd) / steps, timed(g_bwd) / steps
+    def per_call(graph):
+        return statistics.median(timed(graph) for _ in range(3)) / calls
+
+    return timed, g_steps, per_call(g_fwd), per_call(g_bwd)
 
 
 def kernel_of(path, call):
@@ -399,7 +410,8 @@ def per_workload(args, ctp, dev, stream, peaks, skip):
         d_sino = torch.empty(plan.sino_shape, dtype=torch.float32, device=dev)
         d_g = torch.empty(plan.vol_shape, dtype=torch.float32, device=dev)
         timed, g_steps, fwd_ms, bwd_ms = time_pair(ctp, plan, d_vol, d_y, d_sino, d_g,
-                                                   args.steps, args.warmup, dev, stream)
+                                                   args.steps, args.warmup, dev, stream,
+                                                   calls=max(args.steps, PER_WORKLOAD_CALLS))
         step_ms = timed(g_steps) / args.steps
         seg = golden_segments(idx)
         out[w.name] = {
