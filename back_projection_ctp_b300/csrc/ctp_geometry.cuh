@@ -555,7 +555,7 @@ __global__ void __launch_bounds__(TU *TV) surface_vjp_kernel(RayParams P, GeomPa
     // one offset table per view: every view's pixel has its own sums (out is
     // (n_views, n_v, n_u, 3)); else the sums run over the views
     const bool per_view = P.offsets && P.offsets_per_view;
-    const long long nout = 3LL * P.n_u * P.n_v * (per_view ? P.n_views : 1);
+    [[maybe_unused]] const long long nout = 3LL * P.n_u * P.n_v * (per_view ? P.n_views : 1);
     double acc[3] = {0.0, 0.0, 0.0};
     for (int view = 0; view < P.n_views; ++view) {
         const long long ray = ((long long)view * P.n_v + iv) * P.n_u + iu;

@@ -22,7 +22,8 @@ namespace ctp {
 
 constexpr int kPlaneHalo = 2;
 
-struct PlaneRay {
+// 64 bytes; the walks read only the first 48 (plane_ray_walk_state).
+struct __align__(16) PlaneRay {
     int k0, k1;          // slab range (k1 < k0: the ray misses)
     float tlo, thi;      // partial first / last slab fractions (ray ends)
     uint32_t fb, bb;     // transverse fraction at slab k0 and slope (2^-32 cell)
@@ -30,10 +31,51 @@ struct PlaneRay {
     int addr;            // offset of cell (k0, jb) in the combined padded buffer
     int sp, sb;          // signed strides along the slab axis and the transverse axis
     int jb;              // transverse (mirrored) index at slab k0
-    int nb;              // transverse extent
     float ell;           // physical length per slab
+    int nb;              // transverse extent
     int pad_[3];         // pad_[0]: the slab axis (0 = x, 1 = y)
 };
+
+static_assert(sizeof(PlaneRay) == 64 && offsetof(PlaneRay, ell) == 44,
+              "the walk state is the first three 16-byte words");
+
+// The walk state of a ray (every field but nb and pad_) in three 16-byte
+// loads: a warp reading 32 adjacent records field by field would touch 32
+// sectors per field, for 11 fields.
+__device__ __forceinline__ PlaneRay plane_ray_walk_state(const PlaneRay *__restrict__ T,
+                                                         long long ray)
+{
+    const int4 *q = reinterpret_cast<const int4 *>(T + ray);
+    const int4 a = __ldg(q), b = __ldg(q + 1), c = __ldg(q + 2);
+    PlaneRay R;
+    R.k0 = a.x;
+    R.k1 = a.y;
+    R.tlo = __int_as_float(a.z);
+    R.thi = __int_as_float(a.w);
+    R.fb = (uint32_t)b.x;
+    R.bb = (uint32_t)b.y;
+    R.ib = __int_as_float(b.z);
+    R.addr = b.w;
+    R.sp = c.x;
+    R.sb = c.y;
+    R.jb = c.z;
+    R.ell = __int_as_float(c.w);
+    R.nb = 0;
+    R.pad_[0] = R.pad_[1] = R.pad_[2] = 0;
+    return R;
+}
+
+// The whole record (four 16-byte loads).
+__device__ __forceinline__ PlaneRay plane_ray_record(const PlaneRay *__restrict__ T, long long ray)
+{
+    PlaneRay R = plane_ray_walk_state(T, ray);
+    const int4 d = __ldg(reinterpret_cast<const int4 *>(T + ray) + 3);
+    R.nb = d.x;
+    R.pad_[0] = d.y;
+    R.pad_[1] = d.z;
+    R.pad_[2] = d.w;
+    return R;
+}
 
 struct PlaneLayout {
     int nx, ny;
@@ -329,7 +371,7 @@ __global__ void __launch_bounds__(32 * CH) plane_forward_kernel(RayParams P,
     // 0.162 -> 0.193 ms, the idle iterations cost more issue than the wider
     // loads did).
     if (iu < P.n_u) {
-        R = T[ray];
+        R = plane_ray_walk_state(T, ray);
         if (R.k0 <= R.k1) {
             const int len = (R.k1 - R.k0 + CH) / CH;
             const int ka = R.k0 + chunk * len;
@@ -372,7 +414,7 @@ __global__ void __launch_bounds__(32 * CH) plane_backward_kernel(RayParams P,
     R.ell = 0.0f;
     if (iu < P.n_u && ctp_in(ray, sino_cells(P), kSitePlaneSinoLoad)) {
         y = sino[ray];
-        if (y != 0.0f) R = T[ray];
+        if (y != 0.0f) R = plane_ray_walk_state(T, ray);
     }
     int ka, kb, la, lb;
     if (!plane_lockstep_range<CH>(R, y != 0.0f && R.k0 <= R.k1, chunk, ka, kb, la, lb)) return;
@@ -389,7 +431,7 @@ __global__ void __launch_bounds__(kPlaneBlock) plane_count_kernel(RayParams P,
         (long long)(P.view0 + (int)blockIdx.y) * P.n_u + blockIdx.x * kPlaneBlock + threadIdx.x;
     unsigned n = 0;
     if (blockIdx.x * kPlaneBlock + threadIdx.x < P.n_u) {
-        const PlaneRay R = T[ray];
+        const PlaneRay R = plane_ray_record(T, ray);
         if (R.k0 <= R.k1) {
             PlaneCount op{0u, __fdiv_rn(P.min_len, R.ell), (unsigned)R.nb};
             plane_walk(R, op);
@@ -423,6 +465,23 @@ __global__ void __launch_bounds__(256) plane_pack_kernel(PlaneLayout G, const fl
     }
 }
 
+// Sum over the copies of one cell (stride apart), added in copy order to v.
+// The loads go out four at a time: a thread sums several cells over every
+// copy, and one load in flight per thread left the unpack latency-bound
+// (C2: 31 us of 34 MB in the launch list).
+__device__ __forceinline__ float plane_sum_copies(const float *__restrict__ p, int copies,
+                                                  long long stride, float v)
+{
+    int c = 0;
+    for (; c + 4 <= copies; c += 4) {
+        const float *q = p + c * stride;
+        const float a0 = q[0], a1 = q[stride], a2 = q[2 * stride], a3 = q[3 * stride];
+        v = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(v, a0), a1), a2), a3);
+    }
+    for (; c < copies; ++c) v = __fadd_rn(v, p[c * stride]);
+    return v;
+}
+
 // out (ny, nx) = sum over copies of (interior of the x-fastest buffer +
 // transposed interior of the y-fastest buffer).
 __global__ void __launch_bounds__(256) plane_unpack_kernel(PlaneLayout G,
@@ -435,24 +494,18 @@ __global__ void __launch_bounds__(256) plane_unpack_kernel(PlaneLayout G,
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     for (int j = ty; j < 32; j += 8) {
         const int x = x0 + j, y = y0 + tx;
-        if (x < G.nx && y < G.ny) {
-            float v = 0.0f;
-            for (int c = 0; c < copies; ++c)
-                v = __fadd_rn(v, buf[c * copy_cells + G.off1 + (size_t)(x + kPlaneHalo) * G.py +
-                                     (y + kPlaneHalo)]);
-            tile[j][tx] = v;
-        }
+        if (x < G.nx && y < G.ny)
+            tile[j][tx] = plane_sum_copies(
+                buf + G.off1 + (size_t)(x + kPlaneHalo) * G.py + (y + kPlaneHalo), copies,
+                copy_cells, 0.0f);
     }
     __syncthreads();
     for (int j = ty; j < 32; j += 8) {
         const int y = y0 + j, x = x0 + tx;
-        if (y < G.ny && x < G.nx) {
-            float v = tile[tx][j];
-            for (int c = 0; c < copies; ++c)
-                v = __fadd_rn(v, buf[c * copy_cells + (size_t)(y + kPlaneHalo) * G.px +
-                                     (x + kPlaneHalo)]);
-            out[(size_t)y * G.nx + x] = v;
-        }
+        if (y < G.ny && x < G.nx)
+            out[(size_t)y * G.nx + x] = plane_sum_copies(
+                buf + (size_t)(y + kPlaneHalo) * G.px + (x + kPlaneHalo), copies, copy_cells,
+                tile[tx][j]);
     }
 }
 
@@ -550,7 +603,7 @@ __global__ void __launch_bounds__(256) plane_backward_tiled_kernel(RayParams P,
             if (!ctp_in(ray, sino_cells(P), kSitePlaneSinoLoad)) continue;
             const float y = sino[ray];
             if (y == 0.0f) continue;
-            const PlaneRay R = T[ray];
+            const PlaneRay R = plane_ray_record(T, ray);
             if (R.k0 > R.k1) continue;
             const int p = R.pad_[0];
             const bool mp = R.sp < 0, mb = R.sb < 0;
@@ -695,7 +748,9 @@ inline int plane_walk_forward(const RayParams &P, const void *d_rays, const floa
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 
-// Privatised-accumulator backward: prepare, walk view ranges, layout out.
+// Privatised-accumulator backward: prepare, walk view ranges, layout out.  (A
+// layout out that zeroed the copies as it read them, in place of the
+// zero-fill, measured slower: C2 0.223 -> 0.313 ms.)
 inline int plane_backward_prepare(const RayParams &P, float *d_bwd, cudaStream_t s)
 {
     const PlaneLayout G = plane_layout(P);

@@ -328,8 +328,6 @@ def time_pair(ctp, plan, d_vol, d_y, d_sino, d_g, steps, warmup, dev, stream, ca
     of a CUDA graph of ``calls`` calls (default ``steps``) between CUDA events;
     plus the graph of ``steps`` forward + backward steps and the timing function
     for the caller's timed region."""
-    import statistics
-
     import torch
 
     for _ in range(warmup):
@@ -543,6 +541,9 @@ def run_gpu(args, w, world, rank, local):
                                    "note": f"the same 4 B per segment over the HBM copy "
                                            f"bandwidth ({hbm_src}); not a DRAM measurement"},
                 "dram_frac": (traffic / (dom_ms * 1e-3) / 1e9 / hbm) if traffic else None,
+                # the floor of any implementation's DRAM traffic for one call:
+                # its input and output arrays once each
+                "compulsory_bytes": 4 * (w.n_voxels + w.n_rays),
                 "ncu": stored_ncu(kernel_name, w.name),
                 "note": f"4 algorithmic bytes per segment over the {dominant} call's event "
                         "time; dram_frac = the ncu DRAM bytes of one launch over the same "

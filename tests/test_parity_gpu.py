@@ -130,6 +130,36 @@ def test_plane_backward_variants_match_oracle(torch, ctp, oracle_mod, mode):
     assert rel_l2(g, g_ref) <= TOL_BACKWARD
 
 
+def test_plane_privatised_copies_start_every_call_at_zero(torch, ctp, oracle_mod):
+    """The privatised backward's accumulator copies carry nothing from one call
+    to the next: calls in a row on one plan (device and host-buffer, sinograms
+    of growing scale) each match the oracle, and a zero sinogram after nonzero
+    ones backprojects to exactly zero."""
+    w = SMALL[2]
+    f = ci.frames(w)
+    scan = oracle_mod.Scan.from_workload(w, f)
+    plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w), "plane",
+                        options={"plane_backward": "privatised", "host_chunks": 3})
+    rng = np.random.default_rng(77)
+    d_g = torch.empty(plan.vol_shape, dtype=torch.float32, device="cuda")
+    for k in range(3):
+        y = (rng.standard_normal(plan.sino_shape) * 10.0 ** k).astype(np.float32)
+        g_ref = oracle_mod.backward(scan, y.ravel())
+        if k == 1:
+            g = np.full(plan.vol_shape, np.nan, np.float32)
+            ctp.ctp_backward_host(plan, y, g)
+        else:
+            d_g.fill_(float("nan"))
+            ctp.ctp_backward(plan, torch.from_numpy(y).cuda(), d_g)
+            g = d_g.cpu().numpy()
+        assert rel_l2(g, g_ref) <= TOL_BACKWARD, k
+        assert max_rel_err(g, g_ref) <= TOL_BACKWARD_MAX, k
+    d_g.fill_(float("nan"))
+    ctp.ctp_backward(plan, torch.zeros(plan.sino_shape, device="cuda"), d_g)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(d_g).item() == 0
+
+
 @pytest.mark.parametrize("rows", [1, 2, 3, 4])
 @pytest.mark.parametrize("adjacent", [0, 1])
 def test_column_work_layouts_match_oracle(torch, ctp, oracle_mod, rows, adjacent):
