@@ -18,6 +18,10 @@
 //   ctp_probe_smem_accumulate  float accumulation in shared memory: atomics,
 //                           plain load-add-store, and atomics with 4 lanes per
 //                           word (a work-layout question of the backward walks).
+//   ctp_probe_l2_bulk_reduction  the async copy engine's bulk reductions of
+//                           shared-memory runs into the same kind of buffer
+//                           (full sectors): whether L2 takes them faster than
+//                           a dense stream of float reductions.
 //
 // Both walk the buffer with a per-warp stride so that concurrent warps touch
 // different lines; the caller times them with CUDA events on `stream`.
@@ -86,6 +90,35 @@ __global__ void __launch_bounds__(256) probe_smem_kernel(int iters, int mode, fl
     if (acc[threadIdx.x] == 1.2345e-30f) sink[0] = acc[threadIdx.x];
 }
 
+// Bulk reductions (the async copy engine's cp.reduce.async.bulk .add.f32): the
+// first `lanes` lanes of every warp each add a `bytes`-long run of shared
+// memory into the next run of buf, at most 8 runs in flight per thread.
+__global__ void __launch_bounds__(256) probe_bulk_red_kernel(float *__restrict__ buf, long long n,
+                                                             int iters, int bytes, int lanes)
+{
+    __shared__ __align__(128) float src[1024];
+    for (int i = threadIdx.x; i < 1024; i += blockDim.x) src[i] = 1.0f + 1e-3f * (i & 31);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    if (lane >= lanes) return;
+    const unsigned s = (unsigned)__cvta_generic_to_shared(src);
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long issuers = (((long long)gridDim.x * blockDim.x) >> 5) * lanes;
+    const long long seg = bytes / 4;
+    const long long segs = n / seg;
+    long long g = warp * lanes + lane;
+    for (int it = 0; it < iters; ++it) {
+        asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
+                     :: "l"(buf + g * seg), "r"(s), "r"(bytes) : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group.read 8;" ::: "memory");
+        g += issuers;
+        if (g >= segs) g -= segs;
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 int blocks_for(int sms) { return sms * 8; }
 
 }  // namespace
@@ -138,6 +171,28 @@ int ctp_probe_smem_accumulate(int iters, int mode, float *sink, void *stream)
         return 9;
     if (!sink || iters < 1 || mode < 0 || mode > 2) return 1;
     probe_smem_kernel<<<blocks_for(sms), 256, 0, (cudaStream_t)stream>>>(iters, mode, sink);
+    return cudaGetLastError() == cudaSuccess ? 0 : 9;
+}
+
+// Bulk-reduction rate (see probe_bulk_red_kernel): 8 blocks of 256 threads per
+// SM, `lanes` (1..32) issuing lanes per warp, `iters` runs of `bytes` (16..4096,
+// a multiple of 16) per issuing lane into buf[0, n) (16-byte aligned, n a
+// multiple of bytes / 4, at least as many runs as issuing lanes).  Useful bytes
+// per launch: bytes * issuing lanes * iters.  Returns 0, 1 or 9.
+int ctp_probe_l2_bulk_reduction(float *buf, long long n, int iters, int bytes, int lanes,
+                                void *stream)
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 9;
+    if (!buf || ((uintptr_t)buf & 15) || iters < 1 || bytes < 16 || bytes > 4096 ||
+        bytes % 16 != 0 || lanes < 1 || lanes > 32)
+        return 1;
+    const long long seg = bytes / 4, issuers = (long long)blocks_for(sms) * 256 / 32 * lanes;
+    if (n % seg != 0 || n / seg < issuers) return 1;
+    probe_bulk_red_kernel<<<blocks_for(sms), 256, 0, (cudaStream_t)stream>>>(buf, n, iters, bytes,
+                                                                             lanes);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 

@@ -106,6 +106,8 @@ def l2_peaks(dev, stream, repeats=5):
     lib.ctp_probe_sm_count.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.ctp_probe_smem_accumulate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                               ctypes.c_void_p]
+    lib.ctp_probe_l2_bulk_reduction.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     sms = ctypes.c_int(0)
     if lib.ctp_probe_sm_count(ctypes.byref(sms)) != 0:
         raise RuntimeError("ctp_probe_sm_count failed")
@@ -146,8 +148,15 @@ def l2_peaks(dev, stream, repeats=5):
         rate = best(lambda: check(lib.ctp_probe_smem_accumulate(it_load, mode, sink.data_ptr(),
                                                                 sp)), 1.0 * threads * it_load)
         smem[name] = rate / sms.value / 2.032e9
+    # bulk reductions of the async copy engine: 256-byte runs from shared memory,
+    # 8 issuing lanes per warp (full sectors, like a dense reduction stream)
+    it_bulk, run, lanes = 200, 256, 8
+    bulk = best(lambda: check(lib.ctp_probe_l2_bulk_reduction(buf.data_ptr(), n, it_bulk, run,
+                                                              lanes, sp)),
+                1.0 * run * (threads // 32) * lanes * it_bulk)
     return {"reduction_gbs": red / 1e9, "reduction_sectors_per_s": sectors,
-            "load_gbs": load / 1e9, "smem_adds_per_clock_per_sm": smem,
+            "load_gbs": load / 1e9, "bulk_reduction_gbs": bulk / 1e9,
+            "smem_adds_per_clock_per_sm": smem,
             "how": "libctp_probe.so: 8 blocks x 256 threads per SM over a 64 MiB buffer held "
                    "in L2 (shared memory: 256 words per block); best of 5 launches timed "
                    "with CUDA events"}
