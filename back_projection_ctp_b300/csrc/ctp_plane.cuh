@@ -265,25 +265,43 @@ __device__ __forceinline__ void plane_walk_range(const PlaneRay &R, int ka, int 
 
 // Lockstep walk of the slabs [la, lb] of a ray inside a warp-uniform slab loop
 // [ka, kb] ([la, lb] within both [ka, kb] and the ray's [k0, k1]; la > lb: the
-// lane walks nothing).  Every lane of the warp steps the same slab k at the same
-// time, so the 32 adjacent rays of a view touch one row of the padded copy per
-// instruction (consecutive transverse cells) instead of rows as far apart as
-// their entry slabs.  The fixed-point state jumps exactly to slab la, as in
-// plane_walk_range, so the pieces are those of the whole walk.
+// lane walks nothing and its op is switched off).  Every lane of the warp steps
+// the same slab k at the same time, so the 32 adjacent rays of a view touch one
+// row of the padded copy per instruction (consecutive transverse cells) instead
+// of rows as far apart as their entry slabs.  The fixed-point state jumps
+// exactly to slab la, as in plane_walk_range, so the pieces are those of the
+// whole walk.  The slabs where every active lane is inside its range and off
+// its ray's end slabs run unclamped and untested; only the warp's boundary
+// slabs clamp to [lo, hi] (the ray's own ends, else [0, 1]) and test the range.
 template <class Op>
 __device__ __forceinline__ void plane_walk_lockstep(const PlaneRay &R, int ka, int kb, int la,
                                                     int lb, Op &op)
 {
-    const int start = la <= lb ? la : R.k0;
+    const bool active = la <= lb;
+    const int start = active ? la : R.k0;
     const unsigned long long n = (unsigned long long)(start - R.k0);
     const unsigned long long F = (unsigned long long)R.fb + n * (unsigned long long)R.bb;
     const int carries = (int)(F >> 32);
     uint32_t fb = (uint32_t)F;
     int jb = R.jb + carries;
     int addr = R.addr + (int)n * R.sp + carries * R.sb;
-    // every slab clamps to [lo, hi] (the ray's own ends, else [0, 1]): one code
-    // path for the whole warp, no branch on the first / last slab
-    for (int k = ka; k <= kb; ++k) {
+    op.live = active;
+    // a chunk of the warp's union of ranges can fall in a gap between the
+    // lanes' ranges: then no lane walks anything
+    if (!__any_sync(0xffffffffu, active)) return;
+    // interior [ia, ib] within [ka, kb] (idle lanes pass the chunk's own ends)
+    const int ia = __reduce_max_sync(0xffffffffu, active ? max(la, R.k0 + 1) : ka);
+    const int ib = __reduce_min_sync(0xffffffffu, active ? min(lb, R.k1 - 1) : kb);
+    const int ea = ia <= ib ? ia : kb + 1;
+    for (int k = ka; k < ea; ++k) {
+        if (k < la || k > lb) continue;
+        plane_slab<true>(fb, R.bb, R.ib, jb, addr, R.sp, R.sb, k == R.k0 ? R.tlo : 0.0f,
+                         k == R.k1 ? R.thi : 1.0f, op);
+    }
+    if (ia > ib) return;
+    for (int k = ia; k <= ib; ++k)
+        plane_slab<false>(fb, R.bb, R.ib, jb, addr, R.sp, R.sb, 0.0f, 1.0f, op);
+    for (int k = ib + 1; k <= kb; ++k) {
         if (k < la || k > lb) continue;
         plane_slab<true>(fb, R.bb, R.ib, jb, addr, R.sp, R.sb, k == R.k0 ? R.tlo : 0.0f,
                          k == R.k1 ? R.thi : 1.0f, op);
@@ -320,14 +338,16 @@ struct PlaneGather {
 };
 
 // A piece of zero length adds 0 (no test: the first piece of a slab is all
-// but never empty, the second goes out only after a crossing).
+// but never empty, the second goes out only after a crossing).  live: the
+// lane walks a ray in this chunk (the lockstep walk switches idle lanes off).
 struct PlaneScatter {
     float *__restrict__ img;
     float w;
     long long lim;
+    bool live = true;
     __device__ __forceinline__ void operator()(int a, float d, bool on, int)
     {
-        if (on && ctp_in(a, lim, kSitePlaneScatter)) atomicAdd(img + a, __fmul_rn(d, w));
+        if (on && live && ctp_in(a, lim, kSitePlaneScatter)) atomicAdd(img + a, __fmul_rn(d, w));
     }
 };
 
@@ -366,10 +386,11 @@ __global__ void __launch_bounds__(32 * CH) plane_forward_kernel(RayParams P,
     R.k0 = 0;
     R.k1 = -1;
     R.ell = 0.0f;
-    // Each ray walks its own chunk of its own slab range (a lockstep walk over
-    // the warp's union of ranges measured slower for the gather: C2 forward
-    // 0.162 -> 0.193 ms, the idle iterations cost more issue than the wider
-    // loads did).
+    // Each ray walks its own chunk of its own slab range.  A lockstep walk over
+    // the warp's union of ranges (one row of the padded copy per gather
+    // instruction) measured slower, with every slab clamped (C2 forward 0.162 ->
+    // 0.193 ms) and with only the warp's boundary slabs clamped (0.138 ->
+    // 0.152 ms): its idle iterations cost more issue than L1 saves.
     if (iu < P.n_u) {
         R = plane_ray_walk_state(T, ray);
         if (R.k0 <= R.k1) {
