@@ -397,7 +397,8 @@ int validate_options(const ctp_plan_options *o)
                     o->rows_backward <= 4 &&
                     (o->backward_rows_adjacent == 0 || o->backward_rows_adjacent == 1) &&
                     o->plane_backward >= 0 && o->plane_backward <= 2 && o->host_chunks >= 0 &&
-                    o->host_chunks <= 64 && (o->geometry_walk == 0 || o->geometry_walk == 1);
+                    o->host_chunks <= 64 && (o->geometry_walk == 0 || o->geometry_walk == 1) &&
+                    o->forward_ahead >= 0 && o->forward_ahead <= 2;
     return ok ? CTP_OK : CTP_E_OPTION;
 }
 
@@ -599,7 +600,8 @@ int ctp_plan_ex(const ctp_geometry *geom, const ctp_volume *vol, int path,
     if (chosen == CTP_PATH_COLUMN || chosen == CTP_PATH_PLANE) {
         if (chosen == CTP_PATH_COLUMN)
             st = ctp::column_plan_build(ray_params(p), p->opt.rows_forward, p->opt.rows_backward,
-                                        p->opt.backward_rows_adjacent != 0, &p->col,
+                                        p->opt.backward_rows_adjacent != 0,
+                                        p->opt.forward_ahead, &p->col,
                                         &p->d_table, &p->d_work_fwd,
                                         &p->d_work_bwd, &p->device_bytes);
         else

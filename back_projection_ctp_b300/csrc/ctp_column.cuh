@@ -50,6 +50,7 @@ struct ColumnPlan {
     int rows_fwd;        // detector rows per thread of the forward (1 to 4)
     int rows_bwd;        // ... of the backward and the counter
     bool bwd_interleave; // backward with 2 rows: rows interleaved across lanes
+    bool fwd_ahead;      // forward gathers one slab ahead (column_slab_ahead)
 };
 
 // Zero halo (cells) around x and y of the padded working copies: the walk's
@@ -360,6 +361,70 @@ __device__ __forceinline__ void column_slab(uint32_t &fb, uint32_t bb, float ib,
     fb = gb;
 }
 
+// A check-free slab of the forward gather with its first piece's value loaded
+// one slab ahead: v[r] holds the value of row r's cell at the slab's start,
+// and the slab ends by loading the cell where the row's next slab starts (in
+// the check-free range that cell is inside the grid: the row's z index at the
+// slab's end is).  The gather's latency is then hidden behind a whole slab;
+// the pieces and the order of the sums are those of column_slab.
+template <int R, int SZ>
+__device__ __forceinline__ void column_slab_ahead(uint32_t &fb, uint32_t bb, float ib, int &jb,
+                                                  int sb, int &xy, int sp, RowZ (&Z)[R],
+                                                  const float *__restrict__ vol, float (&acc)[R],
+                                                  float (&v)[R], long long lim)
+{
+    const uint32_t gb = fb + bb;
+    const bool cb = gb < fb;
+    if (!cb) {
+        const int nx = xy + sp;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t gz = Z[r].fz + Z[r].bz;
+            const bool cz = gz < Z[r].fz;
+            const float e = cz ? fmaxf(__fmaf_rn(-__uint2float_rn(gz), Z[r].ibz, 1.0f), 0.0f) : 1.0f;
+            const float d1 = __fsub_rn(1.0f, e);
+            const int sz = SZ ? SZ : Z[r].sz;
+            const int a1 = xy + Z[r].zoff + sz;
+            acc[r] = __fmaf_rn(e, v[r], acc[r]);
+            if (cz && ctp_in(a1, lim, kSiteColumnGather))
+                acc[r] = __fmaf_rn(d1, __ldg(vol + a1), acc[r]);
+            Z[r].fz = gz;
+            if (cz) Z[r].zoff += sz;
+            const int an = nx + Z[r].zoff;
+            v[r] = ctp_in(an, lim, kSiteColumnGather) ? __ldg(vol + an) : 0.0f;
+        }
+        xy = nx;
+    } else {
+        const float tb = fmaxf(__fmaf_rn(-__uint2float_rn(gb), ib, 1.0f), 0.0f);
+        const int nx = xy + sp + sb;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t gz = Z[r].fz + Z[r].bz;
+            const bool cz = gz < Z[r].fz;
+            const float tz =
+                cz ? fmaxf(__fmaf_rn(-__uint2float_rn(gz), Z[r].ibz, 1.0f), 0.0f) : 1.0f;
+            const bool bfirst = tb < tz;
+            const float e1 = fminf(tb, tz), e2 = fmaxf(tb, tz);
+            const float d2 = __fsub_rn(e2, e1);
+            const float d3 = __fsub_rn(1.0f, e2);
+            const int sz = SZ ? SZ : Z[r].sz;
+            const int a0 = xy + Z[r].zoff;
+            const int a2 = a0 + (bfirst ? sb : sz), a3 = a0 + sb + sz;
+            acc[r] = __fmaf_rn(e1, v[r], acc[r]);
+            if (ctp_in(a2, lim, kSiteColumnGather)) acc[r] = __fmaf_rn(d2, __ldg(vol + a2), acc[r]);
+            if (cz && ctp_in(a3, lim, kSiteColumnGather))
+                acc[r] = __fmaf_rn(d3, __ldg(vol + a3), acc[r]);
+            Z[r].fz = gz;
+            if (cz) Z[r].zoff += sz;
+            const int an = nx + Z[r].zoff;
+            v[r] = ctp_in(an, lim, kSiteColumnGather) ? __ldg(vol + an) : 0.0f;
+        }
+        xy = nx;
+        jb += 1;
+    }
+    fb = gb;
+}
+
 // Walk all slabs of a column for R rows: partial first / last slab peeled off;
 // between them the slabs where every row of the warp is inside the grid in z
 // (ka..kb) run without validity tests, the others with them.
@@ -386,7 +451,17 @@ __device__ __forceinline__ void column_walk_sz(const ColumnTrace &C, RowZ (&Z)[R
     if (ka <= kb) {
         for (; k < ka; ++k)
             column_slab<R, false, true, SZ>(fb, bb, ib, jb, sb, xy, sp, Z, nz, 0.0f, 1.0f, op);
-        if constexpr (Op::kUnrollPairs) {
+        if constexpr (Op::kAhead) {
+            // the gather: each row's first piece loaded one slab ahead
+            float v[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int a = xy + Z[r].zoff;
+                v[r] = ctp_in(a, op.lim, kSiteColumnGather) ? __ldg(op.vol + a) : 0.0f;
+            }
+            for (; k <= kb; ++k)
+                column_slab_ahead<R, SZ>(fb, bb, ib, jb, sb, xy, sp, Z, op.vol, op.acc, v, op.lim);
+        } else if constexpr (Op::kUnrollPairs) {
             // two slabs per iteration: the next slab's reductions issue while
             // this one's are in flight (the forward's gathers would spill)
 #pragma unroll 2
@@ -424,10 +499,12 @@ __device__ __forceinline__ void column_walk(const ColumnTrace &C, RowZ (&Z)[R], 
 
 // kUnrollPairs: the walk's check-free slab loop runs two slabs per iteration
 // (measured: backward 0.7-1.4 % faster; the gather at 64 registers spills and
-// slows by up to 16 %).
-template <int R>
+// slows by up to 16 %).  kAhead: the gather's check-free slabs load each row's
+// first piece one slab ahead (column_slab_ahead).
+template <int R, bool AHEAD = false>
 struct ColumnGather {
     static constexpr bool kUnrollPairs = false;
+    static constexpr bool kAhead = AHEAD;
     const float *__restrict__ vol;
     float acc[R];
     long long lim;  // cells of the padded working copy (bounds-checked builds)
@@ -440,6 +517,7 @@ struct ColumnGather {
 template <int R>
 struct ColumnScatter {
     static constexpr bool kUnrollPairs = true;
+    static constexpr bool kAhead = false;
     float *__restrict__ vol;
     float w[R];  // ell * y of each row
     long long lim;
@@ -453,6 +531,7 @@ struct ColumnScatter {
 template <int R>
 struct ColumnCount {
     static constexpr bool kUnrollPairs = false;
+    static constexpr bool kAhead = false;
     unsigned n;
     float thr[R];
     unsigned nb;
@@ -467,7 +546,7 @@ constexpr int kColumnsPerBlock = 8;  // 8 warps: 8 columns, each 32 * R rows
 // Rows a forward thread owns: iv = band * 32R + 32 r + lane, r < R (each load
 // instruction then covers 32 adjacent rows; the backward interleaves its rows,
 // see column_row_slot).
-template <int R>
+template <int R, bool AHEAD>
 __global__ void __launch_bounds__(256, R >= 4 ? 4 : 5) column_forward_kernel(RayParams P,
                                                              const ColumnTrace *__restrict__ T,
                                                              const float *__restrict__ zvol,
@@ -485,7 +564,7 @@ __global__ void __launch_bounds__(256, R >= 4 ? 4 : 5) column_forward_kernel(Ray
         const ColumnTrace C = T[(long long)view * P.n_u + iu];
         if (C.k0 <= C.k1) {
             RowZ Z[R];
-            ColumnGather<R> op;
+            ColumnGather<R, AHEAD> op;
             op.vol = zvol;
             op.lim = (long long)column_padded_cells(P);
 #pragma unroll
@@ -664,8 +743,8 @@ inline int column_rows(const RayParams &P, int requested, int preferred)
 // bwd_adjacent: the 2-row backward covers 32 adjacent rows per instruction
 // instead of interleaving a thread's rows across lanes.
 inline int column_plan_build(const RayParams &P, int rows_fwd, int rows_bwd, bool bwd_adjacent,
-                             ColumnPlan *plan, void **d_columns, float **d_zfwd, float **d_zbwd,
-                             unsigned long long *bytes)
+                             int fwd_ahead, ColumnPlan *plan, void **d_columns, float **d_zfwd,
+                             float **d_zbwd, unsigned long long *bytes)
 {
     if ((long long)P.n_views * P.n_u >= (1LL << 31)) return 11;
     if (column_padded_cells(P) >= (1ULL << 31)) return 11;
@@ -673,6 +752,16 @@ inline int column_plan_build(const RayParams &P, int rows_fwd, int rows_bwd, boo
     plan->rows_fwd = column_rows(P, rows_fwd, 4);
     plan->rows_bwd = column_rows(P, rows_bwd, 2);
     plan->bwd_interleave = !bwd_adjacent;
+    // Loading a slab ahead hides the latency of gathers that miss L2: measured
+    // faster where the working copy is larger than L2 (C4 106.4 -> 104.3 ms,
+    // C5 26.2 -> 26.0 ms) and slower where it fits (C3 10.4 -> 10.9 ms).
+    // fwd_ahead: 0 = by that rule, 1 = never, 2 = always.
+    int dev = 0, l2 = 0;
+    if (fwd_ahead == 0 && (cudaGetDevice(&dev) != cudaSuccess ||
+                           cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess))
+        return 9;
+    plan->fwd_ahead = fwd_ahead == 2 ||
+                      (fwd_ahead == 0 && sizeof(float) * column_padded_cells(P) > (size_t)l2);
     const size_t cbytes = sizeof(ColumnTrace) * (size_t)(plan->n_columns > 0 ? plan->n_columns : 1);
     const size_t vbytes = sizeof(float) * column_padded_cells(P);
     int *d_flag = nullptr;
@@ -724,10 +813,17 @@ inline int column_walk_forward(const RayParams &P, const ColumnPlan &plan, const
     if (P.view_count <= 0) return 0;
     const ColumnTrace *T = (const ColumnTrace *)d_columns;
     const int R = plan.rows_fwd;
-    if (R == 4) column_forward_kernel<4><<<column_grid(P, 4), 256, 0, s>>>(P, T, d_zfwd, sino);
-    else if (R == 3) column_forward_kernel<3><<<column_grid(P, 3), 256, 0, s>>>(P, T, d_zfwd, sino);
-    else if (R == 2) column_forward_kernel<2><<<column_grid(P, 2), 256, 0, s>>>(P, T, d_zfwd, sino);
-    else column_forward_kernel<1><<<column_grid(P, 1), 256, 0, s>>>(P, T, d_zfwd, sino);
+    if (plan.fwd_ahead) {
+        if (R == 4) column_forward_kernel<4, true><<<column_grid(P, 4), 256, 0, s>>>(P, T, d_zfwd, sino);
+        else if (R == 3) column_forward_kernel<3, true><<<column_grid(P, 3), 256, 0, s>>>(P, T, d_zfwd, sino);
+        else if (R == 2) column_forward_kernel<2, true><<<column_grid(P, 2), 256, 0, s>>>(P, T, d_zfwd, sino);
+        else column_forward_kernel<1, true><<<column_grid(P, 1), 256, 0, s>>>(P, T, d_zfwd, sino);
+    } else {
+        if (R == 4) column_forward_kernel<4, false><<<column_grid(P, 4), 256, 0, s>>>(P, T, d_zfwd, sino);
+        else if (R == 3) column_forward_kernel<3, false><<<column_grid(P, 3), 256, 0, s>>>(P, T, d_zfwd, sino);
+        else if (R == 2) column_forward_kernel<2, false><<<column_grid(P, 2), 256, 0, s>>>(P, T, d_zfwd, sino);
+        else column_forward_kernel<1, false><<<column_grid(P, 1), 256, 0, s>>>(P, T, d_zfwd, sino);
+    }
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 

@@ -145,6 +145,10 @@ typedef struct ctp_plan ctp_plan_t;
  *                 of sinogram, at most 8); never more than the views.
  *   geometry_walk ctp_geometry_vjp on column-path plans: 0 = the column walk,
  *                 1 = the ray walk (other plans always take the ray walk).
+ *   forward_ahead column path: the forward loads each row's next cell one slab
+ *                 ahead in the slabs where its warp is inside the grid; 0 = when
+ *                 the padded working copy is larger than the device's L2, 1 =
+ *                 never, 2 = always.
  * Values outside these ranges make ctp_plan_ex return CTP_E_OPTION.
  */
 typedef struct ctp_plan_options {
@@ -154,6 +158,7 @@ typedef struct ctp_plan_options {
     int plane_backward;
     int host_chunks;
     int geometry_walk;
+    int forward_ahead;
 } ctp_plan_options;
 
 typedef struct ctp_plan_info {

@@ -162,9 +162,11 @@ def test_plane_privatised_copies_start_every_call_at_zero(torch, ctp, oracle_mod
 
 @pytest.mark.parametrize("rows", [1, 2, 3, 4])
 @pytest.mark.parametrize("adjacent", [0, 1])
-def test_column_work_layouts_match_oracle(torch, ctp, oracle_mod, rows, adjacent):
-    """Every rows-per-thread choice of the column walks (forward and backward)
-    and both row orders of the 2-row backward compute the same operator."""
+@pytest.mark.parametrize("ahead", ["off", "on"])
+def test_column_work_layouts_match_oracle(torch, ctp, oracle_mod, rows, adjacent, ahead):
+    """Every rows-per-thread choice of the column walks (forward and backward),
+    both row orders of the 2-row backward and the forward with and without its
+    gathers loaded a slab ahead compute the same operator."""
     w = SMALL[3]
     f = ci.frames(w)
     scan = oracle_mod.Scan.from_workload(w, f)
@@ -174,7 +176,7 @@ def test_column_work_layouts_match_oracle(torch, ctp, oracle_mod, rows, adjacent
     y_clean = np.where(amb, np.float32(0), y)
     plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w), "column",
                         options={"rows_forward": rows, "rows_backward": rows,
-                                 "backward_rows_adjacent": adjacent})
+                                 "backward_rows_adjacent": adjacent, "forward_ahead": ahead})
     p, g = _run_pair(torch, ctp, plan, vol, y_clean)
     p_ref = oracle_mod.forward(scan, vol)
     g_ref = oracle_mod.backward(scan, y_clean.ravel())
@@ -184,6 +186,23 @@ def test_column_work_layouts_match_oracle(torch, ctp, oracle_mod, rows, adjacent
     assert max_rel_err(g, g_ref) <= TOL_BACKWARD_MAX
     n_ref = oracle_mod.segment_count(scan)
     assert abs(ctp.ctp_segment_count(plan) - n_ref) <= max(1e-6 * n_ref, 4)
+
+
+@pytest.mark.parametrize("idx", [3, 4, 5])
+def test_forward_ahead_is_bit_identical(torch, ctp, idx):
+    """Loading the gathers a slab ahead changes when the values arrive, not the
+    sums: the column forward with and without it agree bit for bit."""
+    w = SMALL[idx]
+    f = ci.frames(w)
+    vol = torch.from_numpy(ci.phantom(w)).cuda()
+    out = []
+    for ahead in ("off", "on"):
+        plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w), "column",
+                            options={"forward_ahead": ahead})
+        p = torch.empty(plan.sino_shape, device="cuda")
+        ctp.ctp_forward(plan, vol, p)
+        out.append(p.cpu().numpy())
+    assert np.array_equal(out[0], out[1])
 
 
 def test_tilted_2d_frames_fall_back_to_ray_path(torch, ctp, oracle_mod):
