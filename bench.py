@@ -282,7 +282,8 @@ def max_over_ranks(value: float, world: int) -> float:
 def oracle_sample_rate(w, vol, y, budget_s: float = 15.0):
     """The float64 oracle, as it stands, on a bounded sample of the workload:
     forward and backward over the rays of the first m views, m sized so the
-    timed work is about budget_s seconds.  Returns (Gseg/s, sample text, cores)."""
+    timed work is about budget_s seconds.  Returns (Gseg/s of forward +
+    backward, sample text, cores, seconds, {forward / backward Gseg/s})."""
     import oracle
     scan = oracle.Scan.from_workload(w, ci.frames(w))
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
@@ -297,11 +298,15 @@ def oracle_sample_rate(w, vol, y, budget_s: float = 15.0):
     segs = oracle.segment_count(scan, 0, ray1, threads=cores)
     t = time.perf_counter()
     oracle.forward(scan, vol, 0, ray1, threads=cores)
+    t_fwd = time.perf_counter() - t
+    t = time.perf_counter()
     oracle.backward(scan, y[:ray1], 0, ray1, threads=cores)
-    dt = time.perf_counter() - t
+    t_bwd = time.perf_counter() - t
+    dt = t_fwd + t_bwd
     sample = (f"views 0..{m - 1} of {w.n_views} ({ray1} rays, {segs} segments), forward + "
               f"backward, float64 C oracle, {cores} threads, {dt:.1f} s")
-    return 2.0 * segs / dt / 1e9, sample, cores, dt
+    parts = {"forward_gseg_per_s": segs / t_fwd / 1e9, "backward_gseg_per_s": segs / t_bwd / 1e9}
+    return 2.0 * segs / dt / 1e9, sample, cores, dt, parts
 
 
 def run_reference(args, w, world, rank):
@@ -311,7 +316,7 @@ def run_reference(args, w, world, rank):
     y = ci.sinogram_noise(w).ravel()
     rates, samples = [], []
     for step in range(args.warmup + args.steps):
-        rate, sample, cores, dt = oracle_sample_rate(w, vol, y, budget_s=args.ref_budget)
+        rate, sample, cores, dt, parts = oracle_sample_rate(w, vol, y, budget_s=args.ref_budget)
         if step >= args.warmup:
             rates.append(rate)
             samples.append(dt)
@@ -323,7 +328,7 @@ def run_reference(args, w, world, rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "note": "each step is a bounded sample of the workload"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, **parts},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -523,8 +528,10 @@ def run_gpu(args, w, world, rank, local):
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            rate, sample, cores, _ = oracle_sample_rate(w, vol_h, y_h.ravel(), args.ref_budget)
-            cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+            rate, sample, cores, _, parts = oracle_sample_rate(w, vol_h, y_h.ravel(),
+                                                               args.ref_budget)
+            cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                   **parts}
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
