@@ -27,7 +27,11 @@ def test_reference_arm_prints_one_json_line():
     assert len(lines) == 1
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["unit"] == "Gseg/s" and rec["value"] > 0
-    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
+    cpu = rec["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1
+    # the step's rate is the harmonic combination of the forward and backward rates
+    f, b = cpu["forward_gseg_per_s"], cpu["backward_gseg_per_s"]
+    assert abs(2.0 / (1.0 / f + 1.0 / b) - cpu["value"]) <= 1e-9 * cpu["value"]
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["e2e"]["value"] == rec["value"]
     assert rec["config"]["workload"] == "c1_parallel2d_64"
 
