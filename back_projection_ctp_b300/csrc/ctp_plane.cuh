@@ -595,11 +595,14 @@ __global__ void __launch_bounds__(256) plane_backward_tiled_kernel(RayParams P,
     const int s_begin = blockIdx.y * views_per_block;
     const int s_end = min(P.n_views, s_begin + views_per_block);
     // warps take views far apart in angle (warp w: s_begin + w * span + i), so the
-    // concurrently updated cells of the tile differ
+    // concurrently updated cells of the tile differ; a block of fewer than 8
+    // views gives each view 8 / nv warps, which split its rays in runs of 32
     const int nv = s_end - s_begin;
-    const int span = (nv + 7) / 8;
+    const int wpv = nv >= 8 ? 1 : 8 / nv;  // warps per view
+    const int span = wpv == 1 ? (nv + 7) / 8 : 1;
+    const int slice = warp % wpv;
     for (int i = 0; i < span; ++i) {
-        const int s = s_begin + warp * span + i;
+        const int s = s_begin + (wpv == 1 ? warp * span + i : warp / wpv);
         if (s >= s_end) break;
         const ViewFrame &V = P.views[s];
         // candidate rays: projections of the tile's corners (cell coordinates)
@@ -619,7 +622,7 @@ __global__ void __launch_bounds__(256) plane_backward_tiled_kernel(RayParams P,
             u0 = max(0, (int)floorf(umin) - 1);
             u1 = min(P.n_u - 1, (int)ceilf(umax) + 1);
         }
-        for (int iu = u0 + lane; iu <= u1; iu += 32) {
+        for (int iu = u0 + 32 * slice + lane; iu <= u1; iu += 32 * wpv) {
             const long long ray = (long long)s * P.n_u + iu;
             if (!ctp_in(ray, sino_cells(P), kSitePlaneSinoLoad)) continue;
             const float y = sino[ray];
@@ -817,9 +820,14 @@ inline int plane_backward_whole(const RayParams &P, const void *d_rays, const fl
     if (cudaMemsetAsync(img, 0, sizeof(float) * (size_t)P.n[0] * P.n[1], s) != cudaSuccess)
         return 9;
     if ((long long)P.n_views * P.n_u == 0) return 0;
+    // view groups: enough blocks for about four per SM, down to one view per
+    // block on small images (C1 with one warp per view: 1 / 2 / 4 / 8 views per
+    // block 16.5 / 16.9 / 17.1 / 19.1 us per call, the extra tile flushes
+    // cheaper than serial views; 12.1 us with a view's rays split over the
+    // block's 8 warps)
     const int tiles = ((P.n[0] + kTile - 1) / kTile) * ((P.n[1] + kTile - 1) / kTile);
     int groups = (4 * 148 + tiles - 1) / tiles;
-    groups = max(1, min(groups, (P.n_views + 7) / 8));
+    groups = max(1, min(groups, P.n_views));
     const int vpb = (P.n_views + groups - 1) / groups;
     groups = (P.n_views + vpb - 1) / vpb;
     plane_backward_tiled_kernel<<<dim3(tiles, groups), 256, 0, s>>>(
