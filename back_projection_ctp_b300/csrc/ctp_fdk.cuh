@@ -258,6 +258,10 @@ __global__ void __launch_bounds__(256, K > 1 ? 5 : 8) wbp_gather_kernel(FdkParam
 #pragma unroll
     for (int t = 0; t < K; ++t) acc[t] = 0.0f;
     const long long plane = (long long)F.n_u * F.n_v;
+    // two views per iteration: the second view's set-up chain overlaps the
+    // first's (C3 / C4 / C5 gather 6-7 % faster; the same for the transpose
+    // measured no faster)
+#pragma unroll 2
     for (int s = 0; s < F.n_views; ++s) {
         ColumnView C;
         if (!fdk_column_view(F, F.views[s], i, j, k0, C)) continue;
