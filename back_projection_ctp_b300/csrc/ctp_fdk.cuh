@@ -246,8 +246,11 @@ __device__ __forceinline__ void store_column(const FdkParams &F, int i, int j, i
 
 // One thread per (x, y) column and K consecutive z; blocks of 32 x 8 columns;
 // stencil values straight from global memory (2-D scans, and a tuning override).
+// 3-D: 4 blocks per SM (64 registers) with the view loop unrolled by two; 5
+// blocks (48 registers, spilling) measured C3 8.61 / C4 101.2 / C5 55.2 ms
+// against 8.14 / 97.2 / 57.3.
 template <int K>
-__global__ void __launch_bounds__(256, K > 1 ? 5 : 8) wbp_gather_kernel(FdkParams F, const float *__restrict__ q,
+__global__ void __launch_bounds__(256, K > 1 ? 4 : 8) wbp_gather_kernel(FdkParams F, const float *__restrict__ q,
                                                          float *__restrict__ vol)
 {
     int i, j;
