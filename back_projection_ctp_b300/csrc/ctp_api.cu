@@ -56,6 +56,7 @@ struct ctp_plan {
     ctp::FdkParams fdk{};
     ctp::FdkView *d_fdk = nullptr;
     float *d_ramp[ctp::kRampKinds] = {};    // ramp kernels (2 n_u - 1) by ctp_ramp value
+    bool ramp_odd[ctp::kRampKinds] = {};    // even nonzero taps all zero (Ram-Lak)
     unsigned long long device_bytes = 0;
     ctp_plan_options opt{};                 // work-layout options (all zero: defaults)
 };
@@ -330,6 +331,7 @@ int fdk_setup(ctp_plan_t *p, const ctp_geometry *g, const ctp_volume *v)
         for (int kind = 0; kind < ctp::kRampKinds; ++kind) {
             std::vector<float> h;
             ctp::fdk_ramp_kernel(g->n_u, g->pitch_u, kind, h);
+            p->ramp_odd[kind] = ctp::ramp_taps_odd(h, g->n_u);
             const size_t hb = sizeof(float) * h.size();
             if (cudaMalloc(&p->d_ramp[kind], hb) != cudaSuccess ||
                 cudaMemcpy(p->d_ramp[kind], h.data(), hb, cudaMemcpyHostToDevice) != cudaSuccess)
@@ -880,7 +882,8 @@ int ctp_ramp_filter(const ctp_plan_t *plan, const float *sino_dev, float *out_de
     int st = fdk_check(plan);
     if (st != CTP_OK) return st;
     if (!plan->d_ramp[ramp]) return CTP_E_LIMIT;
-    return ctp::fdk_filter(plan->fdk, plan->d_ramp[ramp], sino_dev, out_dev, view_weight_dev,
+    return ctp::fdk_filter(plan->fdk, plan->d_ramp[ramp], plan->ramp_odd[ramp], sino_dev, out_dev,
+                           view_weight_dev,
                            pixel_weight_dev, transpose ? 1 : 0, (cudaStream_t)stream)
                ? CTP_E_CUDA : CTP_OK;
 }

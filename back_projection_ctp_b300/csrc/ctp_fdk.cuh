@@ -379,7 +379,7 @@ __device__ __forceinline__ float fdk_cosine(const FdkParams &F, const FdkView &V
 // the kernel h; each thread forms 4 outputs (stride blockDim) of every row, so
 // per input sample it issues RB + 4 shared loads (the row values are warp
 // broadcasts, the kernel values consecutive) for 4 RB fused multiply-adds.
-template <int RB>
+template <int RB, bool ODD>
 __global__ void ramp_filter_kernel(FdkParams F, const float *__restrict__ h,
                                    const float *__restrict__ x, float *__restrict__ out,
                                    const float *__restrict__ view_weight,
@@ -420,7 +420,10 @@ __global__ void ramp_filter_kernel(FdkParams F, const float *__restrict__ h,
         int hoff[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) hoff[m] = min(i0 + m * T, nu - 1) + nu - 1;
-        for (int jj = 0; jj < nu; ++jj) {
+        // ODD: every even nonzero tap is zero (Ram-Lak).  A thread's outputs
+        // i0 + m T share i0's parity (T is a multiple of 32), so only inputs of
+        // the other parity meet nonzero taps; the centre tap is added last.
+        for (int jj = ODD ? ((i0 & 1) ^ 1) : 0; jj < nu; jj += ODD ? 2 : 1) {
             float hv[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) hv[m] = hs[hoff[m] - jj];
@@ -429,6 +432,16 @@ __global__ void ramp_filter_kernel(FdkParams F, const float *__restrict__ h,
                 const float xv = xs[r * nu + jj];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) acc[r][m] = __fmaf_rn(hv[m], xv, acc[r][m]);
+            }
+        }
+        if (ODD) {
+            const float h0 = hs[nu - 1];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int i = i0 + m * T;
+                if (i >= nu) continue;
+#pragma unroll
+                for (int r = 0; r < RB; ++r) acc[r][m] = __fmaf_rn(h0, xs[r * nu + i], acc[r][m]);
             }
         }
 #pragma unroll
@@ -635,7 +648,10 @@ inline void fdk_ramp_kernel(int n, double tau, int kind, std::vector<float> &h)
         const double m = (double)(t - (n - 1));
         double v;
         switch (kind) {
-        case 0: v = fdk_band_ramp(m, tau); break;
+        // the band-limited ramp is exactly zero at even nonzero offsets (sin and
+        // cos - 1 of an even multiple of pi); its float64 evaluation leaves
+        // ~1e-17 there, so those samples are set to zero directly
+        case 0: v = (t - (n - 1)) % 2 == 0 && t != n - 1 ? 0.0 : fdk_band_ramp(m, tau); break;
         case 1: v = -4.0 / (kPi * tau * tau * (4.0 * m * m - 1.0)); break;
         case 2: v = 0.5 * (fdk_band_ramp(m - 0.5, tau) + fdk_band_ramp(m + 0.5, tau)); break;
         case 3:
@@ -686,7 +702,7 @@ inline int fdk_scatter(const FdkParams &F, const float *vol, float *q, cudaStrea
 // Largest detector row this filter takes (shared memory: one row and the kernel).
 constexpr int kFilterMaxU = 16384;
 
-template <int RB>
+template <int RB, bool ODD>
 inline int ramp_launch(const FdkParams &F, const float *h, const float *x, float *out,
                        const float *view_weight, const float *pixel_weight, int transpose,
                        cudaStream_t s)
@@ -694,31 +710,49 @@ inline int ramp_launch(const FdkParams &F, const float *h, const float *x, float
     const long long rows = (long long)F.n_views * F.n_v;
     const size_t smem = sizeof(float) * ((size_t)RB * F.n_u + 2 * (size_t)F.n_u);
     if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(ramp_filter_kernel<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(ramp_filter_kernel<RB, ODD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return 9;
     int threads = (F.n_u + 3) / 4;
     threads = ((threads + 31) / 32) * 32;
     threads = threads < 32 ? 32 : (threads > 256 ? 256 : threads);
     const long long blocks = (rows + RB - 1) / RB;
-    ramp_filter_kernel<RB><<<(unsigned)blocks, threads, smem, s>>>(F, h, x, out, view_weight,
-                                                                   pixel_weight, transpose, rows);
+    ramp_filter_kernel<RB, ODD><<<(unsigned)blocks, threads, smem, s>>>(
+        F, h, x, out, view_weight, pixel_weight, transpose, rows);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 
-inline int fdk_filter(const FdkParams &F, const float *h, const float *x, float *out,
+template <bool ODD>
+inline int fdk_filter_rows(const FdkParams &F, const float *h, const float *x, float *out,
+                           const float *vw, const float *pw, int transpose, cudaStream_t s)
+{
+    // rows per block: as many as fit 48 KB of shared memory, at most 8
+    const size_t per_row = sizeof(float) * (size_t)F.n_u;
+    const size_t hbytes = 2 * per_row;
+    if (hbytes + 8 * per_row <= 48 * 1024) return ramp_launch<8, ODD>(F, h, x, out, vw, pw, transpose, s);
+    if (hbytes + 4 * per_row <= 48 * 1024) return ramp_launch<4, ODD>(F, h, x, out, vw, pw, transpose, s);
+    if (hbytes + 2 * per_row <= 48 * 1024) return ramp_launch<2, ODD>(F, h, x, out, vw, pw, transpose, s);
+    return ramp_launch<1, ODD>(F, h, x, out, vw, pw, transpose, s);
+}
+
+// odd: every even nonzero tap of h is zero (ramp_taps_odd), so the filter skips
+// them (C4 Ram-Lak filter about half the time).
+inline int fdk_filter(const FdkParams &F, const float *h, bool odd, const float *x, float *out,
                       const float *view_weight, const float *pixel_weight, int transpose,
                       cudaStream_t s)
 {
     if ((long long)F.n_views * F.n_v == 0) return 0;
-    // rows per block: as many as fit 48 KB of shared memory, at most 8
-    const size_t per_row = sizeof(float) * (size_t)F.n_u;
-    const size_t hbytes = 2 * per_row;
-    const float *vw = view_weight, *pw = pixel_weight;
-    if (hbytes + 8 * per_row <= 48 * 1024) return ramp_launch<8>(F, h, x, out, vw, pw, transpose, s);
-    if (hbytes + 4 * per_row <= 48 * 1024) return ramp_launch<4>(F, h, x, out, vw, pw, transpose, s);
-    if (hbytes + 2 * per_row <= 48 * 1024) return ramp_launch<2>(F, h, x, out, vw, pw, transpose, s);
-    return ramp_launch<1>(F, h, x, out, vw, pw, transpose, s);
+    return odd ? fdk_filter_rows<true>(F, h, x, out, view_weight, pixel_weight, transpose, s)
+               : fdk_filter_rows<false>(F, h, x, out, view_weight, pixel_weight, transpose, s);
+}
+
+// True when every tap of h (2 n - 1 taps, centre n - 1) at an even nonzero
+// offset is exactly zero.
+inline bool ramp_taps_odd(const std::vector<float> &h, int n)
+{
+    for (int t = 0; t < 2 * n - 1; ++t)
+        if ((t - (n - 1)) % 2 == 0 && t != n - 1 && h[t] != 0.0f) return false;
+    return true;
 }
 
 // Parker's short-scan weights (Parker 1982) of a circular divergent scan about
