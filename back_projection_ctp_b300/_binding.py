@@ -52,7 +52,7 @@ class _PlanOptions(ctypes.Structure):
     _fields_ = [("rows_forward", ctypes.c_int), ("rows_backward", ctypes.c_int),
                 ("backward_rows_adjacent", ctypes.c_int), ("plane_backward", ctypes.c_int),
                 ("host_chunks", ctypes.c_int), ("geometry_walk", ctypes.c_int),
-                ("forward_ahead", ctypes.c_int)]
+                ("forward_ahead", ctypes.c_int), ("forward_views_first", ctypes.c_int)]
 
 
 # Work-layout options of a plan (include/ctp.h, ctp_plan_options); keyword values
@@ -60,6 +60,7 @@ class _PlanOptions(ctypes.Structure):
 PLANE_BACKWARD = {"auto": 0, "tiled": 1, "privatised": 2}
 GEOMETRY_WALK = {"auto": 0, "ray": 1}
 FORWARD_AHEAD = {"auto": 0, "off": 1, "on": 2}
+FORWARD_VIEWS_FIRST = {"auto": 0, "off": 1, "on": 2}
 
 
 def _plan_options(options):
@@ -73,6 +74,8 @@ def _plan_options(options):
             value = GEOMETRY_WALK[value] if isinstance(value, str) else value
         elif key == "forward_ahead":
             value = FORWARD_AHEAD[value] if isinstance(value, str) else value
+        elif key == "forward_views_first":
+            value = FORWARD_VIEWS_FIRST[value] if isinstance(value, str) else value
         elif key not in ("rows_forward", "rows_backward", "backward_rows_adjacent",
                          "host_chunks"):
             raise ValueError(f"unknown plan option {key!r}")

@@ -400,7 +400,8 @@ int validate_options(const ctp_plan_options *o)
                     (o->backward_rows_adjacent == 0 || o->backward_rows_adjacent == 1) &&
                     o->plane_backward >= 0 && o->plane_backward <= 2 && o->host_chunks >= 0 &&
                     o->host_chunks <= 64 && (o->geometry_walk == 0 || o->geometry_walk == 1) &&
-                    o->forward_ahead >= 0 && o->forward_ahead <= 2;
+                    o->forward_ahead >= 0 && o->forward_ahead <= 2 &&
+                    o->forward_views_first >= 0 && o->forward_views_first <= 2;
     return ok ? CTP_OK : CTP_E_OPTION;
 }
 
@@ -600,10 +601,17 @@ int ctp_plan_ex(const ctp_geometry *geom, const ctp_volume *vol, int path,
         }
     }
     if (chosen == CTP_PATH_COLUMN || chosen == CTP_PATH_PLANE) {
+        // every view's source and detector centre at one height (a circular
+        // scan): then views first for the column forward's blocks
+        bool level = true;
+        for (int v = 1; v < p->n_views && level; ++v)
+            level = p->raw[12 * (size_t)v + 2] == p->raw[2] && p->raw[12 * (size_t)v + 5] == p->raw[5];
+        const int views_first = p->opt.forward_views_first == 0 ? (level ? 2 : 1)
+                                                                 : p->opt.forward_views_first;
         if (chosen == CTP_PATH_COLUMN)
             st = ctp::column_plan_build(ray_params(p), p->opt.rows_forward, p->opt.rows_backward,
                                         p->opt.backward_rows_adjacent != 0,
-                                        p->opt.forward_ahead, &p->col,
+                                        p->opt.forward_ahead, views_first == 2, &p->col,
                                         &p->d_table, &p->d_work_fwd,
                                         &p->d_work_bwd, &p->device_bytes);
         else

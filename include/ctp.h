@@ -149,6 +149,11 @@ typedef struct ctp_plan ctp_plan_t;
  *                 ahead in the slabs where its warp is inside the grid; 0 = when
  *                 the padded working copy is larger than the device's L2, 1 =
  *                 never, 2 = always.
+ *   forward_views_first  column path: the forward's blocks run views before
+ *                 detector columns (the resident blocks then hold few columns
+ *                 at many angles, a thin shell of the volume); 0 = when every
+ *                 view's source and detector centre lie at one height (circular
+ *                 scans), 1 = never, 2 = always.
  * Values outside these ranges make ctp_plan_ex return CTP_E_OPTION.
  */
 typedef struct ctp_plan_options {
@@ -159,6 +164,7 @@ typedef struct ctp_plan_options {
     int host_chunks;
     int geometry_walk;
     int forward_ahead;
+    int forward_views_first;
 } ctp_plan_options;
 
 typedef struct ctp_plan_info {

@@ -115,6 +115,7 @@ def test_shape_and_option_errors():
 @pytest.mark.parametrize("options", [
     {"rows_forward": 5}, {"rows_backward": -1}, {"backward_rows_adjacent": 2},
     {"plane_backward": 3}, {"host_chunks": 65}, {"geometry_walk": 2}, {"forward_ahead": 3},
+    {"forward_views_first": -1},
 ])
 def test_plan_options_out_of_range_are_rejected_on_the_host(options):
     """ctp_plan_ex checks its work-layout options before any CUDA call."""

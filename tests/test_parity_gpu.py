@@ -210,20 +210,23 @@ def test_column_work_layouts_match_oracle(torch, ctp, oracle_mod, rows, adjacent
 
 
 @pytest.mark.parametrize("idx", [3, 4, 5])
-def test_forward_ahead_is_bit_identical(torch, ctp, idx):
-    """Loading the gathers a slab ahead changes when the values arrive, not the
-    sums: the column forward with and without it agree bit for bit."""
+def test_forward_ahead_and_order_are_bit_identical(torch, ctp, idx):
+    """Loading the gathers a slab ahead and running the blocks views first change
+    when values arrive and which blocks run together, not the sums: the column
+    forward agrees bit for bit in all four combinations."""
     w = SMALL[idx]
     f = ci.frames(w)
     vol = torch.from_numpy(ci.phantom(w)).cuda()
     out = []
     for ahead in ("off", "on"):
-        plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w), "column",
-                            options={"forward_ahead": ahead})
-        p = torch.empty(plan.sino_shape, device="cuda")
-        ctp.ctp_forward(plan, vol, p)
-        out.append(p.cpu().numpy())
-    assert np.array_equal(out[0], out[1])
+        for first in ("off", "on"):
+            plan = ctp.ctp_plan(geometry_of(w, f), volume_of(w), "column",
+                                options={"forward_ahead": ahead, "forward_views_first": first})
+            p = torch.empty(plan.sino_shape, device="cuda")
+            ctp.ctp_forward(plan, vol, p)
+            out.append(p.cpu().numpy())
+    for o in out[1:]:
+        assert np.array_equal(out[0], o)
 
 
 def test_tilted_2d_frames_fall_back_to_ray_path(torch, ctp, oracle_mod):
