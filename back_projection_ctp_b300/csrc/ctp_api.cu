@@ -948,7 +948,8 @@ int ctp_geometry_vjp(const ctp_plan_t *plan, const float *vol_dev, const float *
         // the column walk reads the plan's padded z-fastest working copy
         if ((st = forward_in(plan, vol_dev, s)) != CTP_OK) return st;
         return ctp::column_geometry_vjp(ray_params(plan), Q, (const ctp::ColumnTrace *)plan->d_table,
-                                        plan->d_work_fwd, weight_dev, grad_dev, s)
+                                        plan->d_work_fwd, weight_dev, grad_dev,
+                                        plan->col.fwd_views_first, s)
                    ? CTP_E_CUDA : CTP_OK;
     }
     return ctp::geometry_vjp(ray_params(plan), Q, vol_dev, weight_dev, grad_dev, s) ? CTP_E_CUDA

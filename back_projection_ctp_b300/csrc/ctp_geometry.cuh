@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(TU *TV) geometry_vjp_kernel(RayParams P, GeomP
 // uniform across the warp) and each row's own z crossings, on the padded
 // z-fastest working copy of the volume (zero halo in x and y; z validity per
 // access).  t of the p coordinate is shared by the column's rows.
-template <int R>
+template <int R, bool VF>
 __global__ void __launch_bounds__(256, 4) column_gvjp_kernel(RayParams P, GeomParams Q,
                                                           const ColumnTrace *__restrict__ T,
                                                           const float *__restrict__ zvol,
@@ -333,8 +333,9 @@ __global__ void __launch_bounds__(256, 4) column_gvjp_kernel(RayParams P, GeomPa
 {
     __shared__ float part[kColumnsPerBlock][12];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int iu = blockIdx.x * kColumnsPerBlock + warp;
-    const int view = P.view0 + (int)blockIdx.y;
+    // VF: grid (views, column groups, row bands), as the column forward's
+    const int iu = (VF ? (int)blockIdx.y : (int)blockIdx.x) * kColumnsPerBlock + warp;
+    const int view = P.view0 + (int)(VF ? blockIdx.x : blockIdx.y);
     float g[12];
 #pragma unroll
     for (int m = 0; m < 12; ++m) g[m] = 0.0f;
@@ -527,14 +528,21 @@ __global__ void __launch_bounds__(256, 4) column_gvjp_kernel(RayParams P, GeomPa
     }
 }
 
+// views_first: the plan's forward block order (circular scans), whose resident
+// blocks then read a thin shell of the volume that L2 holds.
 inline int column_geometry_vjp(const RayParams &P, const GeomParams &Q, const ColumnTrace *T,
-                               const float *zvol, const float *w, double *out, cudaStream_t s)
+                               const float *zvol, const float *w, double *out, bool views_first,
+                               cudaStream_t s)
 {
     if (cudaMemsetAsync(out, 0, sizeof(double) * 12 * (size_t)(P.n_views > 0 ? P.n_views : 0), s) !=
         cudaSuccess)
         return 9;
     if (P.view_count <= 0) return 0;
-    column_gvjp_kernel<2><<<column_grid(P, 2), 256, 0, s>>>(P, Q, T, zvol, w, out);
+    if (views_first)
+        column_gvjp_kernel<2, true><<<column_grid_views_first(P, 2), 256, 0, s>>>(P, Q, T, zvol, w,
+                                                                                 out);
+    else
+        column_gvjp_kernel<2, false><<<column_grid(P, 2), 256, 0, s>>>(P, Q, T, zvol, w, out);
     return cudaGetLastError() == cudaSuccess ? 0 : 9;
 }
 

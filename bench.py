@@ -850,7 +850,8 @@ def run_geometry(args, w, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     frames = ci.frames(w)
-    plan = ctp.ctp_plan(geometry_of(w, frames), volume_of(w), args.path)
+    plan = ctp.ctp_plan(geometry_of(w, frames), volume_of(w), args.path,
+                        options=args.plan_options)
     segments = golden_segments(args.config) if args.views is None else ctp.ctp_segment_count(plan)
     stream = torch.cuda.current_stream(dev)
     d_vol = torch.from_numpy(ci.phantom(w)).to(dev)
