@@ -766,15 +766,18 @@ inline int column_plan_build(const RayParams &P, int rows_fwd, int rows_bwd, boo
     // (C4 159.3 -> 169.5 ms).
     plan->fwd_views_first = fwd_views_first;
     // Loading a slab ahead hides the latency of gathers that miss L2: measured
-    // faster where the working copy is larger than L2 (C4 106.4 -> 104.3 ms,
-    // C5 26.2 -> 26.0 ms) and slower where it fits (C3 10.4 -> 10.9 ms).
-    // fwd_ahead: 0 = by that rule, 1 = never, 2 = always.
+    // faster where the blocks run columns first over a working copy larger
+    // than L2 (C5 26.2 -> 26.0 ms; C4 106.4 -> 104.3 ms in that order) and
+    // slower where the reads stay in L2: a copy that fits (C3 10.4 -> 10.9 ms)
+    // or the views-first order (C4 93.3 -> 99.4 ms).  fwd_ahead: 0 = by that
+    // rule, 1 = never, 2 = always.
     int dev = 0, l2 = 0;
     if (fwd_ahead == 0 && (cudaGetDevice(&dev) != cudaSuccess ||
                            cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess))
         return 9;
     plan->fwd_ahead = fwd_ahead == 2 ||
-                      (fwd_ahead == 0 && sizeof(float) * column_padded_cells(P) > (size_t)l2);
+                      (fwd_ahead == 0 && !fwd_views_first &&
+                       sizeof(float) * column_padded_cells(P) > (size_t)l2);
     const size_t cbytes = sizeof(ColumnTrace) * (size_t)(plan->n_columns > 0 ? plan->n_columns : 1);
     const size_t vbytes = sizeof(float) * column_padded_cells(P);
     int *d_flag = nullptr;

@@ -147,7 +147,8 @@ typedef struct ctp_plan ctp_plan_t;
  *                 1 = the ray walk (other plans always take the ray walk).
  *   forward_ahead column path: the forward loads each row's next cell one slab
  *                 ahead in the slabs where its warp is inside the grid; 0 = when
- *                 the padded working copy is larger than the device's L2, 1 =
+ *                 its blocks run columns first (forward_views_first) and the
+ *                 padded working copy is larger than the device's L2, 1 =
  *                 never, 2 = always.
  *   forward_views_first  column path: the forward's blocks run views before
  *                 detector columns (the resident blocks then hold few columns
