@@ -150,11 +150,12 @@ typedef struct ctp_plan ctp_plan_t;
  *                 its blocks run columns first (forward_views_first) and the
  *                 padded working copy is larger than the device's L2, 1 =
  *                 never, 2 = always.
- *   forward_views_first  column path: the forward's blocks run views before
- *                 detector columns (the resident blocks then hold few columns
- *                 at many angles, a thin shell of the volume); 0 = when every
- *                 view's source and detector centre lie at one height (circular
- *                 scans), 1 = never, 2 = always.
+ *   forward_views_first  column path: the blocks of the forward (and of the
+ *                 column geometry walk) run views before detector columns (the
+ *                 resident blocks then hold few columns at many angles, a thin
+ *                 shell of the volume); 0 = when every view's source and
+ *                 detector centre lie at one height (circular scans), 1 =
+ *                 never, 2 = always.
  * Values outside these ranges make ctp_plan_ex return CTP_E_OPTION.
  */
 typedef struct ctp_plan_options {
